@@ -1,0 +1,172 @@
+/*
+ * dg.h - C ABI of the GB300 (sm_103a) blockwise-scaled FP8 grouped-GEMM library (libdg.so).
+ *
+ * The library computes the data-parallel hot path of FP8 Mixture-of-Experts layers as they
+ * are described on three DeepGEMM issue/PR pages:
+ *   [P1] "Non-deterministic numerical problem of k_grouped_fp8_gemm_nt_contiguous" (#365):
+ *        the per-channel cast listing, the K-major per-expert pack, the k-grouped wgrad call
+ *        k_grouped_fp8_gemm_nt_contiguous(a, b, d, ks, ks_tensor, c, recipe=(1,1,128)).
+ *   [P2] "Fix cross-expert output overwrites in SM90 masked GEMM" (#469): the masked call
+ *        m_grouped_*_gemm_nt_masked(a, b, d, masked_m, expected_m) and its output boundary.
+ *   [P3] "SM120 m_grouped_fp8 contiguous kernel: illegal memory access at CUDA graph replay"
+ *        (#444): the m-grouped contiguous call routed by m_indices, UE8M0 scale factors, and
+ *        graph replay with a changed expert distribution.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.  The
+ *     library allocates nothing, never copies device data to the host and never
+ *     synchronises: each call only enqueues kernels on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Calls are therefore capturable into CUDA graphs, and a
+ *     captured call re-reads m_indices / counts / ks from device memory on every replay.
+ *   - Return value: DG_OK, or an error code with nothing enqueued.  dg_last_error() gives a
+ *     message for the calling thread's most recent failure.
+ *   - `status` (optional, may be NULL): a caller-owned device int32.  Kernels OR DG_STATUS_*
+ *     bits into it when they meet bad device-side data (an m_indices value outside [-1, G),
+ *     count > cap, K_e not a multiple of 128, ks overflowing K_cap, a wait that timed out);
+ *     the offending work is skipped.  Kernels never trap.  The caller clears it.
+ *   - Alignment: buffers read or written by TMA (fp8 operands, outputs, C) must be 16-byte
+ *     aligned; N, K (and H) must be multiples of 128.
+ *   - e4m3 = OCP FP8 E4M3FN (max 448).  bf16 buffers are passed as `const void*`.
+ *   - Scale factors: DG_SF_FP32 = fp32 values; DG_SF_UE8M0 = one byte per scale, value
+ *     2^(byte-127).
+ *
+ * Scale-factor layouts (all row-major in the order written)
+ *   sfa, per-token 1x128 (MN-major, "column-major TMA-aligned"): [K/128][Mp] where
+ *        Mp = round_up(M, 4) for fp32, round_up(M, 16) for UE8M0 bytes; element (kb, m).
+ *   sfb, per-128x128 block: [G][N/128][K/128].
+ *   sf, per-channel over 128 tokens ([P1] `sf.T` is a view of this): [K_cap/128][C].
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum dg_result { DG_OK = 0, DG_ERR_INVALID_ARG = 1, DG_ERR_UNSUPPORTED = 2, DG_ERR_CUDA = 3 };
+enum dg_sf_format { DG_SF_FP32 = 0, DG_SF_UE8M0 = 1 };
+enum dg_out_dtype { DG_OUT_BF16 = 0, DG_OUT_FP32 = 1 };
+enum dg_status_bits {
+    DG_STATUS_BAD_INDEX = 1,     /* m_indices outside [-1, G), or a row of another expert in a block */
+    DG_STATUS_COUNT_GT_CAP = 2,  /* masked count > cap (clamped to cap) or < 0 (taken as 0) */
+    DG_STATUS_K_NOT_ALIGNED = 4, /* some K_e < 0 or not a multiple of 128 */
+    DG_STATUS_K_OVERFLOW = 8,    /* prefix of ks runs past K_cap */
+    DG_STATUS_TIMEOUT = 16,      /* a bounded wait inside a kernel gave up */
+    DG_STATUS_TOO_MANY_RUNS = 32 /* contiguous layout has more expert segments than supported */
+};
+enum dg_op { DG_OP_M_GROUPED_CONTIGUOUS = 0, DG_OP_M_GROUPED_MASKED = 1, DG_OP_K_GROUPED_WGRAD = 2 };
+
+/* Largest supported values (DG_ERR_UNSUPPORTED beyond them). */
+#define DG_MAX_GROUPS 1024          /* G for every grouped call */
+#define DG_MAX_M_BLOCKS 4096        /* ceil(M/128) for the contiguous call: M <= 524288 */
+
+/* Message describing the calling thread's most recent error ("" if none). */
+const char* dg_last_error(void);
+
+/* Bytes of device workspace `op` needs (0 if none).  The workspace must be 128-byte aligned
+ * and must not be used by two calls that may run at the same time. */
+size_t dg_workspace_size(int op, int G, int64_t M, int64_t N, int64_t K);
+
+/*
+ * 1x128 per-token cast ([P2] "1d" activation scales of sm90_fp8_gemm_1d2d; [P3] "activations
+ * quantized with column-major TMA-aligned packed scales").  For every row m < M and K block
+ * kb: amax = max |x[m, kb*128 : kb*128+128]| (fp32), sf = amax / 448, sf == 0 -> sf_zero,
+ * sf = max(sf, 1e-30) ([P1] per-channel listing, same rules taken along K); for UE8M0 sf is
+ * rounded up to a power of two.  q = e4m3_rne_satfinite(x * (1/sf)) with an fp32 reciprocal
+ * and an fp32 product.
+ *   x:  bf16 [M, K], row stride ldx elements (ldx >= K, ldx*2 a multiple of 16).
+ *   q:  e4m3 [M, K], row stride K.   sfa: see "Scale-factor layouts" (per sf_format).
+ *   row_counts: optional int32 [G]; when given, the M rows form G groups of M/G rows (the
+ *     masked [G, cap, K] activation) and only rows r < clamp(row_counts[g], 0, M/G) are read
+ *     and written, so padding rows cost no traffic.  G is ignored when row_counts is NULL.
+ */
+int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                             void* sfa, int sf_format, float sf_zero, const int32_t* row_counts,
+                             int G, void* stream);
+
+/*
+ * Per-channel cast over 128-token blocks with the per-expert K-major pack ([P1] repro:
+ * `_per_channel_cast_to_fp8(x, gran_k=128, sf_val)` then `_pack_kmajor`).  For every
+ * 128-token block tb inside sum(ks) and every column c: amax over the 128 tokens, then the
+ * scale and code rules of dg_quant_per_token_1x128 (fp32 scales only).
+ *   x:  bf16 [K_cap, C] token-major (row stride C); rows at or past sum(ks) are not read.
+ *   ks: int32 [G] device token counts per expert, each a multiple of 128, sum <= K_cap.
+ *   q_packed: e4m3, expert e's codes transposed into a [C, K_e] row-major block at element
+ *     offset prefix_e * C (prefix_e = ks[0] + ... + ks[e-1]).
+ *   sf: fp32 [K_cap/128][C].
+ * Bad ks set DG_STATUS_K_NOT_ALIGNED / DG_STATUS_K_OVERFLOW and stop the walk over experts at
+ * the first bad one (later experts are not written).
+ */
+int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C, const int32_t* ks, int G,
+                             uint8_t* q_packed, float* sf, float sf_zero, int32_t* status,
+                             void* stream);
+
+/*
+ * 128x128 per-block cast of expert weights ([P2] "2d" weight scales of sm90_fp8_gemm_1d2d;
+ * [P3] "weights requantized to 2^k scales" for UE8M0).  amax over each 128x128 block, then
+ * the rules of dg_quant_per_token_1x128.
+ *   w: bf16 [G, N, K].  q: e4m3 [G, N, K].  sfb: [G][N/128][K/128] fp32 or UE8M0 bytes.
+ */
+int dg_quant_block_128x128(const void* w, int G, int64_t N, int64_t K, uint8_t* q, void* sfb,
+                           int sf_format, float sf_zero, void* stream);
+
+/*
+ * m-grouped contiguous FP8 GEMM ([P3] m_grouped_fp8_fp4_gemm_nt_contiguous, FP8 operands):
+ *   D[m, n] = sum_k A[m, k] sfa[k/128, m] * B[e, n, k] sfb[e, n/128, k/128],  e = m_indices[m]
+ * for rows with e >= 0; rows with m_indices = -1 are never written.  Expert segments are
+ * aligned to 128 rows: the expert of 128-row block b is m_indices[128 b]; a block whose first
+ * row is -1 is padding and skipped; inside a block, rows whose index differs from the block's
+ * expert are not written (DG_STATUS_BAD_INDEX if it is another valid expert).
+ *   a: e4m3 [M, K].  b: e4m3 [G, N, K].  d: [M, N] bf16 or fp32 (out_dtype).
+ *   sfa: [K/128][Mp] (per sf_format), sfb: [G][N/128][K/128] (same sf_format).
+ *   m_indices: int32 [M] device.  Accumulation is fp32 in tensor memory, promoted per 128-K
+ *   block; results are bitwise reproducible run to run.
+ */
+int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b,
+                                const void* sfb, void* d, int out_dtype, const int32_t* m_indices,
+                                int64_t M, int G, int64_t N, int64_t K, int sf_format,
+                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                void* stream);
+
+/*
+ * m-grouped masked FP8 GEMM ([P2] m_grouped_*_gemm_nt_masked(a, b, d, masked_m, expected_m)):
+ *   D[g, r, n] = sum_k A[g, r, k] sfa[k/128, g*cap + r] * B[g, n, k] sfb[g, n/128, k/128]
+ * for r < min(counts[g], cap).  Rows at or past the count are never written: the output is
+ * kept per expert as a 3-D [G, cap, N] tensor (the fix of [P2]), so no tile can reach the
+ * next expert's rows, and rows in [count, cap) inside a tile are not stored either.
+ *   a: e4m3 [G, cap, K].  b: e4m3 [G, N, K].  d: [G, cap, N] bf16 or fp32.
+ *   sfa: [K/128][Mp] with M = G*cap.  counts: int32 [G] device.
+ *   expected_m: a hint only; it never changes the result.
+ */
+int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
+                            void* d, int out_dtype, const int32_t* counts, int G, int64_t cap,
+                            int64_t N, int64_t K, int expected_m, int sf_format, void* workspace,
+                            size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * k-grouped FP8 weight-gradient GEMM ([P1] k_grouped_fp8_gemm_nt_contiguous with
+ * recipe (1, 1, 128)): for each expert e with token span [o_e, o_e + K_e) along K,
+ *   D_e[n, h] = C_e[n, h] + sum_{t < K_e} A_e[n, t] sfa[(o_e+t)/128, n] * B_e[h, t] sfb[(o_e+t)/128, h]
+ * where A_e / B_e are the K-major packed blocks written by dg_quant_per_channel_128.
+ *   a_packed: e4m3, [N, K_e] blocks at offset o_e*N.  b_packed: e4m3, [H, K_e] at o_e*H.
+ *   sfa: fp32 [K_cap/128][N].  sfb: fp32 [K_cap/128][H].
+ *   c: fp32 [G, N, H] or NULL (zero); may alias d (the pages pass the same tensor).
+ *   d: fp32 [G, N, H].  ks: int32 [G] device.
+ *   K_e = 0 gives D_e = C_e.  Bad ks stop the walk as in dg_quant_per_channel_128.
+ *   workspace: dg_workspace_size(DG_OP_K_GROUPED_WGRAD, G, 0, N, H) bytes; it receives the
+ *   per-expert TMA descriptors, rebuilt from ks by a separate launch on every call (so a
+ *   replayed graph never uses descriptors derived from stale counts).
+ */
+int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
+                           const float* sfb, const float* c, float* d, const int32_t* ks, int G,
+                           int64_t K_cap, int64_t N, int64_t H, void* workspace,
+                           size_t workspace_bytes, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H */

@@ -1,0 +1,70 @@
+"""ctypes declarations of libdg.so (include/dg.h).  Loading fails loudly when the library is
+missing: there is no fallback implementation of any entry point."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB
+
+DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_CUDA = 0, 1, 2, 3
+DG_SF_FP32, DG_SF_UE8M0 = 0, 1
+DG_OUT_BF16, DG_OUT_FP32 = 0, 1
+DG_STATUS_BAD_INDEX = 1
+DG_STATUS_COUNT_GT_CAP = 2
+DG_STATUS_K_NOT_ALIGNED = 4
+DG_STATUS_K_OVERFLOW = 8
+DG_STATUS_TIMEOUT = 16
+DG_STATUS_TOO_MANY_RUNS = 32
+DG_OP_M_GROUPED_CONTIGUOUS, DG_OP_M_GROUPED_MASKED, DG_OP_K_GROUPED_WGRAD = 0, 1, 2
+DG_MAX_GROUPS = 1024
+DG_MAX_M_BLOCKS = 4096
+
+# name -> (restype, argtypes); every symbol include/dg.h declares
+P, I64, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "dg_last_error": (ctypes.c_char_p, []),
+    "dg_workspace_size": (SZ, [I32, I32, I64, I64, I64]),
+    "dg_quant_per_token_1x128": (I32, [P, I64, I64, I64, P, P, I32, F32, P, I32, P]),
+    "dg_quant_per_channel_128": (I32, [P, I64, I64, P, I32, P, P, F32, P, P]),
+    "dg_quant_block_128x128": (I32, [P, I32, I64, I64, P, P, I32, F32, P]),
+    "dg_m_grouped_fp8_contiguous": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, I32, P, SZ, P, P]),
+    "dg_m_grouped_fp8_masked": (I32, [P, P, P, P, P, I32, P, I32, I64, I64, I64, I32, I32, P, SZ, P, P]),
+    "dg_k_grouped_fp8_wgrad": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
+}
+# test hooks exported by the library (not part of include/dg.h)
+TESTING_SIGNATURES = {
+    "dg_testing_kgrouped_prologue": (I32, [P, P, P, I32, I64, I64, I64, P, P]),
+    "dg_testing_kgrouped_host_maps": (I32, [P, P, P, I32, I64, I64, P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DGError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"dg error {code}: {msg}")
+        self.code = code
+
+
+def load() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(f"{LIB} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                                   "(or moe_grouped_fp8_gb300.build.build()); there is no fallback path")
+            lib = ctypes.CDLL(LIB)
+            for name, (res, args) in {**SIGNATURES, **TESTING_SIGNATURES}.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def check(rc: int):
+    if rc != DG_OK:
+        raise DGError(rc, load().dg_last_error().decode())

@@ -1,0 +1,162 @@
+"""Python binding of libdg.so: the same entry points as include/dg.h, taking torch tensors.
+
+Argument marshalling only: every step of the computation runs in the library's CUDA kernels.
+PyTorch provides device memory and the current stream.  Each function checks tensor dtypes,
+devices and sizes against the C ABI's layouts before the call, then raises DGError on a
+non-zero return code.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import DG_OP_K_GROUPED_WGRAD, DG_OUT_BF16, DG_OUT_FP32, DG_SF_FP32, DGError, check, load
+
+__all__ = [
+    "dg_quant_per_token_1x128", "dg_quant_per_channel_128", "dg_quant_block_128x128",
+    "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad",
+    "dg_workspace_size", "dg_last_error", "sfa_padded_rows", "empty_sfa", "kgrouped_workspace", "DGError",
+]
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None:
+            _need(t.is_cuda, "all tensors must be CUDA tensors")
+
+
+def _sf_dtype(fmt):
+    return torch.float32 if fmt == DG_SF_FP32 else torch.uint8
+
+
+def sfa_padded_rows(M: int, sf_format: int) -> int:
+    """Row count Mp of the MN-major per-token scale layout [K/128][Mp]."""
+    return (M + 3) // 4 * 4 if sf_format == DG_SF_FP32 else (M + 15) // 16 * 16
+
+
+def empty_sfa(M: int, K: int, sf_format: int, device) -> torch.Tensor:
+    return torch.empty((K // 128, sfa_padded_rows(M, sf_format)), dtype=_sf_dtype(sf_format), device=device)
+
+
+def dg_last_error() -> str:
+    return load().dg_last_error().decode()
+
+
+def dg_workspace_size(op: int, G: int, M: int = 0, N: int = 0, K: int = 0) -> int:
+    return int(load().dg_workspace_size(op, G, M, N, K))
+
+
+def kgrouped_workspace(G: int, device) -> torch.Tensor:
+    return torch.empty(dg_workspace_size(DG_OP_K_GROUPED_WGRAD, G), dtype=torch.uint8, device=device)
+
+
+def dg_quant_per_token_1x128(x, q, sfa, sf_format=DG_SF_FP32, sf_zero=1e-30, row_counts=None, stream=None):
+    """x bf16 [M, K] (row stride >= K) -> q e4m3/uint8 [M, K], sfa [K/128][Mp]."""
+    _dev(x, q, sfa, row_counts)
+    _need(x.dim() == 2 and x.dtype == torch.bfloat16 and x.stride(1) == 1, "x must be a 2-D bf16 row-major view")
+    M, K = x.shape
+    _need(q.is_contiguous() and q.numel() == M * K and q.element_size() == 1, "q must be a contiguous 1-byte [M, K]")
+    _need(sfa.is_contiguous() and sfa.dtype == _sf_dtype(sf_format)
+          and sfa.numel() >= (K // 128) * sfa_padded_rows(M, sf_format), "sfa has the wrong dtype or size")
+    G = 0
+    if row_counts is not None:
+        _need(row_counts.dtype == torch.int32 and row_counts.is_contiguous(), "row_counts must be int32")
+        G = row_counts.numel()
+    check(load().dg_quant_per_token_1x128(_p(x), M, K, x.stride(0), _p(q), _p(sfa), sf_format, sf_zero,
+                                          _p(row_counts), G, _s(stream)))
+
+
+def dg_quant_per_channel_128(x, ks, q_packed, sf, sf_zero=1e-30, status=None, stream=None):
+    """x bf16 [K_cap, C] token-major -> q_packed [K_cap*C] per-expert K-major, sf fp32 [K_cap/128][C]."""
+    _dev(x, ks, q_packed, sf, status)
+    _need(x.dim() == 2 and x.dtype == torch.bfloat16 and x.is_contiguous(), "x must be contiguous bf16 [K_cap, C]")
+    K_cap, C = x.shape
+    _need(ks.dtype == torch.int32 and ks.is_contiguous(), "ks must be int32")
+    _need(q_packed.is_contiguous() and q_packed.numel() >= K_cap * C and q_packed.element_size() == 1, "q_packed size")
+    _need(sf.is_contiguous() and sf.dtype == torch.float32 and sf.numel() >= (K_cap // 128) * C, "sf size")
+    check(load().dg_quant_per_channel_128(_p(x), K_cap, C, _p(ks), ks.numel(), _p(q_packed), _p(sf), sf_zero,
+                                          _p(status), _s(stream)))
+
+
+def dg_quant_block_128x128(w, q, sfb, sf_format=DG_SF_FP32, sf_zero=1e-30, stream=None):
+    """w bf16 [G, N, K] -> q [G, N, K], sfb [G][N/128][K/128]."""
+    _dev(w, q, sfb)
+    _need(w.dim() == 3 and w.dtype == torch.bfloat16 and w.is_contiguous(), "w must be contiguous bf16 [G, N, K]")
+    G, N, K = w.shape
+    _need(q.is_contiguous() and q.numel() == G * N * K and q.element_size() == 1, "q size")
+    _need(sfb.is_contiguous() and sfb.dtype == _sf_dtype(sf_format)
+          and sfb.numel() >= G * (N // 128) * (K // 128), "sfb has the wrong dtype or size")
+    check(load().dg_quant_block_128x128(_p(w), G, N, K, _p(q), _p(sfb), sf_format, sf_zero, _s(stream)))
+
+
+def _out_code(d):
+    if d.dtype == torch.bfloat16:
+        return DG_OUT_BF16
+    _need(d.dtype == torch.float32, "d must be bf16 or fp32")
+    return DG_OUT_FP32
+
+
+def dg_m_grouped_fp8_contiguous(a, sfa, b, sfb, d, m_indices, sf_format=DG_SF_FP32, status=None, workspace=None,
+                                stream=None):
+    """a [M, K] e4m3, b [G, N, K] e4m3, d [M, N] bf16/fp32, m_indices int32 [M]."""
+    _dev(a, sfa, b, sfb, d, m_indices, status)
+    M, K = a.shape
+    G, N, K2 = b.shape
+    _need(K == K2 and tuple(d.shape) == (M, N) and d.is_contiguous() and a.is_contiguous() and b.is_contiguous(),
+          "shapes")
+    _need(m_indices.dtype == torch.int32 and m_indices.numel() == M, "m_indices must be int32 [M]")
+    _need(sfa.dtype == _sf_dtype(sf_format) and sfb.dtype == _sf_dtype(sf_format), "scale dtype")
+    _need(sfa.numel() >= (K // 128) * sfa_padded_rows(M, sf_format), "sfa size")
+    _need(sfb.numel() >= G * (N // 128) * (K // 128), "sfb size")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(load().dg_m_grouped_fp8_contiguous(_p(a), _p(sfa), _p(b), _p(sfb), _p(d), _out_code(d), _p(m_indices), M, G,
+                                             N, K, sf_format, _p(workspace), ws_bytes, _p(status), _s(stream)))
+
+
+def dg_m_grouped_fp8_masked(a, sfa, b, sfb, d, counts, expected_m=0, sf_format=DG_SF_FP32, status=None,
+                            workspace=None, stream=None):
+    """a [G, cap, K] e4m3, b [G, N, K] e4m3, d [G, cap, N] bf16/fp32, counts int32 [G]."""
+    _dev(a, sfa, b, sfb, d, counts, status)
+    G, cap, K = a.shape
+    G2, N, K2 = b.shape
+    _need(G == G2 and K == K2 and tuple(d.shape) == (G, cap, N), "shapes")
+    _need(a.is_contiguous() and b.is_contiguous() and d.is_contiguous(), "contiguity")
+    _need(counts.dtype == torch.int32 and counts.numel() == G, "counts must be int32 [G]")
+    _need(sfa.dtype == _sf_dtype(sf_format) and sfb.dtype == _sf_dtype(sf_format), "scale dtype")
+    _need(sfa.numel() >= (K // 128) * sfa_padded_rows(G * cap, sf_format), "sfa size")
+    _need(sfb.numel() >= G * (N // 128) * (K // 128), "sfb size")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(load().dg_m_grouped_fp8_masked(_p(a), _p(sfa), _p(b), _p(sfb), _p(d), _out_code(d), _p(counts), G, cap, N,
+                                         K, int(expected_m), sf_format, _p(workspace), ws_bytes, _p(status),
+                                         _s(stream)))
+
+
+def dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, workspace, status=None, stream=None):
+    """D_e = C_e + A_e^T B_e.  a_packed/b_packed: per-expert K-major codes; sfa [K_cap/128][N],
+    sfb [K_cap/128][H]; c (or None, may be d) and d fp32 [G, N, H]; ks int32 [G]."""
+    _dev(a_packed, sfa, b_packed, sfb, c, d, ks, workspace, status)
+    G, N, H = d.shape
+    _need(d.dtype == torch.float32 and d.is_contiguous(), "d must be contiguous fp32 [G, N, H]")
+    _need(c is None or (tuple(c.shape) == tuple(d.shape) and c.dtype == torch.float32 and c.is_contiguous()), "c")
+    _need(ks.dtype == torch.int32 and ks.numel() == G, "ks must be int32 [G]")
+    _need(sfa.dtype == torch.float32 and sfa.numel() >= (K_cap // 128) * N, "sfa")
+    _need(sfb.dtype == torch.float32 and sfb.numel() >= (K_cap // 128) * H, "sfb")
+    _need(a_packed.numel() >= K_cap * N and b_packed.numel() >= K_cap * H, "packed operand size")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(load().dg_k_grouped_fp8_wgrad(_p(a_packed), _p(sfa), _p(b_packed), _p(sfb), _p(c), _p(d), _p(ks), G, K_cap,
+                                        N, H, _p(workspace), ws_bytes, _p(status), _s(stream)))

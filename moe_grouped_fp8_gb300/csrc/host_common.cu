@@ -1,0 +1,86 @@
+// host_common.cu - error state, device properties, TMA descriptor encoding, workspace sizes.
+#include <cstdlib>
+#include <mutex>
+
+#include "host_common.hpp"
+
+namespace dg {
+
+namespace {
+thread_local std::string g_err;
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+cudaError_t g_encode_err = cudaSuccess;
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+}  // namespace
+
+int set_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+const char* last_error() { return g_err.c_str(); }
+void clear_error() { g_err.clear(); }
+
+int device_sm_count(int* out) {
+    int dev = 0;
+    DG_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return set_error(DG_ERR_UNSUPPORTED, "device index %d", dev);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        DG_CHECK_CUDA(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+        g_sm_count[dev] = n;
+    }
+    *out = g_sm_count[dev];
+    return DG_OK;
+}
+
+uint64_t wait_limit_ns() {
+    static uint64_t v = [] {
+        const char* s = std::getenv("DG_WAIT_LIMIT_MS");
+        long long ms = s ? std::atoll(s) : 2000;
+        if (ms <= 0) ms = 2000;
+        return static_cast<uint64_t>(ms) * 1000000ull;
+    }();
+    return v;
+}
+
+int encode_tmap(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode == nullptr)
+        return set_error(DG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(g_encode_err));
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(tm, dtype, rank, const_cast<void*>(base), reinterpret_cast<const cuuint64_t*>(dims),
+                          reinterpret_cast<const cuuint64_t*>(strides_bytes), reinterpret_cast<const cuuint32_t*>(box),
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(DG_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the layout (CUresult %d)", (int)r);
+    return DG_OK;
+}
+
+}  // namespace dg
+
+extern "C" const char* dg_last_error(void) { return dg::last_error(); }
+
+extern "C" size_t dg_workspace_size(int op, int G, int64_t M, int64_t N, int64_t K) {
+    (void)M;
+    (void)N;
+    (void)K;
+    if (op == DG_OP_K_GROUPED_WGRAD && G > 0) return static_cast<size_t>(G) * 2 * 128;  // two tensor maps per expert
+    return 0;
+}

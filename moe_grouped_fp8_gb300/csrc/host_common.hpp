@@ -1,0 +1,53 @@
+// host_common.hpp - host-side helpers of the C ABI: thread-local error messages, argument
+// checks, device properties, and TMA descriptor encoding through the driver entry point
+// (no link-time dependency on libcuda).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "dg.h"
+
+namespace dg {
+
+int set_error(int code, const char* fmt, ...);
+const char* last_error();
+void clear_error();
+
+#define DG_CHECK_ARG(cond, ...)                                               \
+    do {                                                                      \
+        if (!(cond)) return ::dg::set_error(DG_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+#define DG_CHECK_SUPPORTED(cond, ...)                                         \
+    do {                                                                      \
+        if (!(cond)) return ::dg::set_error(DG_ERR_UNSUPPORTED, __VA_ARGS__); \
+    } while (0)
+#define DG_CHECK_CUDA(expr)                                                                     \
+    do {                                                                                        \
+        cudaError_t e_ = (expr);                                                                \
+        if (e_ != cudaSuccess)                                                                  \
+            return ::dg::set_error(DG_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+    } while (0)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count(int* out);
+
+// Upper bound, in nanoseconds, of every spin-wait inside the kernels (env DG_WAIT_LIMIT_MS,
+// default 2000 ms).
+uint64_t wait_limit_ns();
+
+// cuTensorMapEncodeTiled through cudaGetDriverEntryPointByVersion; returns DG_OK or an error
+// code with a message.
+int encode_tmap(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                const uint64_t* dims, const uint64_t* strides_bytes /* rank-1 entries */,
+                const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+}  // namespace dg

@@ -1,0 +1,400 @@
+// quant.cu - FP8 (e4m3) cast kernels: 1x128 per-token, 128x128 per-block, and per-channel over
+// 128 tokens with the per-expert K-major pack.  All three are HBM-bound single-pass kernels:
+// one read of the bf16 input, one write of the codes and the scales.
+//
+// Scale rule (per-channel cast listing of "Non-deterministic numerical problem of
+// k_grouped_fp8_gemm_nt_contiguous", applied along K or over a 128x128 tile for the other two
+// casts): sf = amax / 448 in fp32; sf == 0 -> sf_zero; sf = max(sf, 1e-30); UE8M0 rounds sf up
+// to a power of two.  Codes: e4m3(x * (1/sf)), an IEEE fp32 reciprocal and product, then
+// round-to-nearest-even with saturation to +-448.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "host_common.hpp"
+#include "ptx.cuh"
+
+namespace dg {
+namespace {
+
+__device__ __forceinline__ float scale_rule(float amax, float sf_zero) {
+    float sf = __fdiv_rn(amax, 448.0f);
+    if (sf == 0.0f) sf = sf_zero;
+    return fmaxf(sf, 1e-30f);
+}
+
+// Round a positive normal fp32 scale up to a power of two; *byte = its biased exponent.
+__device__ __forceinline__ float ue8m0_round_up(float sf, uint8_t* byte) {
+    uint32_t b = __float_as_uint(sf);
+    uint32_t e = (b >> 23) & 0xFFu;
+    if (b & 0x7FFFFFu) e += 1;
+    *byte = static_cast<uint8_t>(e);
+    return __uint_as_float(e << 23);
+}
+
+__device__ __forceinline__ uint8_t to_e4m3(float v, float r) {
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fmul_rn(v, r), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// 1x128 per-token cast.  An item is one (row, 128-column block); a half-warp handles one item
+// (16 lanes x 8 bf16).  Each half-warp takes TOKEN_ITEMS_PER_HW items per pass so that several
+// 16-byte loads are in flight per thread.
+// ---------------------------------------------------------------------------------------
+constexpr int TOKEN_ITEMS_PER_HW = 4;
+
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                           int64_t ldx, uint8_t* __restrict__ q, void* sfa,
+                                                           int64_t Mp, float sf_zero,
+                                                           const int32_t* __restrict__ row_counts, int64_t rpg) {
+    const int64_t KB = K / 128;
+    const int64_t items = M * KB;
+    const int lane = threadIdx.x & 31;
+    const int hw = lane >> 4;   // half-warp
+    const int sub = lane & 15;  // 16-byte chunk within the 256-byte block
+    const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    constexpr int PER_WARP = 2 * TOKEN_ITEMS_PER_HW;
+
+    for (int64_t base = warp_global * PER_WARP; base < items; base += nwarps * PER_WARP) {
+        uint4 raw[TOKEN_ITEMS_PER_HW];
+        bool live[TOKEN_ITEMS_PER_HW];
+        int64_t m_of[TOKEN_ITEMS_PER_HW], kb_of[TOKEN_ITEMS_PER_HW];
+#pragma unroll
+        for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
+            const int64_t it = base + 2 * j + hw;
+            bool ok = it < items;
+            int64_t m = ok ? it / KB : 0, kb = ok ? it % KB : 0;
+            if (ok && row_counts != nullptr) {
+                const int64_t g = m / rpg, r = m % rpg;
+                int64_t lim = row_counts[g];
+                lim = lim < 0 ? 0 : (lim > rpg ? rpg : lim);
+                ok = r < lim;
+            }
+            live[j] = ok;
+            m_of[j] = m;
+            kb_of[j] = kb;
+            raw[j] = ok ? __ldg(reinterpret_cast<const uint4*>(x + m * ldx + kb * 128) + sub) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
+            float f[8];
+            bf16x8_to_float(raw[j], f);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (!live[j]) continue;
+            float sf = scale_rule(amax, sf_zero);
+            uint8_t byte = 0;
+            if constexpr (UE8M0) sf = ue8m0_round_up(sf, &byte);
+            const float r = __frcp_rn(sf);
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(to_e4m3(f[i], r)) << (8 * i);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(to_e4m3(f[4 + i], r)) << (8 * i);
+            const int64_t m = m_of[j], kb = kb_of[j];
+            *reinterpret_cast<uint2*>(q + m * K + kb * 128 + sub * 8) = make_uint2(lo, hi);
+            if (sub == 0) {
+                if constexpr (UE8M0)
+                    static_cast<uint8_t*>(sfa)[kb * Mp + m] = byte;
+                else
+                    static_cast<float*>(sfa)[kb * Mp + m] = sf;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// 128x128 per-block cast.  One CTA (256 threads) per block; thread t holds 16-byte column
+// chunk (t % 16) of rows (t / 16) + 16 j, j < 8, so each warp load covers two full 256-byte
+// row segments.
+// ---------------------------------------------------------------------------------------
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) k_quant_block_128x128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
+                                                             uint8_t* __restrict__ q, void* sfb, float sf_zero) {
+    const int64_t NB = N / 128, KB = K / 128;
+    const int64_t blk = blockIdx.x;
+    const int64_t kb = blk % KB;
+    const int64_t nb = (blk / KB) % NB;
+    const int64_t g = blk / (KB * NB);
+    const int t = threadIdx.x;
+    const int c = t & 15, r0 = t >> 4;
+    const uint16_t* base = w + (g * N + nb * 128) * K + kb * 128;
+
+    uint4 raw[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        raw[j] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(r0 + 16 * j) * K) + c);
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float f[8];
+        bf16x8_to_float(raw[j], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    __shared__ float s_amax[8];
+    if ((t & 31) == 0) s_amax[t >> 5] = amax;
+    __syncthreads();
+    amax = s_amax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_amax[i]);
+
+    float sf = scale_rule(amax, sf_zero);
+    uint8_t byte = 0;
+    if constexpr (UE8M0) sf = ue8m0_round_up(sf, &byte);
+    const float r = __frcp_rn(sf);
+    uint8_t* qb = q + (g * N + nb * 128) * K + kb * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float f[8];
+        bf16x8_to_float(raw[j], f);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(to_e4m3(f[i], r)) << (8 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(to_e4m3(f[4 + i], r)) << (8 * i);
+        *reinterpret_cast<uint2*>(qb + static_cast<int64_t>(r0 + 16 * j) * K + c * 8) = make_uint2(lo, hi);
+    }
+    if (t == 0) {
+        const int64_t si = (g * NB + nb) * KB + kb;
+        if constexpr (UE8M0)
+            static_cast<uint8_t*>(sfb)[si] = byte;
+        else
+            static_cast<float*>(sfb)[si] = sf;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Per-channel cast over 128-token blocks + per-expert K-major pack.  CTA = (64-column block,
+// 128-token block).  Thread t holds columns 8 (t % 8) .. +8 of the four consecutive tokens
+// 4 (t / 8) .. +4; codes are transposed through shared memory (4 tokens packed per 32-bit word)
+// and written as 128-byte column runs of the expert's [C, K_e] block.
+// ---------------------------------------------------------------------------------------
+constexpr int CH_COLS = 64;
+constexpr int CH_PITCH = 132;  // bytes per transposed column row (128 tokens + 4 pad)
+
+// Expert lookup for token `tok`: returns the expert index with its token offset and K_e, or
+// -1 when the token lies past the last valid expert.  Walks ks with a block-wide scan in
+// chunks of blockDim.x (<= 256 threads) and stops at the first bad expert (K_e < 0,
+// K_e % 128 != 0, or a span past K_cap); *bad_bits gets the DG_STATUS_* bits it met.
+__device__ int find_expert(const int32_t* __restrict__ ks, int G, int64_t K_cap, int64_t tok, int64_t* o_out,
+                           int64_t* k_out, int* bad_bits) {
+    __shared__ long long s_warp[8];
+    __shared__ long long s_carry, s_o, s_k;
+    __shared__ int s_found, s_first_bad, s_bad;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int nwarps = static_cast<int>(blockDim.x >> 5);
+    if (t == 0) {
+        s_carry = 0;
+        s_found = -1;
+        s_first_bad = 0x7fffffff;
+        s_bad = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < G; base += blockDim.x) {
+        const int e = base + t;
+        const long long k = (e < G) ? ks[e] : 0;
+        int bad = (e < G && (k < 0 || (k % 128) != 0)) ? DG_STATUS_K_NOT_ALIGNED : 0;
+        const long long kk = bad ? 0 : k;
+        long long incl = kk;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_warp[wid] = incl;
+        __syncthreads();
+        long long wpre = 0;
+        for (int i = 0; i < wid; ++i) wpre += s_warp[i];
+        const long long o_e = s_carry + wpre + incl - kk;  // exclusive prefix of valid K_e
+        if (e < G && !bad && o_e + kk > K_cap) bad = DG_STATUS_K_OVERFLOW;
+        if (bad) {
+            atomicOr(&s_bad, bad);
+            atomicMin(&s_first_bad, e);
+        }
+        __syncthreads();
+        const int first_bad = s_first_bad;
+        if (e < G && e < first_bad && kk > 0 && tok >= o_e && tok < o_e + kk) {
+            s_found = e;
+            s_o = o_e;
+            s_k = kk;
+        }
+        __syncthreads();
+        const bool done = (s_found >= 0) || (first_bad != 0x7fffffff);
+        if (t == 0) {
+            long long tot = 0;
+            for (int i = 0; i < nwarps; ++i) tot += s_warp[i];
+            s_carry += tot;
+        }
+        __syncthreads();
+        if (done) break;
+    }
+    *bad_bits = s_bad;
+    const int f = s_found;
+    if (f >= 0) {
+        *o_out = s_o;
+        *k_out = s_k;
+    }
+    return f;
+}
+
+__global__ void __launch_bounds__(256) k_quant_channel_128(const uint16_t* __restrict__ x, int64_t K_cap, int64_t C,
+                                                           const int32_t* __restrict__ ks, int G,
+                                                           uint8_t* __restrict__ qp, float* __restrict__ sf_out,
+                                                           float sf_zero, int32_t* status) {
+    __shared__ float s_part[8][CH_COLS];
+    __shared__ float s_r[CH_COLS];
+    __shared__ __align__(16) uint8_t s_t[CH_COLS * CH_PITCH];
+
+    const int64_t tb = blockIdx.y;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * CH_COLS;
+    int64_t o_e = 0, k_e = 0;
+    int bad = 0;
+    const int e = find_expert(ks, G, K_cap, tb * 128, &o_e, &k_e, &bad);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) status_or(status, bad);
+    if (e < 0) return;
+
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int c = t & 7;          // 8-column chunk
+    const int rb = (t >> 3) * 4;  // first of 4 consecutive tokens
+    uint4 raw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        raw[j] = __ldg(reinterpret_cast<const uint4*>(x + (tb * 128 + rb + j) * C + c0) + c);
+    float f[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) bf16x8_to_float(raw[j], f[j]);
+    float cm[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        cm[i] = fmaxf(fmaxf(fabsf(f[0][i]), fabsf(f[1][i])), fmaxf(fabsf(f[2][i]), fabsf(f[3][i])));
+        cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 8));
+        cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], 16));
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s_part[wid][c * 8 + i] = cm[i];
+    }
+    __syncthreads();
+    if (t < CH_COLS) {
+        float amax = s_part[0][t];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_part[w][t]);
+        const float sf = scale_rule(amax, sf_zero);
+        sf_out[tb * C + c0 + t] = sf;
+        s_r[t] = __frcp_rn(sf);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float r = s_r[c * 8 + i];
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) word |= static_cast<uint32_t>(to_e4m3(f[j][i], r)) << (8 * j);
+        *reinterpret_cast<uint32_t*>(&s_t[(c * 8 + i) * CH_PITCH + rb]) = word;
+    }
+    __syncthreads();
+    // column `col` of this CTA -> 128 consecutive bytes of row (c0 + col) of expert e's block
+    uint8_t* dst_base = qp + o_e * C + (tb * 128 - o_e);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int s = t + 256 * u;
+        const int col = s >> 3, piece = s & 7;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&s_t[col * CH_PITCH + piece * 16]);
+        uint4 v = make_uint4(src[0], src[1], src[2], src[3]);
+        *reinterpret_cast<uint4*>(dst_base + (c0 + col) * k_e + piece * 16) = v;
+    }
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, void* sfa,
+                                        int sf_format, float sf_zero, const int32_t* row_counts, int G,
+                                        void* stream) {
+    DG_CHECK_ARG(M >= 0 && K > 0 && K % 128 == 0, "need M >= 0 and K a positive multiple of 128 (M=%lld K=%lld)",
+                 (long long)M, (long long)K);
+    DG_CHECK_ARG(ldx >= K && (ldx * 2) % 16 == 0, "ldx must be >= K and ldx*2 a multiple of 16 (ldx=%lld)",
+                 (long long)ldx);
+    DG_CHECK_ARG(sf_format == DG_SF_FP32 || sf_format == DG_SF_UE8M0, "bad sf_format %d", sf_format);
+    if (M == 0) return DG_OK;
+    DG_CHECK_ARG(x && q && sfa, "null pointer argument");
+    DG_CHECK_ARG(aligned16(x) && ((reinterpret_cast<uintptr_t>(q) & 7u) == 0), "x must be 16-byte and q 8-byte aligned");
+    int64_t rpg = M;
+    if (row_counts != nullptr) {
+        DG_CHECK_ARG(G >= 1 && M % G == 0, "row_counts needs G >= 1 dividing M (M=%lld G=%d)", (long long)M, G);
+        rpg = M / G;
+    }
+    const int64_t Mp = (sf_format == DG_SF_FP32) ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
+    int sms = 0;
+    if (int rc = device_sm_count(&sms)) return rc;
+    const int64_t items = M * (K / 128);
+    const int64_t per_block = 8 * 2 * TOKEN_ITEMS_PER_HW;  // 8 warps
+    int64_t blocks = (items + per_block - 1) / per_block;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (sf_format == DG_SF_UE8M0)
+        k_quant_token_1x128<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+            static_cast<const uint16_t*>(x), M, K, ldx, q, sfa, Mp, sf_zero, row_counts, rpg);
+    else
+        k_quant_token_1x128<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+            static_cast<const uint16_t*>(x), M, K, ldx, q, sfa, Mp, sf_zero, row_counts, rpg);
+    DG_CHECK_CUDA(cudaGetLastError());
+    return DG_OK;
+}
+
+extern "C" int dg_quant_block_128x128(const void* w, int G, int64_t N, int64_t K, uint8_t* q, void* sfb,
+                                      int sf_format, float sf_zero, void* stream) {
+    DG_CHECK_ARG(G >= 0 && N >= 0 && K >= 0 && N % 128 == 0 && K % 128 == 0,
+                 "need N and K multiples of 128 (G=%d N=%lld K=%lld)", G, (long long)N, (long long)K);
+    DG_CHECK_ARG(sf_format == DG_SF_FP32 || sf_format == DG_SF_UE8M0, "bad sf_format %d", sf_format);
+    const int64_t blocks = static_cast<int64_t>(G) * (N / 128) * (K / 128);
+    if (blocks == 0) return DG_OK;
+    DG_CHECK_ARG(w && q && sfb, "null pointer argument");
+    DG_CHECK_ARG(aligned16(w) && ((reinterpret_cast<uintptr_t>(q) & 7u) == 0), "w must be 16-byte and q 8-byte aligned");
+    DG_CHECK_SUPPORTED(blocks < (1ll << 31), "too many 128x128 blocks");
+    auto s = static_cast<cudaStream_t>(stream);
+    if (sf_format == DG_SF_UE8M0)
+        k_quant_block_128x128<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint16_t*>(w), N,
+                                                                                   K, q, sfb, sf_zero);
+    else
+        k_quant_block_128x128<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint16_t*>(w),
+                                                                                    N, K, q, sfb, sf_zero);
+    DG_CHECK_CUDA(cudaGetLastError());
+    return DG_OK;
+}
+
+extern "C" int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C, const int32_t* ks, int G,
+                                        uint8_t* q_packed, float* sf, float sf_zero, int32_t* status,
+                                        void* stream) {
+    DG_CHECK_ARG(K_cap >= 0 && K_cap % 128 == 0, "K_cap must be a multiple of 128 (%lld)", (long long)K_cap);
+    DG_CHECK_ARG(C > 0 && C % CH_COLS == 0, "C must be a positive multiple of %d (%lld)", CH_COLS, (long long)C);
+    DG_CHECK_ARG(G >= 1 && G <= DG_MAX_GROUPS, "G must be in [1, %d] (%d)", DG_MAX_GROUPS, G);
+    if (K_cap == 0) return DG_OK;
+    DG_CHECK_ARG(x && ks && q_packed && sf, "null pointer argument");
+    DG_CHECK_ARG(aligned16(x) && aligned16(q_packed), "x and q_packed must be 16-byte aligned");
+    DG_CHECK_SUPPORTED(K_cap / 128 < 65536, "K_cap too large");
+    dim3 grid(static_cast<unsigned>(C / CH_COLS), static_cast<unsigned>(K_cap / 128));
+    k_quant_channel_128<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(x), K_cap, C, ks, G, q_packed, sf, sf_zero, status);
+    DG_CHECK_CUDA(cudaGetLastError());
+    return DG_OK;
+}
