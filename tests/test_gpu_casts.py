@@ -1,0 +1,118 @@
+"""GPU parity of the three cast kernels against the oracle: codes and scales bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_K_NOT_ALIGNED, DG_STATUS_K_OVERFLOW
+from moe_grouped_fp8_gb300 import workloads as wl
+
+from gpu_helpers import gpu_quant_blocks, gpu_quant_channels, gpu_quant_tokens, sfa_rows, sync
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+@pytest.mark.parametrize("M,K,scale", [(1, 128, 1.0), (37, 256, 3.0), (300, 1024, 1e-3), (1029, 7168, 0.02)])
+def test_per_token_codes_and_scales_bit_exact(fmt, M, K, scale):
+    x = wl.randn_bf16((M, K), 100 + M, scale)
+    x[0, :128] = 0                                     # all-zero block -> sf_zero
+    if M > 3:
+        x[3, 128 % K:128 % K + 5] = 448 * scale * 30    # dominant element
+    q, sfa = gpu_quant_tokens(x.cuda(), fmt, sf_zero=0.5)
+    sync()
+    oq, osf, oue = oracle.quant_per_token_1x128(x, sf_zero=0.5, ue8m0=(fmt == DG_SF_UE8M0))
+    np.testing.assert_array_equal(q.cpu().numpy(), oq)
+    got = sfa_rows(sfa, M)
+    if fmt == DG_SF_FP32:
+        np.testing.assert_array_equal(got.view(np.uint32), osf.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(got, oue)
+
+
+def test_per_token_strided_input_and_row_counts():
+    G, cap, K = 5, 40, 512
+    x = wl.randn_bf16((G, cap, K + 64), 7)             # padded rows: ldx = K + 64
+    xd = x.cuda().view(G * cap, K + 64)[:, :K]
+    counts = torch.tensor([0, 40, 13, 99, 1], dtype=torch.int32)
+    q, sfa = gpu_quant_tokens(xd, DG_SF_FP32, row_counts=counts.cuda())
+    sync()
+    oq, osf, _ = oracle.quant_per_token_1x128(x.view(G * cap, K + 64)[:, :K].contiguous(), row_counts=counts.numpy())
+    live = np.zeros(G * cap, bool)
+    for g, c in enumerate(np.clip(counts.numpy(), 0, cap)):
+        live[g * cap:g * cap + c] = True
+    qn = q.cpu().numpy()
+    np.testing.assert_array_equal(qn[live], oq[live])
+    assert np.all(qn[~live] == 0), "rows past the count must not be written"
+    got = sfa_rows(sfa, G * cap)
+    np.testing.assert_array_equal(got[live], osf[live])
+    assert np.all(got[~live] == 0)
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+@pytest.mark.parametrize("G,N,K,scale", [(1, 128, 128, 1.0), (3, 256, 384, 0.02), (2, 512, 1024, 5.0)])
+def test_block_codes_and_scales_bit_exact(fmt, G, N, K, scale):
+    w = wl.randn_bf16((G, N, K), 200 + G, scale)
+    w[0, :128, :128] = 0
+    q, sfb = gpu_quant_blocks(w.cuda(), fmt, sf_zero=2.0)
+    sync()
+    oq, osf, oue = oracle.quant_block_128x128(w, sf_zero=2.0, ue8m0=(fmt == DG_SF_UE8M0))
+    np.testing.assert_array_equal(q.cpu().numpy(), oq)
+    if fmt == DG_SF_FP32:
+        np.testing.assert_array_equal(sfb.cpu().numpy().view(np.uint32), osf.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(sfb.cpu().numpy(), oue)
+
+
+@pytest.mark.parametrize("sf_zero", [1.0, 1e-4, 1e-8, 1e-30])
+@pytest.mark.parametrize("ks,C", [([256, 128, 128, 256], 2048), ([128, 0, 384, 128], 192), ([640], 64)])
+def test_per_channel_codes_pack_and_scales_bit_exact(ks, C, sf_zero):
+    T = sum(ks)
+    K_cap = T + 256                                     # capacity beyond sum(ks) is left untouched
+    x = wl.randn_bf16((K_cap, C), 300 + C, 1e-7)
+    o = 0
+    for k in ks:
+        if k == 128:
+            x[o:o + k, 0] = 0
+        o += k
+    qp, sf = gpu_quant_channels(x.cuda(), torch.tensor(ks, dtype=torch.int32, device="cuda"), sf_zero)
+    sync()
+    oq, osf = oracle.quant_per_channel_128(x[:T], sf_zero)
+    packed = oracle.pack_kmajor(oq, ks)
+    qpn = qp.cpu().numpy()
+    np.testing.assert_array_equal(qpn[:T * C], packed)
+    assert np.all(qpn[T * C:] == 0)
+    sfn = sf.cpu().numpy()
+    np.testing.assert_array_equal(sfn[:T // 128].view(np.uint32), osf.view(np.uint32))
+    assert np.all(sfn[T // 128:] == 0)
+
+
+def test_per_channel_bad_ks_sets_status_and_stops():
+    C = 128
+    x = wl.randn_bf16((512, C), 5).cuda()
+    for ks, bit, good in [([128, 100, 128], DG_STATUS_K_NOT_ALIGNED, 128), ([256, 512, 128], DG_STATUS_K_OVERFLOW, 256)]:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        qp, sf = gpu_quant_channels(x, torch.tensor(ks, dtype=torch.int32, device="cuda"), status=status)
+        sync()
+        assert status.item() & bit
+        sfn = sf.cpu().numpy()
+        assert np.all(sfn[:good // 128] > 0) and np.all(sfn[good // 128:] == 0)
+
+
+def test_cast_matches_oracle_on_every_code_midpoint():
+    """Device encode on values at every e4m3 midpoint (ties to even), with every scale exactly 1."""
+    grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    vals = np.concatenate([grid.astype(np.float32), mids, -mids])
+    n = (vals.size + 127) // 128 * 128
+    row = np.zeros(n, np.float32)
+    row[:vals.size] = vals
+    row = row.reshape(-1, 128)
+    row[:, 0] = 448.0                                    # every block has amax 448 -> sf = 1 exactly
+    x = torch.from_numpy(row).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.from_numpy(row)), "midpoints are bf16-exact"
+    q, sfa = gpu_quant_tokens(x.cuda(), DG_SF_FP32)
+    sync()
+    oq, osf, _ = oracle.quant_per_token_1x128(x)
+    assert np.all(osf == 1.0)
+    np.testing.assert_array_equal(q.cpu().numpy(), oq)

@@ -1,0 +1,210 @@
+"""GPU parity of the m-grouped contiguous FP8 GEMM (m_indices routing, -1 padding rows), including
+CUDA-graph replay with the expert distribution re-drawn in place between replays."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_BAD_INDEX, api
+from moe_grouped_fp8_gb300 import workloads as wl
+
+from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
+                         sentinel_value, sync, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def contiguous_case(a, b, m_indices, fmt=DG_SF_FP32, out=torch.bfloat16, calls=1):
+    M, K = a.shape
+    G, N, _ = b.shape
+    qa, sfa = gpu_quant_tokens(a.cuda(), fmt)
+    qb, sfb = gpu_quant_blocks(b.cuda(), fmt)
+    mi = torch.tensor(np.asarray(m_indices, np.int32), device="cuda")
+    d = sentinel_like((M, N), out)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    first = None
+    for i in range(calls):
+        api.dg_m_grouped_fp8_contiguous(qa, sfa, qb, sfb, d, mi, fmt, status)
+        if calls > 1:
+            bits = out_bits(d)
+            if first is None:
+                first = bits
+            else:
+                assert np.array_equal(bits, first), f"call {i} differs bitwise"
+    sync()
+    ue = fmt == DG_SF_UE8M0
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a, ue8m0=ue)
+    oqb, osfb, _ = oracle.quant_block_128x128(b, ue8m0=ue)
+    np.testing.assert_array_equal(qa.cpu().numpy(), oqa)
+    ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, m_indices)
+    mi_np = np.asarray(m_indices)
+    # rows written: routed rows whose 128-row block is headed by the same expert
+    block_e = mi_np[(np.arange(M) // 128) * 128]
+    valid = (mi_np >= 0) & (mi_np == block_e)
+    fp32 = out == torch.float32
+    if valid.any():
+        assert_close(to_f64(d)[valid], ref_out(ref[valid], fp32), fp32, "contiguous routed rows")
+    assert np.all(out_bits(d)[~valid] == sentinel_value(out)), "a padding row was written"
+    return d, status
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
+def test_small_ragged_segments(fmt, out):
+    counts = [130, 0, 1, 128, 257]
+    mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
+    a = wl.randn_bf16((mi.size, 384), 51, 1.5)
+    b = wl.randn_bf16((5, 256, 384), 52, 0.02)
+    contiguous_case(a, b, mi, fmt, out)
+
+
+def test_single_expert_plain_gemm_and_repeat_bitwise():
+    mi = np.zeros(300, np.int32)
+    mi[290:] = -1
+    a = wl.randn_bf16((300, 256), 61)
+    b = wl.randn_bf16((1, 512, 256), 62)
+    contiguous_case(a, b, mi, calls=8)
+
+
+def test_all_padding_and_ragged_last_block():
+    mi = np.full(200, -1, np.int32)
+    a = wl.randn_bf16((200, 128), 71)
+    b = wl.randn_bf16((2, 128, 128), 72)
+    contiguous_case(a, b, mi)
+    mi2 = np.full(200, -1, np.int32)
+    mi2[128:133] = 1                                   # ragged final block (rows 128..199 of a 256 block)
+    contiguous_case(a, b, mi2)
+
+
+def test_segments_out_of_expert_order():
+    mi = np.full(512, -1, np.int32)
+    mi[0:70] = 2
+    mi[128:256] = 0
+    mi[256:300] = 1
+    a = wl.randn_bf16((512, 256), 81)
+    b = wl.randn_bf16((3, 256, 256), 82)
+    contiguous_case(a, b, mi)
+
+
+def test_bad_indices_flagged_and_skipped():
+    mi = np.full(256, -1, np.int32)
+    mi[0:10] = 0
+    mi[10:12] = 7                                      # >= G: bad and not written
+    mi[128] = -9                                       # < -1: bad block head -> block skipped
+    mi[129:140] = 1
+    a = wl.randn_bf16((256, 128), 91)
+    b = wl.randn_bf16((2, 128, 128), 92)
+    qa, sfa = gpu_quant_tokens(a.cuda(), DG_SF_FP32)
+    qb, sfb = gpu_quant_blocks(b.cuda(), DG_SF_FP32)
+    d = sentinel_like((256, 128), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dg_m_grouped_fp8_contiguous(qa, sfa, qb, sfb, d, torch.tensor(mi, device="cuda"), DG_SF_FP32, status)
+    sync()
+    assert status.item() & DG_STATUS_BAD_INDEX
+    bits = out_bits(d)
+    assert np.all(bits[10:12] == 0xFFFF) and np.all(bits[128:] == 0xFFFF)
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a)
+    oqb, osfb, _ = oracle.quant_block_128x128(b)
+    ok = np.full(256, -1, np.int32)
+    ok[0:10] = 0
+    ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, ok)
+    assert_close(to_f64(d)[:10], ref_out(ref[:10], False), False, "rows before the bad ones")
+
+
+def replay_case(G, N, K, E, replays, check_every, seed):
+    """Capture cast + GEMM once; replay with routing re-drawn in place (same buffers)."""
+    T = G * E
+    m_max = wl.contiguous_capacity(T, G)
+    a = wl.randn_bf16((m_max, K), seed, 1.0, device="cuda")
+    b = wl.randn_bf16((G, N, K), seed + 1, 0.02, device="cuda")
+    fmt = DG_SF_UE8M0
+    qa = torch.empty(m_max, K, dtype=torch.uint8, device="cuda")
+    sfa = api.empty_sfa(m_max, K, fmt, "cuda")
+    qb, sfb = gpu_quant_blocks(b, fmt)
+    mi_dev = torch.full((m_max,), -1, dtype=torch.int32, device="cuda")
+    d = torch.empty(m_max, N, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        api.dg_quant_per_token_1x128(a, qa, sfa, fmt)
+        api.dg_m_grouped_fp8_contiguous(qa, sfa, qb, sfb, d, mi_dev, fmt, status)
+
+    mi_dev.copy_(torch.from_numpy(wl.contiguous_m_indices(wl.multinomial_counts(T, G, seed), m_max)))
+    step()                                             # eager warm-up before capture
+    sync()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    sync()
+    oqb = osfb = None
+    checked = 0
+    for it in range(replays):
+        counts = wl.multinomial_counts(T, G, seed + 1 + it)
+        if it == replays // 2:
+            counts = np.zeros(G, np.int32)             # an all-empty phase
+        mi_np = wl.contiguous_m_indices(counts, m_max)
+        mi_dev.copy_(torch.from_numpy(mi_np))          # same pointer, new values
+        d.view(torch.int16).fill_(-1)
+        g.replay()
+        if it % check_every == 0 or it == replays // 2:
+            sync()
+            assert status.item() == 0
+            bits = out_bits(d)
+            assert np.all(bits[mi_np < 0] == 0xFFFF), f"replay {it}: padding row written"
+            rows = np.nonzero(mi_np >= 0)[0]
+            if rows.size:
+                if oqb is None:
+                    oqb, osfb, _ = oracle.quant_block_128x128(b.cpu(), ue8m0=True)
+                pick = np.unique(np.random.default_rng(it).choice(rows, min(24, rows.size), replace=False))
+                oqa, osfa, _ = oracle.quant_per_token_1x128(a[torch.from_numpy(pick).cuda()].cpu(), ue8m0=True)
+                ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, mi_np[pick])
+                assert_close(to_f64(d)[pick], ref_out(ref, False), False, f"replay {it}")
+            checked += 1
+    assert checked >= replays // check_every
+
+
+def test_graph_replay_with_changed_routing_small():
+    replay_case(G=16, N=256, K=256, E=20, replays=30, check_every=3, seed=7)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("which,E", [("w13", 1), ("w13", 32), ("w2", 113)])
+def test_many_expert_ue8m0_graph_replay(which, E):
+    """G=288 many-expert shapes, UE8M0 scales, 100 replays with re-drawn routing (every 10th
+    replay checked against the oracle on sampled rows)."""
+    N, K = (512, 4096) if which == "w13" else (4096, 256)
+    replay_case(G=288, N=N, K=K, E=E, replays=100, check_every=10, seed=1005 + E)
+
+
+@pytest.mark.slow
+def test_prefill_shape_full_size_sampled():
+    """G=32, N=4096, K=7168, 8192 Zipf-routed tokens: the full-size launch, sampled rows."""
+    w = wl.contiguous_prefill()
+    M, K, N = w.m_max, w.K, w.N
+    a, b = w.draw(device="cuda")
+    mi = w.m_indices
+    qa, sfa = gpu_quant_tokens(a, DG_SF_FP32)
+    qb, sfb = gpu_quant_blocks(b, DG_SF_FP32)
+    d = sentinel_like((M, N), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dg_m_grouped_fp8_contiguous(qa, sfa, qb, sfb, d, torch.from_numpy(mi).cuda(), DG_SF_FP32, status)
+    sync()
+    assert status.item() == 0
+    rng = np.random.default_rng(3)
+    rows = rng.choice(np.nonzero(mi >= 0)[0], 24, replace=False)
+    gpu_vals, ref_vals = [], []
+    for nb in rng.choice(N // 128, 2, replace=False):
+        for r in rows:
+            e = int(mi[r])
+            oqb, osfb, _ = oracle.quant_block_128x128(b[e:e + 1, nb * 128:(nb + 1) * 128].cpu())
+            oqa, osfa, _ = oracle.quant_per_token_1x128(a[r:r + 1].cpu())
+            ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, np.zeros(1, np.int32))
+            gpu_vals.append(to_f64(d[r, nb * 128:(nb + 1) * 128]))
+            ref_vals.append(ref_out(ref[0], False))
+    assert_close(np.concatenate(gpu_vals), np.concatenate(ref_vals), False, "prefill sampled")
+    pad = torch.from_numpy(mi < 0).cuda()
+    assert bool((d.view(torch.int16)[pad] == -1).all()), "padding rows written"

@@ -1,0 +1,155 @@
+"""GPU parity of the m-grouped masked FP8 GEMM against the oracle (cast -> GEMM on the device,
+the oracle's own cast -> fp64 GEMM on the host, from the same bf16 bytes)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_COUNT_GT_CAP, api
+from moe_grouped_fp8_gb300 import workloads as wl
+
+from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
+                         sentinel_value, sync, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def masked_case(a, b, counts, fmt=DG_SF_FP32, out=torch.bfloat16, expected_m=0, calls=1):
+    """Run the device path `calls` times into one sentinel-filled output and check it."""
+    G, cap, K = a.shape
+    N = b.shape[1]
+    ad, bd = a.cuda(), b.cuda()
+    cnt = torch.tensor(np.asarray(counts, np.int32), device="cuda")
+    qa, sfa = gpu_quant_tokens(ad.view(G * cap, K), fmt)
+    qb, sfb = gpu_quant_blocks(bd, fmt)
+    d = sentinel_like((G, cap, N), out)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    first = None
+    for i in range(calls):
+        api.dg_m_grouped_fp8_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, expected_m, fmt, status)
+        if calls > 1:
+            bits = out_bits(d)
+            if first is None:
+                first = bits
+            else:
+                assert np.array_equal(bits, first), f"call {i} differs bitwise from call 0"
+    sync()
+    ue = fmt == DG_SF_UE8M0
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a.view(G * cap, K), ue8m0=ue)
+    oqb, osfb, _ = oracle.quant_block_128x128(b, ue8m0=ue)
+    np.testing.assert_array_equal(qa.cpu().numpy(), oqa)
+    np.testing.assert_array_equal(qb.cpu().numpy(), oqb)
+    ref = oracle.gemm_masked(oqa.reshape(G, cap, K), osfa.reshape(G, cap, K // 128), oqb, osfb, counts)
+    v = np.clip(np.asarray(counts), 0, cap)
+    valid = np.arange(cap)[None, :] < v[:, None]
+    fp32 = out == torch.float32
+    if valid.any():
+        assert_close(to_f64(d)[valid], ref_out(ref[valid], fp32), fp32, "masked valid rows")
+    assert np.all(out_bits(d)[~valid] == sentinel_value(out)), "a row at or past its expert's count was written"
+    return d, status
+
+
+def test_pages_boundary_repro_16_calls():
+    """G=8, cap=32, N=K=256, counts [0,1,16,31,32,1,32,32], seed 29; 16 calls, all bitwise equal;
+    valid rows within tolerance; every padding row keeps its sentinel."""
+    w = wl.masked_repro()
+    a, b = w.draw()
+    masked_case(a, b, w.counts, calls=16, expected_m=32)
+
+
+CAPS = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 96, 127, 128, 129, 160, 200, 255, 256, 257]
+
+
+@pytest.mark.parametrize("cap", CAPS)
+def test_capacity_panel(cap):
+    rng = np.random.default_rng(cap)
+    G, N, K = 4, 256, 256
+    counts = rng.integers(0, cap + 1, G)
+    counts[rng.integers(0, G)] = cap                  # one full expert
+    counts[rng.integers(0, G)] = 0                    # one empty expert
+    a = wl.randn_bf16((G, cap, K), 1000 + cap)
+    b = wl.randn_bf16((G, N, K), 2000 + cap)
+    masked_case(a, b, counts)
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
+def test_formats_and_output_dtypes(fmt, out):
+    G, cap, N, K = 3, 200, 384, 512
+    a = wl.randn_bf16((G, cap, K), 11, 2.0)
+    b = wl.randn_bf16((G, N, K), 12, 0.02)
+    masked_case(a, b, [200, 77, 129], fmt=fmt, out=out)
+
+
+def test_single_expert_and_all_empty():
+    a = wl.randn_bf16((1, 130, 256), 21)
+    b = wl.randn_bf16((1, 128, 256), 22)
+    masked_case(a, b, [130])
+    a3 = wl.randn_bf16((3, 64, 256), 23)
+    b3 = wl.randn_bf16((3, 128, 256), 24)
+    masked_case(a3, b3, [0, 0, 0])
+
+
+def test_expected_m_does_not_change_result():
+    w = wl.masked_repro()
+    a, b = w.draw()
+    d1, _ = masked_case(a, b, w.counts, expected_m=1)
+    d2, _ = masked_case(a, b, w.counts, expected_m=4096)
+    assert np.array_equal(out_bits(d1), out_bits(d2))
+
+
+def test_counts_out_of_range_are_clamped_and_flagged():
+    G, cap, N, K = 3, 48, 128, 256
+    a = wl.randn_bf16((G, cap, K), 31)
+    b = wl.randn_bf16((G, N, K), 32)
+    _, status = masked_case(a, b, [-5, 1000, 20])
+    assert status.item() & DG_STATUS_COUNT_GT_CAP
+
+
+def test_group_independence_bitwise():
+    G, cap, N, K = 3, 160, 256, 384
+    a = wl.randn_bf16((G, cap, K), 41)
+    b = wl.randn_bf16((G, N, K), 42)
+    counts = [160, 100, 33]
+    d0, _ = masked_case(a, b, counts)
+    a2, b2 = a.clone(), b.clone()
+    a2[1] *= -3
+    b2[2] = wl.randn_bf16((N, K), 43)
+    d1, _ = masked_case(a2, b2, counts)
+    assert np.array_equal(out_bits(d0)[0], out_bits(d1)[0])
+
+
+@pytest.mark.slow
+def test_decode_shape_full_size_sampled():
+    """G=32, cap=4096, N=6144, K=7168, counts ~ Poisson(192): the full-size launch, checked on
+    sampled rows x column blocks that the oracle computes one by one."""
+    w = wl.masked_decode()
+    G, cap, N, K = w.G, w.cap, w.N, w.K
+    a, b = w.draw(device="cuda")
+    cnt = torch.tensor(w.counts, device="cuda")
+    qa, sfa = gpu_quant_tokens(a.view(G * cap, K), DG_SF_FP32, row_counts=cnt)
+    qb, sfb = gpu_quant_blocks(b, DG_SF_FP32)
+    d = sentinel_like((G, cap, N), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dg_m_grouped_fp8_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, 192, DG_SF_FP32, status)
+    sync()
+    assert status.item() == 0
+    rng = np.random.default_rng(5)
+    groups = [g for g in range(G) if w.counts[g] > 0]
+    gpu_vals, ref_vals = [], []
+    for g in rng.choice(groups, 6, replace=False):
+        c = int(w.counts[g])
+        rows = np.unique(np.concatenate([[0, c - 1], rng.integers(0, c, 4)]))
+        for nb in rng.choice(N // 128, 2, replace=False):
+            wb = b[g, nb * 128:(nb + 1) * 128].cpu()
+            oqb, osfb, _ = oracle.quant_block_128x128(wb.unsqueeze(0))
+            np.testing.assert_array_equal(qb[g, nb * 128:(nb + 1) * 128].cpu().numpy(), oqb[0])
+            for r in rows:
+                oqa, osfa, _ = oracle.quant_per_token_1x128(a[g, r:r + 1].cpu())
+                ref = oracle.gemm_masked(oqa.reshape(1, 1, K), osfa.reshape(1, 1, K // 128), oqb, osfb, [1])
+                gpu_vals.append(to_f64(d[g, r, nb * 128:(nb + 1) * 128]))
+                ref_vals.append(ref_out(ref[0, 0], False))
+    assert_close(np.concatenate(gpu_vals), np.concatenate(ref_vals), False, "decode sampled")
+    rows = torch.arange(cap, device="cuda")[None, :]
+    pad = rows >= cnt[:, None]
+    assert bool((d.view(torch.int16)[pad] == -1).all()), "padding rows written"
