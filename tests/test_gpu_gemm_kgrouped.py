@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 
 def test_prologue_descriptors_match_host_encoding():
     lib = _lib.load()
-    for ks, N, H in [([256, 0, 128, 384], 256, 384), ([256, 128, 128, 256], 2048, 2048), ([128] * 40, 128, 128)]:
+    for ks, N, H in [([256, 0, 128, 384], 256, 384), ([256, 128, 128, 256], 2048, 2048), ([128] * 40, 128, 128),
+                     ([128, 1024, 512], 128, 256)]:
         G = len(ks)
         K_cap = sum(ks) + 128
         ap = torch.empty(K_cap * N, dtype=torch.uint8, device="cuda")
