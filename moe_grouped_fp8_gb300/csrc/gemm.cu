@@ -1026,14 +1026,17 @@ int check_kgrouped(const uint8_t* a_packed, const float* sfa, const uint8_t* b_p
 }  // namespace
 }  // namespace dg
 
-extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
-                                      const float* sfb, const float* c, float* d, const int32_t* ks, int G,
-                                      int64_t K_cap, int64_t N, int64_t H, void* workspace, size_t workspace_bytes,
-                                      int32_t* status, void* stream) {
+namespace dg {
+namespace {
+
+// The two launches of a k-grouped call: the descriptor prologue (skipped when `prologue` is
+// false, i.e. the workspace already holds this call's descriptors) and the GEMM.
+int kgrouped_launch(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, const float* sfb,
+                    const float* c, float* d, const int32_t* ks, int G, int64_t K_cap, int64_t N, int64_t H,
+                    void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t s, bool prologue) {
     if (int rc = check_kgrouped(a_packed, sfa, b_packed, sfb, d, ks, G, K_cap, N, H, workspace, workspace_bytes))
         return rc;
     DG_CHECK_ARG(c == nullptr || aligned16(c), "c must be 16-byte aligned");
-    auto s = static_cast<cudaStream_t>(stream);
     auto* ws = static_cast<CUtensorMap*>(workspace);
     KgTemplates tmpl;
     if (int rc = kgrouped_templates(a_packed, b_packed, N, H, &tmpl)) return rc;
@@ -1048,8 +1051,10 @@ extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
             return rc;
     }
-    k_kgrouped_prologue<<<1, 256, 0, s>>>(tmpl, a_packed, b_packed, ks, G, K_cap, N, H, ws);
-    DG_CHECK_CUDA(cudaGetLastError());
+    if (prologue) {
+        k_kgrouped_prologue<<<1, 256, 0, s>>>(tmpl, a_packed, b_packed, ks, G, K_cap, N, H, ws);
+        DG_CHECK_CUDA(cudaGetLastError());
+    }
     GemmArgs args{};
     args.routing = ks;
     args.sfa = sfa;
@@ -1069,6 +1074,17 @@ extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa,
     return launch_gemm<Layout::KGrouped, KG_BN, KG_STAGES, true, false>(tD, tD, tD, tD, tC, args, s);
 }
 
+}  // namespace
+}  // namespace dg
+
+extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
+                                      const float* sfb, const float* c, float* d, const int32_t* ks, int G,
+                                      int64_t K_cap, int64_t N, int64_t H, void* workspace, size_t workspace_bytes,
+                                      int32_t* status, void* stream) {
+    return kgrouped_launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes,
+                           status, static_cast<cudaStream_t>(stream), true);
+}
+
 // ------------------------------------------------------------------------- test hooks
 // Launch only the k-grouped descriptor prologue, and host-encode the descriptors it should
 // produce, so that a test can compare the two byte for byte before any TMA uses them.
@@ -1082,6 +1098,16 @@ extern "C" int dg_testing_kgrouped_prologue(const uint8_t* a_packed, const uint8
         tmpl, a_packed, b_packed, ks, G, K_cap, N, H, static_cast<CUtensorMap*>(workspace));
     DG_CHECK_CUDA(cudaGetLastError());
     return DG_OK;
+}
+
+// The GEMM launch of dg_k_grouped_fp8_wgrad alone, reading the descriptors that an earlier
+// call with the same operands left in the workspace (used to time the kernel by itself).
+extern "C" int dg_testing_kgrouped_gemm_only(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
+                                             const float* sfb, const float* c, float* d, const int32_t* ks, int G,
+                                             int64_t K_cap, int64_t N, int64_t H, void* workspace,
+                                             size_t workspace_bytes, int32_t* status, void* stream) {
+    return kgrouped_launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes,
+                           status, static_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" int dg_testing_kgrouped_host_maps(const uint8_t* a_packed, const uint8_t* b_packed,
