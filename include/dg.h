@@ -165,6 +165,31 @@ int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa, const uint
                            int64_t K_cap, int64_t N, int64_t H, void* workspace,
                            size_t workspace_bytes, int32_t* status, void* stream);
 
+/* Largest G accepted by dg_k_grouped_fp8_wgrad_noalloc. */
+#define DG_NOALLOC_MAX_GROUPS 256
+
+/*
+ * dg_k_grouped_fp8_wgrad without a workspace.  This entry point has no counterpart on the
+ * source pages; it exists for callers that cannot allocate device memory when they make the
+ * call: runtimes that carve all device memory into a fixed arena at start-up and forbid later
+ * allocation, serving loops that must not pay cudaMalloc's implicit device-wide
+ * synchronisation, and plain C callers that have no device allocator of their own to provide
+ * the workspace.  The caller still owns and passes every input and output.
+ *   Arguments, layouts, results and status bits are those of dg_k_grouped_fp8_wgrad.
+ *   The per-expert descriptors go to a 64 KiB array compiled into the library
+ *   (2 * DG_NOALLOC_MAX_GROUPS descriptors of 128 bytes), held by every device that loads the
+ *   library until the process exits.  G > DG_NOALLOC_MAX_GROUPS returns DG_ERR_UNSUPPORTED.
+ *   The first call on each device looks up the array's device address (once per device, with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array: calls that may overlap on the GPU (other streams, other
+ *   host threads) race on it and must be serialised by the caller.  Every descriptor a call
+ *   reads is rewritten by that same call, so nothing is carried over from the previous call.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+int dg_k_grouped_fp8_wgrad_noalloc(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
+                                   const float* sfb, const float* c, float* d, const int32_t* ks, int G,
+                                   int64_t K_cap, int64_t N, int64_t H, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

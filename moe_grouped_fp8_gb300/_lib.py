@@ -20,6 +20,7 @@ DG_STATUS_TOO_MANY_RUNS = 32
 DG_OP_M_GROUPED_CONTIGUOUS, DG_OP_M_GROUPED_MASKED, DG_OP_K_GROUPED_WGRAD = 0, 1, 2
 DG_MAX_GROUPS = 1024
 DG_MAX_M_BLOCKS = 4096
+DG_NOALLOC_MAX_GROUPS = 256
 
 # name -> (restype, argtypes); every symbol include/dg.h declares
 P, I64, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -32,6 +33,7 @@ SIGNATURES = {
     "dg_m_grouped_fp8_contiguous": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, I32, P, SZ, P, P]),
     "dg_m_grouped_fp8_masked": (I32, [P, P, P, P, P, I32, P, I32, I64, I64, I64, I32, I32, P, SZ, P, P]),
     "dg_k_grouped_fp8_wgrad": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
+    "dg_k_grouped_fp8_wgrad_noalloc": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, P]),
 }
 # test hooks exported by the library (not part of include/dg.h)
 TESTING_SIGNATURES = {

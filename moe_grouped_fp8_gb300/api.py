@@ -16,6 +16,7 @@ from ._lib import DG_OP_K_GROUPED_WGRAD, DG_OUT_BF16, DG_OUT_FP32, DG_SF_FP32, D
 __all__ = [
     "dg_quant_per_token_1x128", "dg_quant_per_channel_128", "dg_quant_block_128x128",
     "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad",
+    "dg_k_grouped_fp8_wgrad_noalloc",
     "dg_workspace_size", "dg_last_error", "sfa_padded_rows", "empty_sfa", "kgrouped_workspace", "DGError",
 ]
 
@@ -160,3 +161,19 @@ def dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, worksp
     ws_bytes = workspace.numel() * workspace.element_size()
     check(load().dg_k_grouped_fp8_wgrad(_p(a_packed), _p(sfa), _p(b_packed), _p(sfb), _p(c), _p(d), _p(ks), G, K_cap,
                                         N, H, _p(workspace), ws_bytes, _p(status), _s(stream)))
+
+
+def dg_k_grouped_fp8_wgrad_noalloc(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, status=None, stream=None):
+    """dg_k_grouped_fp8_wgrad for callers that cannot allocate device memory: no workspace
+    argument; the library's built-in descriptor scratch (at most DG_NOALLOC_MAX_GROUPS experts)
+    is shared by all calls, so calls that may overlap on the GPU must be serialised."""
+    _dev(a_packed, sfa, b_packed, sfb, c, d, ks, status)
+    G, N, H = d.shape
+    _need(d.dtype == torch.float32 and d.is_contiguous(), "d must be contiguous fp32 [G, N, H]")
+    _need(c is None or (tuple(c.shape) == tuple(d.shape) and c.dtype == torch.float32 and c.is_contiguous()), "c")
+    _need(ks.dtype == torch.int32 and ks.numel() == G, "ks must be int32 [G]")
+    _need(sfa.dtype == torch.float32 and sfa.numel() >= (K_cap // 128) * N, "sfa")
+    _need(sfb.dtype == torch.float32 and sfb.numel() >= (K_cap // 128) * H, "sfb")
+    _need(a_packed.numel() >= K_cap * N and b_packed.numel() >= K_cap * H, "packed operand size")
+    check(load().dg_k_grouped_fp8_wgrad_noalloc(_p(a_packed), _p(sfa), _p(b_packed), _p(sfb), _p(c), _p(d), _p(ks),
+                                                G, K_cap, N, H, _p(status), _s(stream)))

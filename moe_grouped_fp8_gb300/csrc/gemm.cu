@@ -31,6 +31,8 @@
 // written by their owner threads.  Rows that are not valid are never written.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "host_common.hpp"
 #include "ptx.cuh"
 
@@ -1082,6 +1084,58 @@ extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa,
                                       int64_t K_cap, int64_t N, int64_t H, void* workspace, size_t workspace_bytes,
                                       int32_t* status, void* stream) {
     return kgrouped_launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes,
+                           status, static_cast<cudaStream_t>(stream), true);
+}
+
+// ------------------------------------------------------------------------- allocation-free variant
+// dg_k_grouped_fp8_wgrad_noalloc: the same k-grouped call, with its descriptor scratch in a
+// fixed array compiled into the library instead of a caller-provided workspace.  Every device
+// that loads the library holds the array (DG_NOALLOC_MAX_GROUPS experts x two 128-byte
+// descriptors = 64 KiB) until the process exits.
+namespace dg {
+namespace {
+
+static __device__ __align__(256) CUtensorMap g_noalloc_maps[2 * DG_NOALLOC_MAX_GROUPS];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of g_noalloc_maps on the current device.  In host code the array's name only
+// stands in for the symbol, so the address is looked up once per device (with that device
+// current) and cached; the first call on each device does this set-up.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    DG_CHECK_CUDA(cudaGetDevice(&dev));
+    DG_CHECK_SUPPORTED(dev >= 0 && dev < 64, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_maps);
+        if (e != cudaSuccess || p == nullptr)
+            return set_error(DG_ERR_CUDA, "cudaGetSymbolAddress of the built-in descriptor scratch failed: %s",
+                             cudaGetErrorString(e));
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return DG_OK;
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" int dg_k_grouped_fp8_wgrad_noalloc(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
+                                              const float* sfb, const float* c, float* d, const int32_t* ks, int G,
+                                              int64_t K_cap, int64_t N, int64_t H, int32_t* status, void* stream) {
+    DG_CHECK_SUPPORTED(G <= DG_NOALLOC_MAX_GROUPS,
+                       "dg_k_grouped_fp8_wgrad_noalloc handles at most %d experts (its built-in scratch holds %d "
+                       "descriptors); G=%d needs dg_k_grouped_fp8_wgrad with a workspace",
+                       DG_NOALLOC_MAX_GROUPS, 2 * DG_NOALLOC_MAX_GROUPS, G);
+    DG_CHECK_ARG(G >= 1, "G must be >= 1 (%d)", G);
+    void* scratch = nullptr;
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+    // Every expert the GEMM reads gets its descriptors rewritten by this call's prologue, so the
+    // array's contents from an earlier call never need clearing.
+    return kgrouped_launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, scratch, sizeof(g_noalloc_maps),
                            status, static_cast<cudaStream_t>(stream), true);
 }
 
