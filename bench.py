@@ -142,6 +142,20 @@ def profiled_traffic(name: str):
         return None
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks of the default process group (the slowest rank
+    sets the job's step time)."""
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world_size: int, flops_per_step: float, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs the same per-GPU work (weak scaling) in at most
+    ms_per_step milliseconds."""
+    return world_size * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 def time_graphs(graphs, n, stream):
     """Average ms per replay of n replays cycling through `graphs`, CUDA events on `stream`."""
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -470,10 +484,8 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
 
     if ws > 1:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = ws * wk.flops / (ms_step * 1e-3) / 1e12
+        ms_step = max_over_ranks(ms_step, device)
+    value = job_throughput(ws, wk.flops, ms_step)
 
     gemm_bytes = wk.gemm_bytes()
     fp8_peak = peaks["bf16_tflops"] * 2.0  # nominal fp8 : bf16 dense ratio 4.5 : 2.25

@@ -140,7 +140,15 @@ def replay_case(G, N, K, E, replays, check_every, seed):
             step()
     torch.cuda.current_stream().wait_stream(s)
     sync()
-    oqb = osfb = None
+    qcache = {}                                        # expert -> oracle codes/scales of its weights
+
+    def oracle_weights(experts):
+        for e in experts:
+            if e not in qcache:
+                q, sf, _ = oracle.quant_block_128x128(b[e:e + 1].cpu(), ue8m0=True)
+                qcache[e] = (q[0], sf[0])
+        return (np.stack([qcache[e][0] for e in experts]), np.stack([qcache[e][1] for e in experts]))
+
     checked = 0
     for it in range(replays):
         counts = wl.multinomial_counts(T, G, seed + 1 + it)
@@ -157,11 +165,12 @@ def replay_case(G, N, K, E, replays, check_every, seed):
             assert np.all(bits[mi_np < 0] == 0xFFFF), f"replay {it}: padding row written"
             rows = np.nonzero(mi_np >= 0)[0]
             if rows.size:
-                if oqb is None:
-                    oqb, osfb, _ = oracle.quant_block_128x128(b.cpu(), ue8m0=True)
                 pick = np.unique(np.random.default_rng(it).choice(rows, min(24, rows.size), replace=False))
+                experts = sorted(set(int(e) for e in mi_np[pick]))
+                oqb, osfb = oracle_weights(experts)
+                local = np.array([experts.index(int(e)) for e in mi_np[pick]], np.int32)
                 oqa, osfa, _ = oracle.quant_per_token_1x128(a[torch.from_numpy(pick).cuda()].cpu(), ue8m0=True)
-                ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, mi_np[pick])
+                ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, local)
                 assert_close(to_f64(d)[pick], ref_out(ref, False), False, f"replay {it}")
             checked += 1
     assert checked >= replays // check_every
