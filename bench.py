@@ -119,7 +119,7 @@ class ClockSampler:
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ["gemm.cu", "ptx.cuh"]:
+    for f in ["gemm.cu", "kgrouped.cu", "kernel_common.cuh", "ptx.cuh"]:
         h.update(open(os.path.join(ROOT, "moe_grouped_fp8_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

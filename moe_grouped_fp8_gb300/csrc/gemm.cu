@@ -1,13 +1,12 @@
-// gemm.cu - persistent, warp-specialised FP8 (e4m3) grouped GEMM for sm_103a.
+// gemm.cu - persistent, warp-specialised FP8 (e4m3) m-grouped GEMM for sm_103a.
 //
-// One kernel template serves the three layouts of the source pages:
+// One kernel template serves the two m-grouped layouts of the source pages:
 //   Contiguous - rows stacked per expert, routed by m_indices (-1 = padding row), segments
 //                aligned to 128 rows ("SM120 m_grouped_fp8 contiguous kernel: illegal memory
 //                access at CUDA graph replay", #444);
 //   Masked     - [G, cap, K] activations with a valid-row count per expert ("Fix cross-expert
-//                output overwrites in SM90 masked GEMM", #469);
-//   KGrouped   - weight gradient D_e = C_e + A_e^T B_e over per-expert token spans ("Non-
-//                deterministic numerical problem of k_grouped_fp8_gemm_nt_contiguous", #365).
+//                output overwrites in SM90 masked GEMM", #469).
+// (The k-grouped weight-gradient GEMM lives in kgrouped.cu.)
 //
 // Roles (320 threads): warps 0-7 promote and store (TMEM lane quarter = warp % 4, column half
 // = warp / 4), warp 8 issues TMA loads, warp 9 owns tensor memory and issues tcgen05.mma.
@@ -17,28 +16,24 @@
 // and no atomic on outputs, so every call is bitwise reproducible.
 //
 // The tile schedule is rebuilt in shared memory by every CTA from the device-side routing
-// tensor (m_indices / counts / ks) at the start of every launch, and the TMA descriptors of
-// the m-grouped layouts are static kernel parameters, so a CUDA graph replayed after the
-// routing tensor changed in place never uses stale schedule or descriptor state.  The
-// k-grouped per-expert descriptors are rebuilt from ks by a separate launch right before
-// the GEMM on every call; the launch boundary orders every descriptor write before any TMA
-// that reads it.
+// tensor (m_indices / counts) at the start of every launch, and the TMA descriptors are static
+// kernel parameters, so a CUDA graph replayed after the routing tensor changed in place never
+// uses stale schedule or descriptor state.
 //
-// Outputs: the m-grouped epilogue stages the tile in shared memory (128-byte swizzle) and
-// stores rows [0, 8*floor(v/8)) of the tile's v valid leading rows with TMA boxes of 128 or 8
-// rows through a descriptor that keeps the expert dimension (3-D [G, cap, N] for the masked
-// layout), so a store can never cross into the next expert; the remaining valid rows are
-// written by their owner threads.  Rows that are not valid are never written.
+// Outputs: the epilogue stages the tile in shared memory (128-byte swizzle) and stores rows
+// [0, 8*floor(v/8)) of the tile's v valid leading rows with TMA boxes of 128 or 8 rows through a
+// descriptor that keeps the expert dimension (3-D [G, cap, N] for the masked layout), so a store
+// can never cross into the next expert; the remaining valid rows are written by their owner
+// threads.  Rows that are not valid are never written.
 #include <cuda_bf16.h>
 
-#include <mutex>
-
 #include "host_common.hpp"
+#include "kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace dg {
 
-enum class Layout : int { Contiguous = 0, Masked = 1, KGrouped = 2 };
+enum class Layout : int { Contiguous = 0, Masked = 1 };
 
 constexpr int BM = 128;  // rows of a tile (TMEM lanes)
 constexpr int BK = 128;  // K per stage = scale-block size
@@ -51,24 +46,20 @@ constexpr int MAX_RUNS = 1024;
 constexpr int EPI_BAR = 1;  // named barrier of the 256 promotion/store threads
 
 struct GemmArgs {
-    const int32_t* routing;      // m_indices [M] | counts [G] | ks [G]
+    const int32_t* routing;      // m_indices [M] | counts [G]
     const void* sfa;             // see the layout notes of each entry point
     const void* sfb;
     void* d;                     // output base (owner-thread stores of tail rows)
-    const CUtensorMap* ws_maps;  // KGrouped: per-expert A/B descriptors
     int32_t* status;
     uint64_t wait_limit_ns;
-    int64_t M;       // Contiguous: rows; Masked: cap; KGrouped: K_cap
-    int64_t sfa_ld;  // Contiguous/Masked: Mp; KGrouped: N
+    int64_t M;       // Contiguous: rows; Masked: cap
+    int64_t sfa_ld;  // Mp of the [K/128][Mp] activation scales
     int64_t ldd;     // output row length in elements
     int G;
     int K;           // m-grouped K
     int KB;          // m-grouped K / 128
     int num_nb;      // output column tiles
-    int num_mb_k;    // KGrouped: N / 128
     int n128;        // m-grouped N / 128 (sfb row count)
-    int sfb_ld;      // KGrouped: H
-    int c_mode;      // KGrouped: 0 no C, 1 separate C, 2 C aliases D
 };
 
 template <Layout L, int BN, int STAGES, bool OUT_FP32>
@@ -86,7 +77,7 @@ struct Plan {
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
     static constexpr int SCHED_BYTES = (MAX_RUNS + 1) * 4 + 4 * MAX_RUNS * 4;
     static constexpr int BAR_OFF = (SCHED_OFF + SCHED_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
-    static constexpr int NUM_BARS = 2 * STAGES + 6;
+    static constexpr int NUM_BARS = 2 * STAGES + 4;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int MISC_BYTES = 256;
     static constexpr int TOTAL = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
@@ -95,80 +86,17 @@ struct Plan {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
     static_assert(CPT % 32 == 0, "promotion threads read 32-column groups");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
-    static_assert(L != Layout::KGrouped || OUT_FP32, "k-grouped output is fp32");
     static_assert(STG_OFF % 1024 == 0 && SCHED_OFF % 1024 == 0, "TMA / swizzle buffers are 1024-byte aligned");
     static_assert(BAR_OFF % 8 == 0 && MISC_OFF % 8 == 0, "mbarrier objects are 8-byte aligned");
 };
 
 // ------------------------------------------------------------------------- small helpers
 
-__device__ __forceinline__ float ue8m0_to_float(uint8_t b) {
-    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(b) << 23);
-}
-
-// Exclusive prefix sum of one int per thread over the whole CTA (NUM_THREADS threads).
-__device__ int cta_excl_scan(int v, int* scratch, int* total) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) scratch[wid] = incl;
-    __syncthreads();
-    int pre = 0, tot = 0;
-#pragma unroll
-    for (int i = 0; i < NUM_WARPS; ++i) {
-        const int w = scratch[i];
-        pre += (i < wid) ? w : 0;
-        tot += w;
-    }
-    __syncthreads();
-    *total = tot;
-    return pre + incl - v;
-}
-
-// OR-reduction across the promotion warps at a named barrier (uniform result).
-__device__ __forceinline__ bool epi_bar_or(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}\n"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(EPI_BAR), "r"(NUM_EPI_WARPS * 32)
-        : "memory");
-    return r != 0;
-}
-
-// Largest r with prefix[r] <= t (prefix is non-decreasing, prefix[0] = 0 <= t).
-__device__ __forceinline__ int find_run(const int* prefix, int R, int t) {
-    int lo = 0, hi = R - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-// Wait used when draining copies in flight on the way out: bounded, ignores the abort flag.
-__device__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > limit_ns) return;
-    }
-}
-
 struct TileInfo {
     int e;        // expert / group
     int nb;       // output column tile
-    int row0;     // first row of the tile: Contiguous global row, Masked row within the group,
-                  // KGrouped row n of D_e
+    int row0;     // first row of the tile: Contiguous global row, Masked row within the group
     int valid;    // Masked: valid rows of the tile (<= 128)
-    int k_off;    // KGrouped: token offset of the expert
     int kbt;      // 128-K blocks of this tile
 };
 
@@ -183,19 +111,13 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
     ti.nb = nb;
     ti.e = run_e[r];
     ti.valid = 0;
-    ti.k_off = 0;
+    ti.kbt = a.KB;
     if constexpr (L == Layout::Contiguous) {
         ti.row0 = (run_first[r] + j) * BM;
-        ti.kbt = a.KB;
-    } else if constexpr (L == Layout::Masked) {
+    } else {
         ti.row0 = j * BM;
         const int v = run_x[r] - ti.row0;
         ti.valid = v < BM ? v : BM;
-        ti.kbt = a.KB;
-    } else {
-        ti.row0 = j * BM;
-        ti.k_off = run_first[r];
-        ti.kbt = run_x[r] / BK;
     }
     return ti;
 }
@@ -203,10 +125,10 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
 // ------------------------------------------------------------------------- the kernel
 
 template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0>
-__global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD8,
-                   const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
+                   const GemmArgs a) {
     using P = Plan<L, BN, STAGES, OUT_FP32>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -224,13 +146,10 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 2;
-    uint64_t* cfull = tempty + 2;
-    uint64_t* sfree = cfull + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + P::MISC_OFF + 4);
     int* s_nruns = reinterpret_cast<int*>(smem + P::MISC_OFF + 8);
     int* s_ntiles = reinterpret_cast<int*>(smem + P::MISC_OFF + 12);
-    int* s_misc = reinterpret_cast<int*>(smem + P::MISC_OFF + 16);  // first bad expert
     uint32_t* s_ballot = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF + 32);  // [2][4]
     int* s_scan = reinterpret_cast<int*>(smem + P::MISC_OFF + 64);              // [NUM_WARPS]
 
@@ -248,10 +167,7 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], NUM_EPI_WARPS);
         }
-        mbar_init(cfull, 1);
-        mbar_init(sfree, 1);
         *s_abort = 0;
-        s_misc[0] = 0x7fffffff;
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
@@ -260,15 +176,10 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
         tc_fence_before();
     }
     if (warp == PRODUCER_WARP && lane == 0) {
-        if constexpr (L != Layout::KGrouped) {
-            prefetch_tmap(&tmA);
-            prefetch_tmap(&tmB);
-            prefetch_tmap(&tmD);
-            prefetch_tmap(&tmD8);
-        } else {
-            prefetch_tmap(&tmD);
-            if (a.c_mode != 0) prefetch_tmap(&tmC);
-        }
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmD);
+        prefetch_tmap(&tmD8);
     }
     __syncthreads();
 
@@ -307,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
             cnt += (e >= 0 && (b == 0 || blk_e[b - 1] != e)) ? 1 : 0;
         }
         int total = 0;
-        int r = cta_excl_scan(cnt, s_scan, &total);
+        int r = cta_excl_scan<NUM_THREADS>(cnt, s_scan, &total);
         for (int b = lo; b < hi; ++b) {
             const int e = blk_e[b];
             if (e >= 0 && (b == 0 || blk_e[b - 1] != e)) {
@@ -324,7 +235,7 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
             cnt2 += (e >= 0 && (b == nblk - 1 || blk_e[b + 1] != e)) ? 1 : 0;
         }
         int total2 = 0;
-        int r2 = cta_excl_scan(cnt2, s_scan, &total2);  // its barriers order the s_first writes
+        int r2 = cta_excl_scan<NUM_THREADS>(cnt2, s_scan, &total2);  // its barriers order the s_first writes
         for (int b = lo; b < hi; ++b) {
             const int e = blk_e[b];
             if (e >= 0 && (b == nblk - 1 || blk_e[b + 1] != e)) {
@@ -338,39 +249,6 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
             R = MAX_RUNS;
         }
         __syncthreads();
-    } else {  // KGrouped
-        R = a.G;
-        const int ch = (a.G + NUM_THREADS - 1) / NUM_THREADS;
-        const int lo = tid * ch, hi = min(a.G, lo + ch);
-        int sum = 0;
-        for (int e = lo; e < hi; ++e) {
-            const int k = a.routing[e];
-            if (!(k < 0 || (k % BK) != 0)) sum += k;
-        }
-        int total = 0;
-        int o = cta_excl_scan(sum, s_scan, &total);
-        for (int e = lo; e < hi; ++e) {
-            const int k = a.routing[e];
-            int bits = 0;
-            if (k < 0 || (k % BK) != 0) bits = DG_STATUS_K_NOT_ALIGNED;
-            else if (static_cast<int64_t>(o) + k > a.M) bits = DG_STATUS_K_OVERFLOW;
-            s_first[e] = o;
-            s_x[e] = bits ? 0 : k;
-            s_e[e] = e;
-            s_L[e] = a.num_mb_k;
-            if (bits) {
-                atomicMin(&s_misc[0], e);
-                if (blockIdx.x == 0) status_or(a.status, bits);
-            }
-            if (k >= 0 && (k % BK) == 0) o += k;
-        }
-        __syncthreads();
-        const int first_bad = s_misc[0];
-        for (int e = tid; e < a.G; e += NUM_THREADS) {
-            const bool live = e < first_bad && (s_x[e] > 0 || a.c_mode != 2);
-            if (!live) s_L[e] = 0;
-        }
-        __syncthreads();
     }
     {
         // tiles per run -> prefix (runs of zero tiles keep L = 0)
@@ -379,7 +257,7 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
         int sum = 0;
         for (int r = lo; r < hi; ++r) sum += s_L[r] * a.num_nb;
         int total = 0;
-        int p = cta_excl_scan(sum, s_scan, &total);
+        int p = cta_excl_scan<NUM_THREADS>(sum, s_scan, &total);
         for (int r = lo; r < hi; ++r) {
             s_prefix[r] = p;
             p += s_L[r] * a.num_nb;
@@ -401,51 +279,21 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
-            uint32_t cpar = 0;
-            int c_issued = 0;
-            int last_e = -1;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile<L>(t, s_prefix, s_first, s_L, s_e, s_x, R, a);
-                const void* mapA = &tmA;
-                const void* mapB = &tmB;
-                if constexpr (L == Layout::KGrouped) {
-                    mapA = a.ws_maps + 2 * ti.e;
-                    mapB = a.ws_maps + 2 * ti.e + 1;
-                    if (ti.e != last_e && ti.kbt > 0) {
-                        tmap_acquire(mapA);
-                        tmap_acquire(mapB);
-                        last_e = ti.e;
-                    }
-                }
                 for (int kb = 0; kb < ti.kbt; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     uint8_t* sa = ring + stage * P::STAGE_BYTES;
                     uint8_t* sb = sa + P::A_BYTES;
                     mbar_arrive_expect_tx(&full[stage], P::STAGE_BYTES);
-                    if constexpr (L == Layout::Masked) {
-                        tma_load_3d(sa, mapA, &full[stage], kb * BK, ti.row0, ti.e);
-                        tma_load_3d(sb, mapB, &full[stage], kb * BK, ti.nb * BN, ti.e);
-                    } else if constexpr (L == Layout::Contiguous) {
-                        tma_load_2d(sa, mapA, &full[stage], kb * BK, ti.row0);
-                        tma_load_3d(sb, mapB, &full[stage], kb * BK, ti.nb * BN, ti.e);
-                    } else {
-                        tma_load_2d(sa, mapA, &full[stage], kb * BK, ti.row0);
-                        tma_load_2d(sb, mapB, &full[stage], kb * BK, ti.nb * BN);
-                    }
+                    if constexpr (L == Layout::Masked)
+                        tma_load_3d(sa, &tmA, &full[stage], kb * BK, ti.row0, ti.e);
+                    else
+                        tma_load_2d(sa, &tmA, &full[stage], kb * BK, ti.row0);
+                    tma_load_3d(sb, &tmB, &full[stage], kb * BK, ti.nb * BN, ti.e);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-                if constexpr (L == Layout::KGrouped) {
-                    if (ok && a.c_mode != 0) {
-                        if (!mbar_wait(sfree, cpar ^ 1u, wc)) { ok = false; break; }
-                        mbar_arrive_expect_tx(cfull, P::STG_BYTES);
-                        for (int c = 0; c < P::CHUNKS; ++c)
-                            tma_load_3d(stg + c * P::CHUNK_BYTES, &tmC, cfull, ti.nb * BN + c * (128 / P::ESIZE),
-                                        ti.row0, ti.e);
-                        ++c_issued;
-                        cpar ^= 1u;
-                    }
                 }
             }
             // drain: every load this thread issued has landed before the CTA may exit
@@ -456,7 +304,6 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
                 while (s < 0) { s += STAGES; ph ^= 1u; }
                 drain_wait(&full[s], ph, a.wait_limit_ns);
             }
-            if (c_issued > 0) drain_wait(cfull, cpar ^ 1u, a.wait_limit_ns);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
@@ -503,7 +350,6 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         int tb = 0;
         uint32_t tphase = 0;
-        uint32_t cpar = 0;
         bool have_store = false;
         int parity_slot = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -514,16 +360,13 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
             if constexpr (L == Layout::Masked) {
                 row_ok = row < ti.valid;
                 grow = static_cast<int64_t>(ti.e) * a.M + ti.row0 + row;
-            } else if constexpr (L == Layout::Contiguous) {
+            } else {
                 grow = static_cast<int64_t>(ti.row0) + row;
                 const int mi = grow < a.M ? a.routing[grow] : -1;
                 row_ok = (mi == ti.e);
                 if (mi >= 0 && mi != ti.e) status_or(a.status, DG_STATUS_BAD_INDEX);
                 const uint32_t bal = __ballot_sync(0xffffffffu, row_ok);
                 if (h2 == 0 && lane == 0) s_ballot[parity_slot * 4 + q] = bal;
-            } else {
-                row_ok = true;
-                grow = ti.row0 + row;  // n
             }
 
             float acc[P::CPT];
@@ -532,33 +375,17 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
 
             for (int kb = 0; kb < ti.kbt; ++kb) {
                 float s = 0.0f;
-                float sbc[P::CPT];
-                if constexpr (L != Layout::KGrouped) {
-                    if (row_ok) {
-                        float sa, sb;
-                        const int sbi = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB + kb;
-                        if constexpr (SF_UE8M0) {
-                            sa = ue8m0_to_float(static_cast<const uint8_t*>(a.sfa)[kb * a.sfa_ld + grow]);
-                            sb = ue8m0_to_float(static_cast<const uint8_t*>(a.sfb)[sbi]);
-                        } else {
-                            sa = static_cast<const float*>(a.sfa)[kb * a.sfa_ld + grow];
-                            sb = static_cast<const float*>(a.sfb)[sbi];
-                        }
-                        s = sa * sb;
+                if (row_ok) {
+                    float sa, sb;
+                    const int sbi = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB + kb;
+                    if constexpr (SF_UE8M0) {
+                        sa = ue8m0_to_float(static_cast<const uint8_t*>(a.sfa)[kb * a.sfa_ld + grow]);
+                        sb = ue8m0_to_float(static_cast<const uint8_t*>(a.sfb)[sbi]);
+                    } else {
+                        sa = static_cast<const float*>(a.sfa)[kb * a.sfa_ld + grow];
+                        sb = static_cast<const float*>(a.sfb)[sbi];
                     }
-                } else {
-                    const int64_t kbg = ti.k_off / BK + kb;
-                    s = static_cast<const float*>(a.sfa)[kbg * a.sfa_ld + grow];
-                    const float4* sbp = reinterpret_cast<const float4*>(static_cast<const float*>(a.sfb) +
-                                                                        kbg * a.sfb_ld + ti.nb * BN + h2 * P::CPT);
-#pragma unroll
-                    for (int i = 0; i < P::CPT / 4; ++i) {
-                        const float4 v = sbp[i];
-                        sbc[4 * i] = s * v.x;
-                        sbc[4 * i + 1] = s * v.y;
-                        sbc[4 * i + 2] = s * v.z;
-                        sbc[4 * i + 3] = s * v.w;
-                    }
+                    s = sa * sb;
                 }
                 if (!mbar_wait(&tfull[tb], tphase, wc)) { failed = true; break; }
                 tc_fence_after();
@@ -568,12 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
                     tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32), v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        if constexpr (L != Layout::KGrouped)
-                            acc[c2 * 32 + i] = fmaf(s, __uint_as_float(v[i]), acc[c2 * 32 + i]);
-                        else
-                            acc[c2 * 32 + i] = fmaf(sbc[c2 * 32 + i], __uint_as_float(v[i]), acc[c2 * 32 + i]);
-                    }
+                    for (int i = 0; i < 32; ++i) acc[c2 * 32 + i] = fmaf(s, __uint_as_float(v[i]), acc[c2 * 32 + i]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -582,14 +404,8 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
             }
 
             // ---- stage the tile in shared memory
-            const bool use_c = (L == Layout::KGrouped) && a.c_mode != 0;
-            if (use_c) {
-                if (!failed && !mbar_wait(cfull, cpar, wc)) failed = true;
-                cpar ^= 1u;
-            } else {
-                if (tid == 0 && have_store) bulk_wait_read_all();
-                named_bar_sync(EPI_BAR, NUM_EPI_WARPS * 32);
-            }
+            if (tid == 0 && have_store) bulk_wait_read_all();  // the previous store has read the staging
+            named_bar_sync(EPI_BAR, NUM_EPI_WARPS * 32);
             if (!failed) {
                 constexpr int PIECES = P::CPT * P::ESIZE / 16;
 #pragma unroll
@@ -598,15 +414,8 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
                     const int chunk = off >> 7, j = (off & 127) >> 4;
                     uint8_t* dst = stg + chunk * P::CHUNK_BYTES + row * 128 + ((j ^ (row & 7)) << 4);
                     if constexpr (OUT_FP32) {
-                        float4 v = make_float4(acc[4 * p], acc[4 * p + 1], acc[4 * p + 2], acc[4 * p + 3]);
-                        if (use_c) {
-                            const float4 c = *reinterpret_cast<const float4*>(dst);
-                            v.x += c.x;
-                            v.y += c.y;
-                            v.z += c.z;
-                            v.w += c.w;
-                        }
-                        *reinterpret_cast<float4*>(dst) = v;
+                        *reinterpret_cast<float4*>(dst) =
+                            make_float4(acc[4 * p], acc[4 * p + 1], acc[4 * p + 2], acc[4 * p + 3]);
                     } else {
                         uint32_t w[4];
 #pragma unroll
@@ -619,13 +428,13 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
                 }
             }
             fence_async_smem();
-            if (epi_bar_or(failed || *s_abort != 0)) break;
+            if (bar_or(EPI_BAR, NUM_EPI_WARPS * 32, failed || *s_abort != 0)) break;
 
             // ---- store: TMA for the leading 8-row-aligned valid rows, owner threads for the rest
             int v = BM;
             if constexpr (L == Layout::Masked) {
                 v = ti.valid;
-            } else if constexpr (L == Layout::Contiguous) {
+            } else {
                 v = 0;
                 for (int qq = 0; qq < 4; ++qq) {
                     const uint32_t bal = s_ballot[parity_slot * 4 + qq];
@@ -655,13 +464,8 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
                     bulk_commit();
                     have_store = true;
                 }
-                if (use_c) {
-                    bulk_wait_read_all();
-                    mbar_arrive(sfree);
-                }
             }
-            if constexpr (L != Layout::KGrouped) {
-                if (row_ok && row >= v8) {
+            if (row_ok && row >= v8) {
                     uint8_t* dst = static_cast<uint8_t*>(a.d) +
                                    ((grow * a.ldd) + ti.nb * BN + h2 * P::CPT) * static_cast<int64_t>(P::ESIZE);
                     constexpr int PIECES = P::CPT * P::ESIZE / 16;
@@ -681,7 +485,6 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
                             *reinterpret_cast<uint4*>(dst + 16 * p) = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
-                }
             }
             parity_slot ^= 1;
         }
@@ -696,138 +499,26 @@ __global__ void __launch_bounds__(NUM_THREADS, (L == Layout::KGrouped) ? 2 : 1)
     }
 }
 
-// ------------------------------------------------------------------------- k-grouped prologue
-// Builds, for every valid expert e, the TMA descriptors of its packed operands from host-built
-// templates: A_e = [N rows, K_e bytes] at a_packed + o_e*N and B_e = [H rows, K_e bytes] at
-// b_packed + o_e*H.  The descriptors are edited in shared memory (tensormap.replace) and
-// published to the workspace with a release fence of the tensor-map proxy.
-//
-// The driver's encoder also records a size class in the descriptor (set when the tensor spans
-// at least 128 KiB) that tensormap.replace does not recompute, so each operand comes with two
-// templates, one per size class, and every expert starts from the template of its own class:
-// the published descriptors then equal the host encoder's output byte for byte.
-constexpr int64_t TMAP_LARGE_BYTES = 131072;
-
-struct KgTemplates {
-    CUtensorMap a_small, a_large, b_small, b_large;
-};
-
-__global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant__ KgTemplates tmpl,
-                                                           const uint8_t* a_packed, const uint8_t* b_packed,
-                                                           const int32_t* ks, int G, int64_t K_cap, int64_t N,
-                                                           int64_t H, CUtensorMap* ws) {
-    __shared__ __align__(128) CUtensorMap s_maps[8][2];
-    __shared__ long long s_warp[8];
-    __shared__ long long s_carry;
-    __shared__ int s_first_bad;
-    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    if (t == 0) {
-        s_carry = 0;
-        s_first_bad = 0x7fffffff;
-    }
-    __syncthreads();
-    for (int base = 0; base < G; base += blockDim.x) {
-        const int e = base + t;
-        const long long k = (e < G) ? ks[e] : 0;
-        bool bad = (e < G) && (k < 0 || (k % BK) != 0);
-        const long long kk = bad ? 0 : k;
-        long long incl = kk;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) s_warp[wid] = incl;
-        __syncthreads();
-        long long pre = s_carry;
-        for (int i = 0; i < wid; ++i) pre += s_warp[i];
-        const long long o_e = pre + incl - kk;
-        if (e < G && !bad && o_e + kk > K_cap) bad = true;
-        if (bad) atomicMin(&s_first_bad, e);
-        __syncthreads();
-        const bool live = e < G && e < s_first_bad && kk > 0;
-        // each warp publishes the descriptors of its own 32 experts, one at a time
-        unsigned live_mask = __ballot_sync(0xffffffffu, live);
-        while (live_mask) {
-            const int src = __ffs(live_mask) - 1;
-            live_mask &= live_mask - 1;
-            const long long o_src = __shfl_sync(0xffffffffu, o_e, src);
-            const long long k_src = __shfl_sync(0xffffffffu, kk, src);
-            const int e_src = base + wid * 32 + src;
-            if (lane == 0) {
-                s_maps[wid][0] = (k_src * N >= TMAP_LARGE_BYTES) ? tmpl.a_large : tmpl.a_small;
-                s_maps[wid][1] = (k_src * H >= TMAP_LARGE_BYTES) ? tmpl.b_large : tmpl.b_small;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t ma = smem_u32(&s_maps[wid][0]);
-                const uint32_t mb = smem_u32(&s_maps[wid][1]);
-                const uint64_t ga = reinterpret_cast<uint64_t>(a_packed + o_src * N);
-                const uint64_t gb = reinterpret_cast<uint64_t>(b_packed + o_src * H);
-                const uint32_t kd = static_cast<uint32_t>(k_src);
-                const uint64_t ks_bytes = static_cast<uint64_t>(k_src);
-                asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(ma), "l"(ga)
-                             : "memory");
-                asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 0, %1;" ::"r"(ma), "r"(kd)
-                             : "memory");
-                asm volatile("tensormap.replace.tile.global_stride.shared::cta.b1024.b64 [%0], 0, %1;" ::"r"(ma),
-                             "l"(ks_bytes)
-                             : "memory");
-                asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(mb), "l"(gb)
-                             : "memory");
-                asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 0, %1;" ::"r"(mb), "r"(kd)
-                             : "memory");
-                asm volatile("tensormap.replace.tile.global_stride.shared::cta.b1024.b64 [%0], 0, %1;" ::"r"(mb),
-                             "l"(ks_bytes)
-                             : "memory");
-            }
-            __syncwarp();
-            asm volatile(
-                "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], "
-                "128;" ::"l"(reinterpret_cast<uint64_t>(ws + 2 * e_src)),
-                "r"(smem_u32(&s_maps[wid][0]))
-                : "memory");
-            asm volatile(
-                "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], "
-                "128;" ::"l"(reinterpret_cast<uint64_t>(ws + 2 * e_src + 1)),
-                "r"(smem_u32(&s_maps[wid][1]))
-                : "memory");
-            __syncwarp();
-        }
-        __syncthreads();
-        if (t == 0) {
-            long long tot = 0;
-            for (int i = 0; i < 8; ++i) tot += s_warp[i];
-            s_carry += tot;
-        }
-        __syncthreads();
-        if (s_first_bad != 0x7fffffff) break;
-    }
-}
-
 // ------------------------------------------------------------------------- host launchers
 
 namespace {
 
 template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0>
 int launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
-                const CUtensorMap& tC, const GemmArgs& args, cudaStream_t stream) {
+                const GemmArgs& args, cudaStream_t stream) {
     using P = Plan<L, BN, STAGES, OUT_FP32>;
     auto kern = k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0>;
     // The attribute is per device: set it on every call (cheap, host-only, capture-safe).
     DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL));
     int sms = 0;
     if (int rc = device_sm_count(&sms)) return rc;
-    const int per_sm = (L == Layout::KGrouped) ? 2 : 1;
-    kern<<<sms * per_sm, NUM_THREADS, P::TOTAL, stream>>>(tA, tB, tD, tD8, tC, args);
+    kern<<<sms, NUM_THREADS, P::TOTAL, stream>>>(tA, tB, tD, tD8, args);
     DG_CHECK_CUDA(cudaGetLastError());
     return DG_OK;
 }
 
 constexpr int MG_BN = 128;
 constexpr int MG_STAGES = 4;
-constexpr int KG_BN = 64;
-constexpr int KG_STAGES = 2;
 
 CUtensorMapDataType out_tmap_type(int out) {
     return out == DG_OUT_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -836,13 +527,12 @@ CUtensorMapDataType out_tmap_type(int out) {
 template <Layout L>
 int dispatch_mgrouped(int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD,
                       const CUtensorMap& tD8, const GemmArgs& args, cudaStream_t s) {
-    const CUtensorMap& tC = tA;  // unused by the m-grouped layouts
     if (out == DG_OUT_FP32) {
-        if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, true, true>(tA, tB, tD, tD8, tC, args, s);
-        return launch_gemm<L, MG_BN, MG_STAGES, true, false>(tA, tB, tD, tD8, tC, args, s);
+        if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, true, true>(tA, tB, tD, tD8, args, s);
+        return launch_gemm<L, MG_BN, MG_STAGES, true, false>(tA, tB, tD, tD8, args, s);
     }
-    if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, false, true>(tA, tB, tD, tD8, tC, args, s);
-    return launch_gemm<L, MG_BN, MG_STAGES, false, false>(tA, tB, tD, tD8, tC, args, s);
+    if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, false, true>(tA, tB, tD, tD8, args, s);
+    return launch_gemm<L, MG_BN, MG_STAGES, false, false>(tA, tB, tD, tD8, args, s);
 }
 
 int check_common_mg(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d, int out,
@@ -980,210 +670,4 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
     args.n128 = static_cast<int>(N / 128);
     return dispatch_mgrouped<Layout::Contiguous>(out_dtype, sf_format, tA, tB, tD, tD8, args,
                                                  static_cast<cudaStream_t>(stream));
-}
-
-namespace dg {
-namespace {
-
-// Host-encoded templates of the per-expert operand descriptors: [rows, K] K-major with a
-// 128x128 (A) or 128xKG_BN (B) box.  The "small" template spans 128 tokens; the "large" one
-// spans the smallest multiple of 128 tokens that reaches TMAP_LARGE_BYTES.  The prologue
-// replaces address, K_e and the row stride.
-int encode_kg_template(CUtensorMap* tm, const uint8_t* base, int64_t rows, int64_t k, uint32_t box_rows) {
-    uint64_t dims[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(rows)};
-    uint64_t str[1] = {static_cast<uint64_t>(k)};
-    uint32_t box[2] = {BK, box_rows};
-    return encode_tmap(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-int64_t large_class_k(int64_t rows) {
-    int64_t k = (TMAP_LARGE_BYTES + rows - 1) / rows;
-    k = (k + BK - 1) / BK * BK;
-    return k < BK ? BK : k;
-}
-
-int kgrouped_templates(const uint8_t* a_packed, const uint8_t* b_packed, int64_t N, int64_t H, KgTemplates* t) {
-    if (int rc = encode_kg_template(&t->a_small, a_packed, N, BK, BM)) return rc;
-    if (int rc = encode_kg_template(&t->a_large, a_packed, N, large_class_k(N), BM)) return rc;
-    if (int rc = encode_kg_template(&t->b_small, b_packed, H, BK, KG_BN)) return rc;
-    return encode_kg_template(&t->b_large, b_packed, H, large_class_k(H), KG_BN);
-}
-
-int check_kgrouped(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, const float* sfb, float* d,
-                   const int32_t* ks, int G, int64_t K_cap, int64_t N, int64_t H, void* workspace,
-                   size_t workspace_bytes) {
-    DG_CHECK_ARG(G >= 1 && G <= DG_MAX_GROUPS, "G must be in [1, %d] (%d)", DG_MAX_GROUPS, G);
-    DG_CHECK_ARG(N > 0 && H > 0 && N % 128 == 0 && H % 128 == 0, "N and H must be positive multiples of 128");
-    DG_CHECK_ARG(K_cap >= 0 && K_cap % 128 == 0, "K_cap must be a multiple of 128");
-    DG_CHECK_ARG(a_packed && sfa && b_packed && sfb && d && ks, "null pointer argument");
-    DG_CHECK_ARG(workspace && workspace_bytes >= dg_workspace_size(DG_OP_K_GROUPED_WGRAD, G, 0, N, H),
-                 "workspace of dg_workspace_size(DG_OP_K_GROUPED_WGRAD, ...) bytes required");
-    DG_CHECK_ARG((reinterpret_cast<uintptr_t>(workspace) & 127u) == 0, "workspace must be 128-byte aligned");
-    DG_CHECK_ARG(aligned16(a_packed) && aligned16(b_packed) && aligned16(d) && aligned16(sfa) && aligned16(sfb),
-                 "operands and scales must be 16-byte aligned");
-    DG_CHECK_SUPPORTED(N <= (1 << 24) && H <= (1 << 24) && K_cap < (1ll << 31), "sizes too large");
-    return DG_OK;
-}
-
-}  // namespace
-}  // namespace dg
-
-namespace dg {
-namespace {
-
-// The two launches of a k-grouped call: the descriptor prologue (skipped when `prologue` is
-// false, i.e. the workspace already holds this call's descriptors) and the GEMM.
-int kgrouped_launch(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, const float* sfb,
-                    const float* c, float* d, const int32_t* ks, int G, int64_t K_cap, int64_t N, int64_t H,
-                    void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t s, bool prologue) {
-    if (int rc = check_kgrouped(a_packed, sfa, b_packed, sfb, d, ks, G, K_cap, N, H, workspace, workspace_bytes))
-        return rc;
-    DG_CHECK_ARG(c == nullptr || aligned16(c), "c must be 16-byte aligned");
-    auto* ws = static_cast<CUtensorMap*>(workspace);
-    KgTemplates tmpl;
-    if (int rc = kgrouped_templates(a_packed, b_packed, N, H, &tmpl)) return rc;
-    CUtensorMap tD, tC;
-    {
-        uint64_t dims[3] = {static_cast<uint64_t>(H), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
-        uint64_t str[2] = {static_cast<uint64_t>(H * 4), static_cast<uint64_t>(N * H * 4)};
-        uint32_t box[3] = {32, BM, 1};
-        if (int rc = encode_tmap(&tD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, d, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return rc;
-        if (int rc = encode_tmap(&tC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, c ? c : d, dims, str, box,
-                                 CU_TENSOR_MAP_SWIZZLE_128B))
-            return rc;
-    }
-    if (prologue) {
-        k_kgrouped_prologue<<<1, 256, 0, s>>>(tmpl, a_packed, b_packed, ks, G, K_cap, N, H, ws);
-        DG_CHECK_CUDA(cudaGetLastError());
-    }
-    GemmArgs args{};
-    args.routing = ks;
-    args.sfa = sfa;
-    args.sfb = sfb;
-    args.d = d;
-    args.ws_maps = ws;
-    args.status = status;
-    args.wait_limit_ns = wait_limit_ns();
-    args.M = K_cap;
-    args.sfa_ld = N;
-    args.ldd = H;
-    args.G = G;
-    args.num_nb = static_cast<int>(H / KG_BN);
-    args.num_mb_k = static_cast<int>(N / BM);
-    args.sfb_ld = static_cast<int>(H);
-    args.c_mode = c == nullptr ? 0 : (c == d ? 2 : 1);
-    return launch_gemm<Layout::KGrouped, KG_BN, KG_STAGES, true, false>(tD, tD, tD, tD, tC, args, s);
-}
-
-}  // namespace
-}  // namespace dg
-
-extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
-                                      const float* sfb, const float* c, float* d, const int32_t* ks, int G,
-                                      int64_t K_cap, int64_t N, int64_t H, void* workspace, size_t workspace_bytes,
-                                      int32_t* status, void* stream) {
-    return kgrouped_launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes,
-                           status, static_cast<cudaStream_t>(stream), true);
-}
-
-// ------------------------------------------------------------------------- allocation-free variant
-// dg_k_grouped_fp8_wgrad_noalloc: the same k-grouped call, with its descriptor scratch in a
-// fixed array compiled into the library instead of a caller-provided workspace.  Every device
-// that loads the library holds the array (DG_NOALLOC_MAX_GROUPS experts x two 128-byte
-// descriptors = 64 KiB) until the process exits.
-namespace dg {
-namespace {
-
-static __device__ __align__(256) CUtensorMap g_noalloc_maps[2 * DG_NOALLOC_MAX_GROUPS];
-
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
-
-// Device address of g_noalloc_maps on the current device.  In host code the array's name only
-// stands in for the symbol, so the address is looked up once per device (with that device
-// current) and cached; the first call on each device does this set-up.
-int noalloc_scratch(void** out) {
-    int dev = 0;
-    DG_CHECK_CUDA(cudaGetDevice(&dev));
-    DG_CHECK_SUPPORTED(dev >= 0 && dev < 64, "device index %d", dev);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_maps);
-        if (e != cudaSuccess || p == nullptr)
-            return set_error(DG_ERR_CUDA, "cudaGetSymbolAddress of the built-in descriptor scratch failed: %s",
-                             cudaGetErrorString(e));
-        g_noalloc_addr[dev] = p;
-    }
-    *out = g_noalloc_addr[dev];
-    return DG_OK;
-}
-
-}  // namespace
-}  // namespace dg
-
-extern "C" int dg_k_grouped_fp8_wgrad_noalloc(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
-                                              const float* sfb, const float* c, float* d, const int32_t* ks, int G,
-                                              int64_t K_cap, int64_t N, int64_t H, int32_t* status, void* stream) {
-    DG_CHECK_SUPPORTED(G <= DG_NOALLOC_MAX_GROUPS,
-                       "dg_k_grouped_fp8_wgrad_noalloc handles at most %d experts (its built-in scratch holds %d "
-                       "descriptors); G=%d needs dg_k_grouped_fp8_wgrad with a workspace",
-                       DG_NOALLOC_MAX_GROUPS, 2 * DG_NOALLOC_MAX_GROUPS, G);
-    DG_CHECK_ARG(G >= 1, "G must be >= 1 (%d)", G);
-    void* scratch = nullptr;
-    if (int rc = noalloc_scratch(&scratch)) return rc;
-    // Every expert the GEMM reads gets its descriptors rewritten by this call's prologue, so the
-    // array's contents from an earlier call never need clearing.
-    return kgrouped_launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, scratch, sizeof(g_noalloc_maps),
-                           status, static_cast<cudaStream_t>(stream), true);
-}
-
-// ------------------------------------------------------------------------- test hooks
-// Launch only the k-grouped descriptor prologue, and host-encode the descriptors it should
-// produce, so that a test can compare the two byte for byte before any TMA uses them.
-extern "C" int dg_testing_kgrouped_prologue(const uint8_t* a_packed, const uint8_t* b_packed, const int32_t* ks,
-                                            int G, int64_t K_cap, int64_t N, int64_t H, void* workspace,
-                                            void* stream) {
-    DG_CHECK_ARG(G >= 1 && G <= DG_MAX_GROUPS && workspace && a_packed && b_packed && ks, "bad arguments");
-    KgTemplates tmpl;
-    if (int rc = kgrouped_templates(a_packed, b_packed, N, H, &tmpl)) return rc;
-    k_kgrouped_prologue<<<1, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        tmpl, a_packed, b_packed, ks, G, K_cap, N, H, static_cast<CUtensorMap*>(workspace));
-    DG_CHECK_CUDA(cudaGetLastError());
-    return DG_OK;
-}
-
-// The GEMM launch of dg_k_grouped_fp8_wgrad alone, reading the descriptors that an earlier
-// call with the same operands left in the workspace (used to time the kernel by itself).
-extern "C" int dg_testing_kgrouped_gemm_only(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
-                                             const float* sfb, const float* c, float* d, const int32_t* ks, int G,
-                                             int64_t K_cap, int64_t N, int64_t H, void* workspace,
-                                             size_t workspace_bytes, int32_t* status, void* stream) {
-    return kgrouped_launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes,
-                           status, static_cast<cudaStream_t>(stream), false);
-}
-
-extern "C" int dg_testing_kgrouped_host_maps(const uint8_t* a_packed, const uint8_t* b_packed,
-                                             const int32_t* ks_host, int G, int64_t N, int64_t H, void* out_host) {
-    auto* out = static_cast<CUtensorMap*>(out_host);
-    int64_t o = 0;
-    for (int e = 0; e < G; ++e) {
-        const int64_t k = ks_host[e];
-        if (k > 0) {
-            uint64_t dA[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(N)};
-            uint64_t sA[1] = {static_cast<uint64_t>(k)};
-            uint32_t bA[2] = {BK, BM};
-            if (int rc = encode_tmap(&out[2 * e], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a_packed + o * N, dA, sA, bA,
-                                     CU_TENSOR_MAP_SWIZZLE_128B))
-                return rc;
-            uint64_t dB[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(H)};
-            uint32_t bB[2] = {BK, static_cast<uint32_t>(KG_BN)};
-            if (int rc = encode_tmap(&out[2 * e + 1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b_packed + o * H, dB, sA, bB,
-                                     CU_TENSOR_MAP_SWIZZLE_128B))
-                return rc;
-        }
-        o += k;
-    }
-    return DG_OK;
 }

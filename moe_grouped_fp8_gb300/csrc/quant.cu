@@ -46,40 +46,46 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
 
 // ---------------------------------------------------------------------------------------
 // 1x128 per-token cast.  An item is one (row, 128-column block); a half-warp handles one item
-// (16 lanes x 8 bf16).  Each half-warp takes TOKEN_ITEMS_PER_HW items per pass so that several
-// 16-byte loads are in flight per thread.
+// (16 lanes x 8 bf16) and takes TOKEN_ITEMS_PER_HW items per pass so that several 16-byte loads
+// are in flight per thread.  CTA (x, y) owns rows [x*rows_per_cta, (x+1)*rows_per_cta) of row
+// group y and returns at once when they lie past the group's count, so padding rows of the
+// masked layout cost neither traffic nor work.
 // ---------------------------------------------------------------------------------------
 constexpr int TOKEN_ITEMS_PER_HW = 4;
+constexpr int TOKEN_ITEMS_PER_CTA = 512;
 
 template <bool UE8M0>
-__global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t K,
-                                                           int64_t ldx, uint8_t* __restrict__ q, void* sfa,
-                                                           int64_t Mp, float sf_zero,
-                                                           const int32_t* __restrict__ row_counts, int64_t rpg) {
+__global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __restrict__ x, int64_t K, int64_t ldx,
+                                                           uint8_t* __restrict__ q, void* sfa, int64_t Mp,
+                                                           float sf_zero, const int32_t* __restrict__ row_counts,
+                                                           int64_t rpg, int64_t rows_per_cta) {
     const int64_t KB = K / 128;
-    const int64_t items = M * KB;
-    const int lane = threadIdx.x & 31;
+    const int64_t g = blockIdx.y;
+    int64_t lim = rpg;
+    if (row_counts != nullptr) {
+        lim = row_counts[g];
+        lim = lim < 0 ? 0 : (lim > rpg ? rpg : lim);
+    }
+    const int64_t r_begin = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
+    if (r_begin >= lim) return;
+    const int64_t r_end = min(lim, r_begin + rows_per_cta);
+    const int64_t m_base = g * rpg + r_begin;
+    const int64_t items = (r_end - r_begin) * KB;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hw = lane >> 4;   // half-warp
     const int sub = lane & 15;  // 16-byte chunk within the 256-byte block
-    const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     constexpr int PER_WARP = 2 * TOKEN_ITEMS_PER_HW;
+    const int nwarps = blockDim.x >> 5;
 
-    for (int64_t base = warp_global * PER_WARP; base < items; base += nwarps * PER_WARP) {
+    for (int64_t base = static_cast<int64_t>(warp) * PER_WARP; base < items; base += nwarps * PER_WARP) {
         uint4 raw[TOKEN_ITEMS_PER_HW];
         bool live[TOKEN_ITEMS_PER_HW];
         int64_t m_of[TOKEN_ITEMS_PER_HW], kb_of[TOKEN_ITEMS_PER_HW];
 #pragma unroll
         for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
             const int64_t it = base + 2 * j + hw;
-            bool ok = it < items;
-            int64_t m = ok ? it / KB : 0, kb = ok ? it % KB : 0;
-            if (ok && row_counts != nullptr) {
-                const int64_t g = m / rpg, r = m % rpg;
-                int64_t lim = row_counts[g];
-                lim = lim < 0 ? 0 : (lim > rpg ? rpg : lim);
-                ok = r < lim;
-            }
+            const bool ok = it < items;
+            const int64_t m = m_base + (ok ? it / KB : 0), kb = ok ? it % KB : 0;
             live[j] = ok;
             m_of[j] = m;
             kb_of[j] = kb;
@@ -343,20 +349,19 @@ extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int
         rpg = M / G;
     }
     const int64_t Mp = (sf_format == DG_SF_FP32) ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
-    int sms = 0;
-    if (int rc = device_sm_count(&sms)) return rc;
-    const int64_t items = M * (K / 128);
-    const int64_t per_block = 8 * 2 * TOKEN_ITEMS_PER_HW;  // 8 warps
-    int64_t blocks = (items + per_block - 1) / per_block;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (blocks > cap) blocks = cap;
+    const int64_t groups = row_counts != nullptr ? G : 1;
+    const int64_t KB = K / 128;
+    const int64_t rows_per_cta = KB >= TOKEN_ITEMS_PER_CTA ? 1 : TOKEN_ITEMS_PER_CTA / KB;
+    const int64_t gx = (rpg + rows_per_cta - 1) / rows_per_cta;
+    DG_CHECK_SUPPORTED(gx < (1ll << 31) && groups < 65536, "too many rows or groups");
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(groups));
     auto s = static_cast<cudaStream_t>(stream);
     if (sf_format == DG_SF_UE8M0)
-        k_quant_token_1x128<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-            static_cast<const uint16_t*>(x), M, K, ldx, q, sfa, Mp, sf_zero, row_counts, rpg);
+        k_quant_token_1x128<true><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), K, ldx, q, sfa, Mp, sf_zero,
+                                                       row_counts, rpg, rows_per_cta);
     else
-        k_quant_token_1x128<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-            static_cast<const uint16_t*>(x), M, K, ldx, q, sfa, Mp, sf_zero, row_counts, rpg);
+        k_quant_token_1x128<false><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), K, ldx, q, sfa, Mp, sf_zero,
+                                                        row_counts, rpg, rows_per_cta);
     DG_CHECK_CUDA(cudaGetLastError());
     return DG_OK;
 }
