@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tmap(&tmD);
         prefetch_tmap(&tmD8);
     }
+    pdl_trigger();
+    pdl_wait();  // every earlier kernel of the stream has finished: inputs are visible
     __syncthreads();
 
     // ---------------------------------------------------------------- tile schedule
@@ -512,9 +514,7 @@ int launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap&
     DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL));
     int sms = 0;
     if (int rc = device_sm_count(&sms)) return rc;
-    kern<<<sms, NUM_THREADS, P::TOTAL, stream>>>(tA, tB, tD, tD8, args);
-    DG_CHECK_CUDA(cudaGetLastError());
-    return DG_OK;
+    return launch_pdl(kern, dim3(sms), dim3(NUM_THREADS), P::TOTAL, stream, tA, tB, tD, tD8, args);
 }
 
 constexpr int MG_BN = 128;

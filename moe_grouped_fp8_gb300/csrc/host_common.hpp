@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <string>
+#include <utility>
 
 #include "dg.h"
 
@@ -49,5 +50,25 @@ uint64_t wait_limit_ns();
 int encode_tmap(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                 const uint64_t* dims, const uint64_t* strides_bytes /* rank-1 entries */,
                 const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Launch `kernel` on `stream` with programmatic stream serialization, so that its launch and
+// set-up overlap the previous kernel in the stream; the kernel calls pdl_wait() before touching
+// global memory.  Returns DG_OK or DG_ERR_CUDA.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) return set_error(DG_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return DG_OK;
+}
 
 }  // namespace dg

@@ -23,6 +23,14 @@ __device__ __forceinline__ void status_or(int32_t* status, int bits) {
     if (status != nullptr && bits != 0) atomicOr(reinterpret_cast<int*>(status), bits);
 }
 
+// ------------------------------------------------------------------------------- dependent launch
+// Kernels launched with programmatic stream serialization: `pdl_trigger` lets the next kernel in
+// the stream be scheduled as soon as resources allow (it still waits for this one); `pdl_wait`
+// blocks until every earlier kernel of the stream has finished and its memory is visible, and is
+// called before a kernel's first global-memory access.  Both are no-ops without such a launch.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __res
                                                            uint8_t* __restrict__ q, void* sfa, int64_t Mp,
                                                            float sf_zero, const int32_t* __restrict__ row_counts,
                                                            int64_t rpg, int64_t rows_per_cta) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t KB = K / 128;
     const int64_t g = blockIdx.y;
     int64_t lim = rpg;
@@ -130,6 +132,8 @@ __global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __res
 template <bool UE8M0>
 __global__ void __launch_bounds__(256) k_quant_block_128x128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                              uint8_t* __restrict__ q, void* sfb, float sf_zero) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t NB = N / 128, KB = K / 128;
     const int64_t blk = blockIdx.x;
     const int64_t kb = blk % KB;
@@ -267,6 +271,8 @@ __global__ void __launch_bounds__(256) k_quant_channel_128(const uint16_t* __res
     __shared__ float s_r[CH_COLS];
     __shared__ __align__(16) uint8_t s_t[CH_COLS * CH_PITCH];
 
+    pdl_trigger();
+    pdl_wait();
     const int64_t tb = blockIdx.y;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * CH_COLS;
     int64_t o_e = 0, k_e = 0;
@@ -356,14 +362,12 @@ extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int
     DG_CHECK_SUPPORTED(gx < (1ll << 31) && groups < 65536, "too many rows or groups");
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(groups));
     auto s = static_cast<cudaStream_t>(stream);
+    const auto* xp = static_cast<const uint16_t*>(x);
     if (sf_format == DG_SF_UE8M0)
-        k_quant_token_1x128<true><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), K, ldx, q, sfa, Mp, sf_zero,
-                                                       row_counts, rpg, rows_per_cta);
-    else
-        k_quant_token_1x128<false><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), K, ldx, q, sfa, Mp, sf_zero,
-                                                        row_counts, rpg, rows_per_cta);
-    DG_CHECK_CUDA(cudaGetLastError());
-    return DG_OK;
+        return launch_pdl(k_quant_token_1x128<true>, grid, dim3(256), 0, s, xp, K, ldx, q, sfa, Mp, sf_zero,
+                          row_counts, rpg, rows_per_cta);
+    return launch_pdl(k_quant_token_1x128<false>, grid, dim3(256), 0, s, xp, K, ldx, q, sfa, Mp, sf_zero, row_counts,
+                      rpg, rows_per_cta);
 }
 
 extern "C" int dg_quant_block_128x128(const void* w, int G, int64_t N, int64_t K, uint8_t* q, void* sfb,
@@ -377,14 +381,11 @@ extern "C" int dg_quant_block_128x128(const void* w, int G, int64_t N, int64_t K
     DG_CHECK_ARG(aligned16(w) && ((reinterpret_cast<uintptr_t>(q) & 7u) == 0), "w must be 16-byte and q 8-byte aligned");
     DG_CHECK_SUPPORTED(blocks < (1ll << 31), "too many 128x128 blocks");
     auto s = static_cast<cudaStream_t>(stream);
+    const auto* wp = static_cast<const uint16_t*>(w);
+    const dim3 grid(static_cast<unsigned>(blocks));
     if (sf_format == DG_SF_UE8M0)
-        k_quant_block_128x128<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint16_t*>(w), N,
-                                                                                   K, q, sfb, sf_zero);
-    else
-        k_quant_block_128x128<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint16_t*>(w),
-                                                                                    N, K, q, sfb, sf_zero);
-    DG_CHECK_CUDA(cudaGetLastError());
-    return DG_OK;
+        return launch_pdl(k_quant_block_128x128<true>, grid, dim3(256), 0, s, wp, N, K, q, sfb, sf_zero);
+    return launch_pdl(k_quant_block_128x128<false>, grid, dim3(256), 0, s, wp, N, K, q, sfb, sf_zero);
 }
 
 extern "C" int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C, const int32_t* ks, int G,
@@ -398,8 +399,6 @@ extern "C" int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C,
     DG_CHECK_ARG(aligned16(x) && aligned16(q_packed), "x and q_packed must be 16-byte aligned");
     DG_CHECK_SUPPORTED(K_cap / 128 < 65536, "K_cap too large");
     dim3 grid(static_cast<unsigned>(C / CH_COLS), static_cast<unsigned>(K_cap / 128));
-    k_quant_channel_128<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), K_cap, C, ks, G, q_packed, sf, sf_zero, status);
-    DG_CHECK_CUDA(cudaGetLastError());
-    return DG_OK;
+    return launch_pdl(k_quant_channel_128, grid, dim3(256), 0, static_cast<cudaStream_t>(stream),
+                      static_cast<const uint16_t*>(x), K_cap, C, ks, G, q_packed, sf, sf_zero, status);
 }
