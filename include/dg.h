@@ -105,6 +105,20 @@ int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C, const int3
                              void* stream);
 
 /*
+ * Both operands of a k-grouped wgrad cast in one launch: the same results as
+ * dg_quant_per_channel_128(x_a, K_cap, C_a, ks, ...) followed by
+ * dg_quant_per_channel_128(x_b, K_cap, C_b, ks, ...) with the same ks, sf_zero and status
+ * ([P1] repro: `_make_operand` applied to grad_y and to the activation).  The two calls are
+ * independent, so one launch covers both and saves a kernel boundary on the wgrad path.
+ *   x_a / x_b: bf16 [K_cap, C_a] / [K_cap, C_b].  q_a / q_b, sf_a / sf_b: as in
+ *   dg_quant_per_channel_128.
+ */
+int dg_quant_per_channel_128_pair(const void* x_a, int64_t C_a, uint8_t* q_a, float* sf_a,
+                                  const void* x_b, int64_t C_b, uint8_t* q_b, float* sf_b,
+                                  int64_t K_cap, const int32_t* ks, int G, float sf_zero,
+                                  int32_t* status, void* stream);
+
+/*
  * 128x128 per-block cast of expert weights ([P2] "2d" weight scales of sm90_fp8_gemm_1d2d;
  * [P3] "weights requantized to 2^k scales" for UE8M0).  amax over each 128x128 block, then
  * the rules of dg_quant_per_token_1x128.

@@ -14,7 +14,8 @@ import torch
 from ._lib import DG_OP_K_GROUPED_WGRAD, DG_OUT_BF16, DG_OUT_FP32, DG_SF_FP32, DGError, check, load
 
 __all__ = [
-    "dg_quant_per_token_1x128", "dg_quant_per_channel_128", "dg_quant_block_128x128",
+    "dg_quant_per_token_1x128", "dg_quant_per_channel_128", "dg_quant_per_channel_128_pair",
+    "dg_quant_block_128x128",
     "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad",
     "dg_k_grouped_fp8_wgrad_noalloc",
     "dg_workspace_size", "dg_last_error", "sfa_padded_rows", "empty_sfa", "kgrouped_workspace", "DGError",
@@ -92,6 +93,20 @@ def dg_quant_per_channel_128(x, ks, q_packed, sf, sf_zero=1e-30, status=None, st
     _need(sf.is_contiguous() and sf.dtype == torch.float32 and sf.numel() >= (K_cap // 128) * C, "sf size")
     check(load().dg_quant_per_channel_128(_p(x), K_cap, C, _p(ks), ks.numel(), _p(q_packed), _p(sf), sf_zero,
                                           _p(status), _s(stream)))
+
+
+def dg_quant_per_channel_128_pair(x_a, x_b, ks, q_a, sf_a, q_b, sf_b, sf_zero=1e-30, status=None, stream=None):
+    """Both wgrad operands in one launch: same results as two dg_quant_per_channel_128 calls."""
+    _dev(x_a, x_b, ks, q_a, sf_a, q_b, sf_b, status)
+    for x, q, sf in ((x_a, q_a, sf_a), (x_b, q_b, sf_b)):
+        _need(x.dim() == 2 and x.dtype == torch.bfloat16 and x.is_contiguous(), "x must be contiguous bf16 [K_cap, C]")
+        _need(q.is_contiguous() and q.numel() >= x.numel() and q.element_size() == 1, "q size")
+        _need(sf.is_contiguous() and sf.dtype == torch.float32 and sf.numel() >= x.numel() // 128, "sf size")
+    _need(x_a.shape[0] == x_b.shape[0], "both operands need the same K_cap")
+    _need(ks.dtype == torch.int32 and ks.is_contiguous(), "ks must be int32")
+    check(load().dg_quant_per_channel_128_pair(_p(x_a), x_a.shape[1], _p(q_a), _p(sf_a), _p(x_b), x_b.shape[1], _p(q_b),
+                                               _p(sf_b), x_a.shape[0], _p(ks), ks.numel(), sf_zero, _p(status),
+                                               _s(stream)))
 
 
 def dg_quant_block_128x128(w, q, sfb, sf_format=DG_SF_FP32, sf_zero=1e-30, stream=None):

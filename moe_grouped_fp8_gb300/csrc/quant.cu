@@ -263,31 +263,46 @@ __device__ int find_expert(const int32_t* __restrict__ ks, int G, int64_t K_cap,
     return f;
 }
 
-__global__ void __launch_bounds__(256) k_quant_channel_128(const uint16_t* __restrict__ x, int64_t K_cap, int64_t C,
-                                                           const int32_t* __restrict__ ks, int G,
-                                                           uint8_t* __restrict__ qp, float* __restrict__ sf_out,
-                                                           float sf_zero, int32_t* status) {
+// One or two operands cast in the same launch (the two operands of a k-grouped wgrad share ks):
+// column blocks [0, nblk0) belong to op0, the rest to op1.
+struct ChannelOperand {
+    const uint16_t* x;  // bf16 [K_cap, C]
+    int64_t C;
+    uint8_t* q;         // packed codes
+    float* sf;          // [K_cap/128][C]
+};
+
+__global__ void __launch_bounds__(256) k_quant_channel_128(const ChannelOperand op0, const ChannelOperand op1,
+                                                           int nblk0, int64_t K_cap, const int32_t* __restrict__ ks,
+                                                           int G, float sf_zero, int32_t* status) {
     __shared__ float s_part[8][CH_COLS];
     __shared__ float s_r[CH_COLS];
     __shared__ __align__(16) uint8_t s_t[CH_COLS * CH_PITCH];
 
+    const bool second = static_cast<int>(blockIdx.x) >= nblk0;
+    const ChannelOperand& op = second ? op1 : op0;
+    const uint16_t* __restrict__ x = op.x;
+    const int64_t C = op.C;
+    const int64_t tb = blockIdx.y;
+    const int64_t c0 = static_cast<int64_t>(second ? blockIdx.x - nblk0 : blockIdx.x) * CH_COLS;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int c = t & 7;          // 8-column chunk
+    const int rb = (t >> 3) * 4;  // first of 4 consecutive tokens
+
     pdl_trigger();
     pdl_wait();
-    const int64_t tb = blockIdx.y;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * CH_COLS;
+    // the bf16 loads do not depend on the expert lookup: issue them first (rows < K_cap exist)
+    uint4 raw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        raw[j] = __ldg(reinterpret_cast<const uint4*>(x + (tb * 128 + rb + j) * C + c0) + c);
     int64_t o_e = 0, k_e = 0;
     int bad = 0;
     const int e = find_expert(ks, G, K_cap, tb * 128, &o_e, &k_e, &bad);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) status_or(status, bad);
     if (e < 0) return;
-
-    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    const int c = t & 7;          // 8-column chunk
-    const int rb = (t >> 3) * 4;  // first of 4 consecutive tokens
-    uint4 raw[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        raw[j] = __ldg(reinterpret_cast<const uint4*>(x + (tb * 128 + rb + j) * C + c0) + c);
+    uint8_t* __restrict__ qp = op.q;
+    float* __restrict__ sf_out = op.sf;
     float f[4][8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) bf16x8_to_float(raw[j], f[j]);
@@ -399,6 +414,28 @@ extern "C" int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C,
     DG_CHECK_ARG(aligned16(x) && aligned16(q_packed), "x and q_packed must be 16-byte aligned");
     DG_CHECK_SUPPORTED(K_cap / 128 < 65536, "K_cap too large");
     dim3 grid(static_cast<unsigned>(C / CH_COLS), static_cast<unsigned>(K_cap / 128));
-    return launch_pdl(k_quant_channel_128, grid, dim3(256), 0, static_cast<cudaStream_t>(stream),
-                      static_cast<const uint16_t*>(x), K_cap, C, ks, G, q_packed, sf, sf_zero, status);
+    const ChannelOperand op{static_cast<const uint16_t*>(x), C, q_packed, sf};
+    return launch_pdl(k_quant_channel_128, grid, dim3(256), 0, static_cast<cudaStream_t>(stream), op, op,
+                      static_cast<int>(C / CH_COLS), K_cap, ks, G, sf_zero, status);
+}
+
+extern "C" int dg_quant_per_channel_128_pair(const void* x_a, int64_t C_a, uint8_t* q_a, float* sf_a, const void* x_b,
+                                             int64_t C_b, uint8_t* q_b, float* sf_b, int64_t K_cap,
+                                             const int32_t* ks, int G, float sf_zero, int32_t* status,
+                                             void* stream) {
+    DG_CHECK_ARG(K_cap >= 0 && K_cap % 128 == 0, "K_cap must be a multiple of 128 (%lld)", (long long)K_cap);
+    DG_CHECK_ARG(C_a > 0 && C_a % CH_COLS == 0 && C_b > 0 && C_b % CH_COLS == 0,
+                 "C_a and C_b must be positive multiples of %d", CH_COLS);
+    DG_CHECK_ARG(G >= 1 && G <= DG_MAX_GROUPS, "G must be in [1, %d] (%d)", DG_MAX_GROUPS, G);
+    if (K_cap == 0) return DG_OK;
+    DG_CHECK_ARG(x_a && q_a && sf_a && x_b && q_b && sf_b && ks, "null pointer argument");
+    DG_CHECK_ARG(aligned16(x_a) && aligned16(q_a) && aligned16(x_b) && aligned16(q_b),
+                 "x and q buffers must be 16-byte aligned");
+    DG_CHECK_SUPPORTED(K_cap / 128 < 65536 && (C_a + C_b) / CH_COLS < (1ll << 31), "sizes too large");
+    const ChannelOperand op0{static_cast<const uint16_t*>(x_a), C_a, q_a, sf_a};
+    const ChannelOperand op1{static_cast<const uint16_t*>(x_b), C_b, q_b, sf_b};
+    const int nblk0 = static_cast<int>(C_a / CH_COLS);
+    dim3 grid(static_cast<unsigned>(nblk0 + C_b / CH_COLS), static_cast<unsigned>(K_cap / 128));
+    return launch_pdl(k_quant_channel_128, grid, dim3(256), 0, static_cast<cudaStream_t>(stream), op0, op1, nblk0,
+                      K_cap, ks, G, sf_zero, status);
 }

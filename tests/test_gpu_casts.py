@@ -116,3 +116,27 @@ def test_cast_matches_oracle_on_every_code_midpoint():
     oq, osf, _ = oracle.quant_per_token_1x128(x)
     assert np.all(osf == 1.0)
     np.testing.assert_array_equal(q.cpu().numpy(), oq)
+
+
+@pytest.mark.parametrize("ks,Ca,Cb", [([256, 128, 128, 256], 2048, 2048), ([128, 0, 384], 192, 64)])
+def test_per_channel_pair_equals_two_single_calls(ks, Ca, Cb):
+    from moe_grouped_fp8_gb300 import api
+    T = sum(ks)
+    K_cap = T + 128
+    xa = wl.randn_bf16((K_cap, Ca), 7, 1e-7)
+    xb = wl.randn_bf16((K_cap, Cb), 8, 0.4)
+    xa[128:256, 0] = 0
+    ks_dev = torch.tensor(ks, dtype=torch.int32, device="cuda")
+    qa1, sa1 = gpu_quant_channels(xa.cuda(), ks_dev, 1e-4)
+    qb1, sb1 = gpu_quant_channels(xb.cuda(), ks_dev, 1e-4)
+    qa2 = torch.zeros_like(qa1)
+    qb2 = torch.zeros_like(qb1)
+    sa2 = torch.zeros_like(sa1)
+    sb2 = torch.zeros_like(sb1)
+    api.dg_quant_per_channel_128_pair(xa.cuda(), xb.cuda(), ks_dev, qa2, sa2, qb2, sb2, sf_zero=1e-4)
+    sync()
+    for one, two in ((qa1, qa2), (qb1, qb2), (sa1, sa2), (sb1, sb2)):
+        assert torch.equal(one.view(torch.uint8), two.view(torch.uint8))
+    oq, osf = oracle.quant_per_channel_128(xb[:T], 1e-4)
+    np.testing.assert_array_equal(qb2.cpu().numpy()[:T * Cb], oracle.pack_kmajor(oq, ks))
+    np.testing.assert_array_equal(sb2.cpu().numpy()[:T // 128].view(np.uint32), osf.view(np.uint32))
