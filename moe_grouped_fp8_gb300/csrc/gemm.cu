@@ -62,6 +62,9 @@ struct GemmArgs {
     int n128;        // m-grouped N / 128 (sfb row count)
 };
 
+constexpr int TBUFS = 4;          // TMEM partial buffers: the tensor core runs up to 3 blocks ahead
+constexpr int SF_PREFETCH = 8;    // 128-K blocks of activation scales each promotion thread keeps in flight
+
 template <Layout L, int BN, int STAGES, bool OUT_FP32>
 struct Plan {
     static constexpr int A_BYTES = BM * BK;
@@ -76,18 +79,21 @@ struct Plan {
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
     static constexpr int SCHED_BYTES = (MAX_RUNS + 1) * 4 + 4 * MAX_RUNS * 4;
-    static constexpr int BAR_OFF = (SCHED_OFF + SCHED_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
-    static constexpr int NUM_BARS = 2 * STAGES + 4;
+    static constexpr int PREF_OFF = SCHED_OFF + SCHED_BYTES;  // [SF_PREFETCH][256 threads] 4-byte slots
+    static constexpr int PREF_BYTES = SF_PREFETCH * NUM_EPI_WARPS * 32 * 4;
+    static constexpr int BAR_OFF = (PREF_OFF + PREF_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int MISC_BYTES = 256;
     static constexpr int TOTAL = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
-    static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                          : (2 * BN <= 256) ? 256 : 512;
+    static constexpr uint32_t TMEM_COLS = TBUFS * BN;
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
     static_assert(CPT % 32 == 0, "promotion threads read 32-column groups");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
     static_assert(STG_OFF % 1024 == 0 && SCHED_OFF % 1024 == 0, "TMA / swizzle buffers are 1024-byte aligned");
     static_assert(BAR_OFF % 8 == 0 && MISC_OFF % 8 == 0, "mbarrier objects are 8-byte aligned");
+    static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two <= 512");
+    static_assert(TOTAL <= 232448, "shared memory");
 };
 
 // ------------------------------------------------------------------------- small helpers
@@ -145,7 +151,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* tempty = tfull + 2;
+    uint64_t* tempty = tfull + TBUFS;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + P::MISC_OFF + 4);
     int* s_nruns = reinterpret_cast<int*>(smem + P::MISC_OFF + 8);
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < TBUFS; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], NUM_EPI_WARPS);
         }
@@ -332,14 +338,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     umma_commit(&tfull[tb]);
                     any = true;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    if (++tb == 2) { tb = 0; tphase ^= 1u; }
+                    if (++tb == TBUFS) { tb = 0; tphase ^= 1u; }
                 }
             }
             if (any) {
                 // the last commit: wait until the tensor core is done with every MMA issued
                 int lt = tb - 1;
                 uint32_t lp = tphase;
-                if (lt < 0) { lt = 1; lp ^= 1u; }
+                if (lt < 0) { lt = TBUFS - 1; lp ^= 1u; }
                 drain_wait(&tfull[lt], lp, a.wait_limit_ns);
             }
         }
@@ -375,35 +381,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < P::CPT; ++i) acc[i] = 0.0f;
 
+            // activation scales: an SF_PREFETCH-deep ring of per-thread cp.async copies (the row's
+            // scale of block kb lands in slot kb % SF_PREFETCH); one commit group per block
+            uint32_t* pref = reinterpret_cast<uint32_t*>(smem + P::PREF_OFF) + tid;
+            auto prefetch = [&](int kbi) {
+                if (row_ok && kbi < ti.kbt) {
+                    const int64_t idx = static_cast<int64_t>(kbi) * a.sfa_ld + grow;
+                    const void* src;
+                    if constexpr (SF_UE8M0)  // the aligned word holding the byte (inside the Mp padding)
+                        src = static_cast<const uint8_t*>(a.sfa) + (idx & ~int64_t(3));
+                    else
+                        src = static_cast<const float*>(a.sfa) + idx;
+                    cp_async4(pref + (kbi % SF_PREFETCH) * (NUM_EPI_WARPS * 32), src);
+                }
+                cp_async_commit();
+            };
+            const int sbi0 = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB;
+            for (int i = 0; i < SF_PREFETCH - 1; ++i) prefetch(i);
             for (int kb = 0; kb < ti.kbt; ++kb) {
+                prefetch(kb + SF_PREFETCH - 1);
+                cp_async_wait<SF_PREFETCH - 1>();  // the group of block kb has landed
                 float s = 0.0f;
                 if (row_ok) {
+                    const uint32_t w = pref[(kb % SF_PREFETCH) * (NUM_EPI_WARPS * 32)];
                     float sa, sb;
-                    const int sbi = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB + kb;
                     if constexpr (SF_UE8M0) {
-                        sa = ue8m0_to_float(static_cast<const uint8_t*>(a.sfa)[kb * a.sfa_ld + grow]);
-                        sb = ue8m0_to_float(static_cast<const uint8_t*>(a.sfb)[sbi]);
+                        const int64_t idx = static_cast<int64_t>(kb) * a.sfa_ld + grow;
+                        sa = ue8m0_to_float(static_cast<uint8_t>(w >> (8 * (idx & 3))));
+                        sb = ue8m0_to_float(__ldg(static_cast<const uint8_t*>(a.sfb) + sbi0 + kb));
                     } else {
-                        sa = static_cast<const float*>(a.sfa)[kb * a.sfa_ld + grow];
-                        sb = static_cast<const float*>(a.sfb)[sbi];
+                        sa = __uint_as_float(w);
+                        sb = __ldg(static_cast<const float*>(a.sfb) + sbi0 + kb);
                     }
                     s = sa * sb;
                 }
                 if (!mbar_wait(&tfull[tb], tphase, wc)) { failed = true; break; }
                 tc_fence_after();
+                uint32_t v[P::CPT / 32][32];
 #pragma unroll
-                for (int c2 = 0; c2 < P::CPT / 32; ++c2) {
-                    uint32_t v[32];
-                    tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32), v);
-                    tmem_wait_ld();
+                for (int c2 = 0; c2 < P::CPT / 32; ++c2)
+                    tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32), v[c2]);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c2 * 32 + i] = fmaf(s, __uint_as_float(v[i]), acc[c2 * 32 + i]);
-                }
+                for (int c2 = 0; c2 < P::CPT / 32; ++c2) tmem_wait_ld(v[c2]);
+                // the partial is in registers: hand the TMEM buffer back before the FMAs
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[tb]);
-                if (++tb == 2) { tb = 0; tphase ^= 1u; }
+                if (++tb == TBUFS) { tb = 0; tphase ^= 1u; }
+#pragma unroll
+                for (int c2 = 0; c2 < P::CPT / 32; ++c2)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[c2 * 32 + i] = fmaf(s, __uint_as_float(v[c2][i]), acc[c2 * 32 + i]);
             }
+            cp_async_wait<0>();
 
             // ---- stage the tile in shared memory
             if (tid == 0 && have_store) bulk_wait_read_all();  // the previous store has read the staging
@@ -519,6 +549,7 @@ int launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap&
 
 constexpr int MG_BN = 128;
 constexpr int MG_STAGES = 4;
+constexpr int MG_STAGES_BF16 = 5;
 
 CUtensorMapDataType out_tmap_type(int out) {
     return out == DG_OUT_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -527,12 +558,13 @@ CUtensorMapDataType out_tmap_type(int out) {
 template <Layout L>
 int dispatch_mgrouped(int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD,
                       const CUtensorMap& tD8, const GemmArgs& args, cudaStream_t s) {
+    // bf16 output stages half as much as fp32, which leaves room for a fifth ring stage
     if (out == DG_OUT_FP32) {
         if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, true, true>(tA, tB, tD, tD8, args, s);
         return launch_gemm<L, MG_BN, MG_STAGES, true, false>(tA, tB, tD, tD8, args, s);
     }
-    if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, false, true>(tA, tB, tD, tD8, args, s);
-    return launch_gemm<L, MG_BN, MG_STAGES, false, false>(tA, tB, tD, tD8, args, s);
+    if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES_BF16, false, true>(tA, tB, tD, tD8, args, s);
+    return launch_gemm<L, MG_BN, MG_STAGES_BF16, false, false>(tA, tB, tD, tD8, args, s);
 }
 
 int check_common_mg(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d, int out,

@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(NT, 1) k_kgrouped_gemm(const __grid_constant__
                 for (int c2 = 0; c2 < CPT / 32; ++c2) {
                     uint32_t v[32];
                     tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + c0 + c2 * 32), v);
-                    tmem_wait_ld();
+                    tmem_wait_ld(v);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float4 sb = sbp[(c0 + c2 * 32) / 4 + i];
