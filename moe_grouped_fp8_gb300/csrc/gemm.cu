@@ -63,7 +63,7 @@ struct GemmArgs {
 };
 
 constexpr int TBUFS = 4;          // TMEM partial buffers: the tensor core runs up to 3 blocks ahead
-constexpr int SF_PREFETCH = 8;    // 128-K blocks of activation scales each promotion thread keeps in flight
+constexpr int SF_GROUP = 4;       // 128-K blocks whose scales a promotion thread loads together
 
 template <Layout L, int BN, int STAGES, bool OUT_FP32>
 struct Plan {
@@ -79,9 +79,7 @@ struct Plan {
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
     static constexpr int SCHED_BYTES = (MAX_RUNS + 1) * 4 + 4 * MAX_RUNS * 4;
-    static constexpr int PREF_OFF = SCHED_OFF + SCHED_BYTES;  // [SF_PREFETCH][256 threads] 4-byte slots
-    static constexpr int PREF_BYTES = SF_PREFETCH * NUM_EPI_WARPS * 32 * 4;
-    static constexpr int BAR_OFF = (PREF_OFF + PREF_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
+    static constexpr int BAR_OFF = (SCHED_OFF + SCHED_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
     static constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int MISC_BYTES = 256;
@@ -381,59 +379,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < P::CPT; ++i) acc[i] = 0.0f;
 
-            // activation scales: an SF_PREFETCH-deep ring of per-thread cp.async copies (the row's
-            // scale of block kb lands in slot kb % SF_PREFETCH); one commit group per block
-            uint32_t* pref = reinterpret_cast<uint32_t*>(smem + P::PREF_OFF) + tid;
-            auto prefetch = [&](int kbi) {
-                if (row_ok && kbi < ti.kbt) {
-                    const int64_t idx = static_cast<int64_t>(kbi) * a.sfa_ld + grow;
-                    const void* src;
-                    if constexpr (SF_UE8M0)  // the aligned word holding the byte (inside the Mp padding)
-                        src = static_cast<const uint8_t*>(a.sfa) + (idx & ~int64_t(3));
-                    else
-                        src = static_cast<const float*>(a.sfa) + idx;
-                    cp_async4(pref + (kbi % SF_PREFETCH) * (NUM_EPI_WARPS * 32), src);
-                }
-                cp_async_commit();
-            };
+            // Scales travel in registers, four 128-K blocks at a time: while the blocks of group g
+            // are promoted, the loads of group g + 1 are in flight (issued one group earlier).
             const int sbi0 = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB;
-            for (int i = 0; i < SF_PREFETCH - 1; ++i) prefetch(i);
-            for (int kb = 0; kb < ti.kbt; ++kb) {
-                prefetch(kb + SF_PREFETCH - 1);
-                cp_async_wait<SF_PREFETCH - 1>();  // the group of block kb has landed
-                float s = 0.0f;
-                if (row_ok) {
-                    const uint32_t w = pref[(kb % SF_PREFETCH) * (NUM_EPI_WARPS * 32)];
-                    float sa, sb;
-                    if constexpr (SF_UE8M0) {
-                        const int64_t idx = static_cast<int64_t>(kb) * a.sfa_ld + grow;
-                        sa = ue8m0_to_float(static_cast<uint8_t>(w >> (8 * (idx & 3))));
-                        sb = ue8m0_to_float(__ldg(static_cast<const uint8_t*>(a.sfb) + sbi0 + kb));
-                    } else {
-                        sa = __uint_as_float(w);
-                        sb = __ldg(static_cast<const float*>(a.sfb) + sbi0 + kb);
+            auto load_group = [&](int g, float (&sa)[SF_GROUP], float (&sb)[SF_GROUP]) {
+#pragma unroll
+                for (int u = 0; u < SF_GROUP; ++u) {
+                    const int kbi = g * SF_GROUP + u;
+                    sa[u] = 0.0f;
+                    sb[u] = 0.0f;
+                    if (row_ok && kbi < ti.kbt) {
+                        const int64_t idx = static_cast<int64_t>(kbi) * a.sfa_ld + grow;
+                        if constexpr (SF_UE8M0) {
+                            sa[u] = ue8m0_to_float(__ldg(static_cast<const uint8_t*>(a.sfa) + idx));
+                            sb[u] = ue8m0_to_float(__ldg(static_cast<const uint8_t*>(a.sfb) + sbi0 + kbi));
+                        } else {
+                            sa[u] = __ldg(static_cast<const float*>(a.sfa) + idx);
+                            sb[u] = __ldg(static_cast<const float*>(a.sfb) + sbi0 + kbi);
+                        }
                     }
-                    s = sa * sb;
                 }
-                if (!mbar_wait(&tfull[tb], tphase, wc)) { failed = true; break; }
-                tc_fence_after();
-                uint32_t v[P::CPT / 32][32];
+            };
+            float sa_c[SF_GROUP], sb_c[SF_GROUP], sa_n[SF_GROUP], sb_n[SF_GROUP];
+            load_group(0, sa_c, sb_c);
+            load_group(1, sa_n, sb_n);
+            for (int kb0 = 0; kb0 < ti.kbt && !failed; kb0 += SF_GROUP) {
 #pragma unroll
-                for (int c2 = 0; c2 < P::CPT / 32; ++c2)
-                    tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32), v[c2]);
+                for (int u = 0; u < SF_GROUP; ++u) {
+                    if (kb0 + u >= ti.kbt) break;
+                    const float s = sa_c[u] * sb_c[u];
+                    if (!mbar_wait(&tfull[tb], tphase, wc)) { failed = true; break; }
+                    tc_fence_after();
+                    uint32_t v[P::CPT / 32][32];
 #pragma unroll
-                for (int c2 = 0; c2 < P::CPT / 32; ++c2) tmem_wait_ld(v[c2]);
-                // the partial is in registers: hand the TMEM buffer back before the FMAs
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[tb]);
-                if (++tb == TBUFS) { tb = 0; tphase ^= 1u; }
+                    for (int c2 = 0; c2 < P::CPT / 32; ++c2)
+                        tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32), v[c2]);
 #pragma unroll
-                for (int c2 = 0; c2 < P::CPT / 32; ++c2)
+                    for (int c2 = 0; c2 < P::CPT / 32; ++c2) tmem_wait_ld(v[c2]);
+                    // the partial is in registers: hand the TMEM buffer back before the FMAs
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[tb]);
+                    if (++tb == TBUFS) { tb = 0; tphase ^= 1u; }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c2 * 32 + i] = fmaf(s, __uint_as_float(v[c2][i]), acc[c2 * 32 + i]);
+                    for (int c2 = 0; c2 < P::CPT / 32; ++c2)
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            ffma2(acc[c2 * 32 + i], acc[c2 * 32 + i + 1], s, __uint_as_float(v[c2][i]),
+                                  __uint_as_float(v[c2][i + 1]));
+                }
+#pragma unroll
+                for (int u = 0; u < SF_GROUP; ++u) {
+                    sa_c[u] = sa_n[u];
+                    sb_c[u] = sb_n[u];
+                }
+                load_group(kb0 / SF_GROUP + 2, sa_n, sb_n);
             }
-            cp_async_wait<0>();
 
             // ---- stage the tile in shared memory
             if (tid == 0 && have_store) bulk_wait_read_all();  // the previous store has read the staging

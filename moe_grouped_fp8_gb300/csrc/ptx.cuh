@@ -240,6 +240,18 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// acc0 += s * v0 and acc1 += s * v1 as one packed fp32 FMA; each lane rounds exactly like fmaf.
+__device__ __forceinline__ void ffma2(float& acc0, float& acc1, float s, float v0, float v1) {
+    asm("{\n\t.reg .b64 d, a, b;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %4};\n\t"
+        "mov.b64 d, {%0, %1};\n\t"
+        "fma.rn.f32x2 d, a, b, d;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "f"(v0), "f"(v1), "f"(s));
+}
+
 // Asynchronous 4-byte global -> shared copy (per thread), grouped with cp.async.commit_group.
 __device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
