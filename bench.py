@@ -120,7 +120,7 @@ class ClockSampler:
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ["gemm.cu", "kgrouped.cu", "kernel_common.cuh", "ptx.cuh"]:
+    for f in ["gemm.cu", "gemm_pair.cu", "mgrouped.cuh", "kgrouped.cu", "kernel_common.cuh", "ptx.cuh"]:
         h.update(open(os.path.join(ROOT, "moe_grouped_fp8_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -180,6 +180,7 @@ def capture(fn, stream):
 
 class KGroupedWorkload:
     name = "kgrouped_wgrad_repro_Ks256-128-128-256_N2048_H2048"
+    kernel_name = "k_kgrouped_gemm"
 
     def __init__(self, device, sets=None, ours=True):
         from moe_grouped_fp8_gb300 import workloads as wl
@@ -328,6 +329,10 @@ class MGroupedWorkload:
             raise SystemExit(f"unknown workload {kind}")
         self.kind = kind
         self.masked = isinstance(self.w, wl.Masked)
+        # the kernel the library picks for this call (bf16 output): CTA pairs when a masked call's
+        # expected_m hint spans more than one 128-row block
+        self.kernel_name = ("k_grouped_gemm_pair" if self.masked and self.w.expected_m > 128
+                            else "k_grouped_gemm")
         w = self.w
         self.fmt = DG_SF_UE8M0 if getattr(w, "ue8m0", False) else DG_SF_FP32
         a, b = w.draw(device=device)
@@ -378,7 +383,7 @@ class MGroupedWorkload:
         w = self.w
         if self.masked:
             self.api.dg_m_grouped_fp8_masked(self.qa.view(w.G, w.cap, w.K), self.sfa, self.qb, self.sfb, self.d,
-                                             self.counts, 0, self.fmt)
+                                             self.counts, w.expected_m, self.fmt)
         else:
             self.api.dg_m_grouped_fp8_contiguous(self.qa, self.sfa, self.qb, self.sfb, self.d, self.mi, self.fmt)
 
@@ -427,6 +432,7 @@ class MGroupedWorkload:
              else "L2-resident (launch-latency-bound shape)", "graphs": "each step replayed from a CUDA graph"}
         if self.masked:
             c["capacity"] = w.cap
+            c["expected_m"] = w.expected_m
         else:
             c["m_rows"] = self.M
         return c
@@ -499,7 +505,7 @@ def run_ours(args, ws, rank, local):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp8_peak, 4)}
     traffic = profiled_traffic(f"{args.workload}_gemm")
-    roof.update({"traffic": traffic, "kernel": "k_grouped_gemm", "algorithmic_bytes": gemm_bytes,
+    roof.update({"traffic": traffic, "kernel": wk.kernel_name, "algorithmic_bytes": gemm_bytes,
                  "kernel_ms": round(ms_gemm, 5), "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json "
                  f"hbm_gbs; fp8 peak = bf16 x 2)" if peaks["source"] == "measured" else "fallback",
                  "tensor_frac": round(wk.flops / (ms_gemm * 1e-3) / 1e12 / fp8_peak, 4),

@@ -41,6 +41,7 @@ TESTING_SIGNATURES = {
     "dg_testing_kgrouped_prologue": (I32, [P, P, P, I32, I64, I64, I64, P, P]),
     "dg_testing_kgrouped_host_maps": (I32, [P, P, P, I32, I64, I64, P]),
     "dg_testing_kgrouped_gemm_only": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
+    "dg_testing_mgrouped_kernel": (I32, [I32]),
 }
 
 _lock = threading.Lock()

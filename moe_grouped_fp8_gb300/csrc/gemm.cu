@@ -27,40 +27,20 @@
 // threads.  Rows that are not valid are never written.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "host_common.hpp"
 #include "kernel_common.cuh"
+#include "mgrouped.cuh"
 #include "ptx.cuh"
 
 namespace dg {
 
-enum class Layout : int { Contiguous = 0, Masked = 1 };
-
-constexpr int BM = 128;  // rows of a tile (TMEM lanes)
-constexpr int BK = 128;  // K per stage = scale-block size
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int NUM_THREADS = 320;
-constexpr int NUM_WARPS = NUM_THREADS / 32;
-constexpr int MAX_RUNS = 1024;
 constexpr int EPI_BAR = 1;  // named barrier of the 256 promotion/store threads
-
-struct GemmArgs {
-    const int32_t* routing;      // m_indices [M] | counts [G]
-    const void* sfa;             // see the layout notes of each entry point
-    const void* sfb;
-    void* d;                     // output base (owner-thread stores of tail rows)
-    int32_t* status;
-    uint64_t wait_limit_ns;
-    int64_t M;       // Contiguous: rows; Masked: cap
-    int64_t sfa_ld;  // Mp of the [K/128][Mp] activation scales
-    int64_t ldd;     // output row length in elements
-    int G;
-    int K;           // m-grouped K
-    int KB;          // m-grouped K / 128
-    int num_nb;      // output column tiles
-    int n128;        // m-grouped N / 128 (sfb row count)
-};
 
 constexpr int TBUFS = 4;          // TMEM partial buffers: the tensor core runs up to 3 blocks ahead
 constexpr int SF_GROUP = 4;       // 128-K blocks whose scales a promotion thread loads together
@@ -78,7 +58,6 @@ struct Plan {
     static constexpr int RING_OFF = 0;
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
-    static constexpr int SCHED_BYTES = (MAX_RUNS + 1) * 4 + 4 * MAX_RUNS * 4;
     static constexpr int BAR_OFF = (SCHED_OFF + SCHED_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
     static constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -105,22 +84,21 @@ struct TileInfo {
 };
 
 template <Layout L>
-__device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const int* run_first, const int* run_L,
-                                                const int* run_e, const int* run_x, int R, const GemmArgs& a) {
-    const int r = find_run(prefix, R, t);
-    const int local = t - prefix[r];
-    const int Lr = run_L[r];
+__device__ __forceinline__ TileInfo decode_tile(int t, const RunTable& rt, int R, const GemmArgs& a) {
+    const int r = find_run(rt.prefix, R, t);
+    const int local = t - rt.prefix[r];
+    const int Lr = rt.L[r];
     const int nb = local / Lr, j = local - nb * Lr;  // m-blocks fastest: consecutive tiles share B
     TileInfo ti;
     ti.nb = nb;
-    ti.e = run_e[r];
+    ti.e = rt.e[r];
     ti.valid = 0;
     ti.kbt = a.KB;
     if constexpr (L == Layout::Contiguous) {
-        ti.row0 = (run_first[r] + j) * BM;
+        ti.row0 = (rt.first[r] + j) * BM;
     } else {
         ti.row0 = j * BM;
-        const int v = run_x[r] - ti.row0;
+        const int v = rt.x[r] - ti.row0;
         ti.valid = v < BM ? v : BM;
     }
     return ti;
@@ -140,11 +118,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     uint8_t* ring = smem + P::RING_OFF;
     uint8_t* stg = smem + P::STG_OFF;
-    int* s_prefix = reinterpret_cast<int*>(smem + P::SCHED_OFF);
-    int* s_first = s_prefix + (MAX_RUNS + 1);
-    int* s_L = s_first + MAX_RUNS;
-    int* s_e = s_L + MAX_RUNS;
-    int* s_x = s_e + MAX_RUNS;
+    const RunTable rt = RunTable::at(smem + P::SCHED_OFF);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::BAR_OFF);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
@@ -152,10 +126,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* tempty = tfull + TBUFS;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + P::MISC_OFF + 4);
-    int* s_nruns = reinterpret_cast<int*>(smem + P::MISC_OFF + 8);
     int* s_ntiles = reinterpret_cast<int*>(smem + P::MISC_OFF + 12);
     uint32_t* s_ballot = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF + 32);  // [2][4]
-    int* s_scan = reinterpret_cast<int*>(smem + P::MISC_OFF + 64);              // [NUM_WARPS]
+    int* s_scan = reinterpret_cast<int*>(smem + P::MISC_OFF + 64);              // [NUM_THREADS / 32]
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -190,92 +163,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
 
     // ---------------------------------------------------------------- tile schedule
-    int R = 0;
-    if constexpr (L == Layout::Masked) {
-        R = a.G;
-        int bad = 0;
-        for (int g = tid; g < a.G; g += NUM_THREADS) {
-            int c = a.routing[g];
-            if (c < 0) { bad |= DG_STATUS_COUNT_GT_CAP; c = 0; }
-            if (c > a.M) { bad |= DG_STATUS_COUNT_GT_CAP; c = static_cast<int>(a.M); }
-            s_first[g] = g;
-            s_e[g] = g;
-            s_x[g] = c;
-            s_L[g] = (c + BM - 1) / BM;
-        }
-        if (bad && blockIdx.x == 0) status_or(a.status, bad);
-        __syncthreads();
-    } else if constexpr (L == Layout::Contiguous) {
-        const int nblk = static_cast<int>((a.M + BM - 1) / BM);
-        int16_t* blk_e = reinterpret_cast<int16_t*>(stg);  // staging is free during set-up
-        int bad = 0;
-        for (int b = tid; b < nblk; b += NUM_THREADS) {
-            int e = a.routing[static_cast<int64_t>(b) * BM];
-            if (e < -1 || e >= a.G) { bad |= DG_STATUS_BAD_INDEX; e = -1; }
-            blk_e[b] = static_cast<int16_t>(e);
-        }
-        if (bad && blockIdx.x == 0) status_or(a.status, bad);
-        __syncthreads();
-        const int ch = (nblk + NUM_THREADS - 1) / NUM_THREADS;
-        const int lo = tid * ch, hi = min(nblk, lo + ch);
-        int cnt = 0;
-        for (int b = lo; b < hi; ++b) {
-            const int e = blk_e[b];
-            cnt += (e >= 0 && (b == 0 || blk_e[b - 1] != e)) ? 1 : 0;
-        }
-        int total = 0;
-        int r = cta_excl_scan<NUM_THREADS>(cnt, s_scan, &total);
-        for (int b = lo; b < hi; ++b) {
-            const int e = blk_e[b];
-            if (e >= 0 && (b == 0 || blk_e[b - 1] != e)) {
-                if (r < MAX_RUNS) {
-                    s_first[r] = b;
-                    s_e[r] = e;
-                }
-                ++r;
-            }
-        }
-        int cnt2 = 0;
-        for (int b = lo; b < hi; ++b) {
-            const int e = blk_e[b];
-            cnt2 += (e >= 0 && (b == nblk - 1 || blk_e[b + 1] != e)) ? 1 : 0;
-        }
-        int total2 = 0;
-        int r2 = cta_excl_scan<NUM_THREADS>(cnt2, s_scan, &total2);  // its barriers order the s_first writes
-        for (int b = lo; b < hi; ++b) {
-            const int e = blk_e[b];
-            if (e >= 0 && (b == nblk - 1 || blk_e[b + 1] != e)) {
-                if (r2 < MAX_RUNS) s_L[r2] = b - s_first[r2] + 1;
-                ++r2;
-            }
-        }
-        R = total;
-        if (R > MAX_RUNS) {
-            if (blockIdx.x == 0 && tid == 0) status_or(a.status, DG_STATUS_TOO_MANY_RUNS);
-            R = MAX_RUNS;
-        }
-        __syncthreads();
-    }
-    {
-        // tiles per run -> prefix (runs of zero tiles keep L = 0)
-        const int ch = (R + NUM_THREADS - 1) / NUM_THREADS;
-        const int lo = tid * ch, hi = min(R, lo + ch);
-        int sum = 0;
-        for (int r = lo; r < hi; ++r) sum += s_L[r] * a.num_nb;
-        int total = 0;
-        int p = cta_excl_scan<NUM_THREADS>(sum, s_scan, &total);
-        for (int r = lo; r < hi; ++r) {
-            s_prefix[r] = p;
-            p += s_L[r] * a.num_nb;
-        }
-        if (tid == 0) {
-            s_prefix[R] = total;
-            *s_nruns = R;
-            *s_ntiles = total;
-        }
-        __syncthreads();
-    }
-    const int num_tiles = *s_ntiles;
+    const int R = build_runs<L, NUM_THREADS>(a, rt, s_scan, stg);  // staging is free during set-up
+    const int num_tiles = tile_prefix<NUM_THREADS, 1>(R, a.num_nb, rt, s_scan, s_ntiles);
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
 
@@ -287,7 +176,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<L>(t, s_prefix, s_first, s_L, s_e, s_x, R, a);
+                const TileInfo ti = decode_tile<L>(t, rt, R, a);
                 for (int kb = 0; kb < ti.kbt; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     uint8_t* sa = ring + stage * P::STAGE_BYTES;
@@ -321,7 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true, any = false;
             constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<L>(t, s_prefix, s_first, s_L, s_e, s_x, R, a);
+                const TileInfo ti = decode_tile<L>(t, rt, R, a);
                 for (int kb = 0; kb < ti.kbt; ++kb) {
                     if (!mbar_wait(&tempty[tb], tphase ^ 1u, wc)) { ok = false; break; }
                     if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
@@ -359,7 +248,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool have_store = false;
         int parity_slot = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            const TileInfo ti = decode_tile<L>(t, s_prefix, s_first, s_L, s_e, s_x, R, a);
+            const TileInfo ti = decode_tile<L>(t, rt, R, a);
             bool failed = false;
             bool row_ok = false;
             int64_t grow = 0;
@@ -382,32 +271,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Scales travel in registers, four 128-K blocks at a time: while the blocks of group g
             // are promoted, the loads of group g + 1 are in flight (issued one group earlier).
             const int sbi0 = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB;
-            auto load_group = [&](int g, float (&sa)[SF_GROUP], float (&sb)[SF_GROUP]) {
+            // raw scale bits (fp32, or the UE8M0 byte): converted where used, so that no
+            // instruction waits on the loads until the group's first block is promoted
+            auto load_group = [&](int g, uint32_t (&sa)[SF_GROUP], uint32_t (&sb)[SF_GROUP]) {
 #pragma unroll
                 for (int u = 0; u < SF_GROUP; ++u) {
                     const int kbi = g * SF_GROUP + u;
-                    sa[u] = 0.0f;
-                    sb[u] = 0.0f;
+                    sa[u] = 0u;
+                    sb[u] = 0u;
                     if (row_ok && kbi < ti.kbt) {
                         const int64_t idx = static_cast<int64_t>(kbi) * a.sfa_ld + grow;
                         if constexpr (SF_UE8M0) {
-                            sa[u] = ue8m0_to_float(__ldg(static_cast<const uint8_t*>(a.sfa) + idx));
-                            sb[u] = ue8m0_to_float(__ldg(static_cast<const uint8_t*>(a.sfb) + sbi0 + kbi));
+                            sa[u] = __ldg(static_cast<const uint8_t*>(a.sfa) + idx);
+                            sb[u] = __ldg(static_cast<const uint8_t*>(a.sfb) + sbi0 + kbi);
                         } else {
-                            sa[u] = __ldg(static_cast<const float*>(a.sfa) + idx);
-                            sb[u] = __ldg(static_cast<const float*>(a.sfb) + sbi0 + kbi);
+                            sa[u] = __float_as_uint(__ldg(static_cast<const float*>(a.sfa) + idx));
+                            sb[u] = __float_as_uint(__ldg(static_cast<const float*>(a.sfb) + sbi0 + kbi));
                         }
                     }
                 }
             };
-            float sa_c[SF_GROUP], sb_c[SF_GROUP], sa_n[SF_GROUP], sb_n[SF_GROUP];
+            auto scale_of = [&](uint32_t sa, uint32_t sb) -> float {
+                if constexpr (SF_UE8M0)
+                    return ue8m0_to_float(static_cast<uint8_t>(sa)) * ue8m0_to_float(static_cast<uint8_t>(sb));
+                else
+                    return __uint_as_float(sa) * __uint_as_float(sb);
+            };
+            uint32_t sa_c[SF_GROUP], sb_c[SF_GROUP], sa_n[SF_GROUP], sb_n[SF_GROUP];
             load_group(0, sa_c, sb_c);
             load_group(1, sa_n, sb_n);
             for (int kb0 = 0; kb0 < ti.kbt && !failed; kb0 += SF_GROUP) {
 #pragma unroll
                 for (int u = 0; u < SF_GROUP; ++u) {
                     if (kb0 + u >= ti.kbt) break;
-                    const float s = sa_c[u] * sb_c[u];
+                    const float s = scale_of(sa_c[u], sb_c[u]);
                     if (!mbar_wait(&tfull[tb], tphase, wc)) { failed = true; break; }
                     tc_fence_after();
                     uint32_t v[P::CPT / 32][32];
@@ -556,9 +453,25 @@ CUtensorMapDataType out_tmap_type(int out) {
     return out == DG_OUT_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
+// Kernel choice.  Both kernels promote the same fp32 tensor-core partials in the same K order
+// with the same FMAs, so their outputs are bitwise identical and the choice may follow a hint.
+// CTA pairs (256 x PAIR_BN tiles, gemm_pair.cu, bf16 output only) halve the weight bytes
+// fetched per row pair but compute a run's odd last block for nothing, so they are chosen when
+// groups are expected to span two or more 128-row blocks (the masked layout's expected_m hint);
+// every other call runs on single CTAs (128 x 128 tiles).  A test hook can force either.
+std::atomic<int> g_force_kernel{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA pairs
+
+bool use_pair(int out, bool prefer_pair) {
+    if (out != DG_OUT_BF16) return false;
+    const int f = g_force_kernel.load(std::memory_order_relaxed);
+    return f == 0 ? prefer_pair : f == 2;
+}
+
 template <Layout L>
-int dispatch_mgrouped(int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD,
-                      const CUtensorMap& tD8, const GemmArgs& args, cudaStream_t s) {
+int dispatch_mgrouped(bool pair, int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB,
+                      const CUtensorMap& tD, const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
+    if (pair) return launch_mgrouped_pair(L, fmt == DG_SF_UE8M0, tA, tB, tD, tD8, args, s);
+    args.num_nb = static_cast<int>(args.N / MG_BN);
     // bf16 output stages half as much as fp32, which leaves room for a fifth ring stage
     if (out == DG_OUT_FP32) {
         if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, true, true>(tA, tB, tD, tD8, args, s);
@@ -589,7 +502,6 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
                                        int out_dtype, const int32_t* counts, int G, int64_t cap, int64_t N, int64_t K,
                                        int expected_m, int sf_format, void* workspace, size_t workspace_bytes,
                                        int32_t* status, void* stream) {
-    (void)expected_m;
     (void)workspace;
     (void)workspace_bytes;
     DG_CHECK_ARG(cap >= 0, "cap must be >= 0");
@@ -600,6 +512,7 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
     const int esize = out_dtype == DG_OUT_FP32 ? 4 : 2;
     const int64_t M = static_cast<int64_t>(G) * cap;
     const int64_t Mp = sf_format == DG_SF_FP32 ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
+    const bool pair = use_pair(out_dtype, expected_m > BM);
     CUtensorMap tA, tB, tD, tD8;
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(cap), static_cast<uint64_t>(G)};
@@ -612,7 +525,8 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        uint32_t box[3] = {BK, MG_BN, 1};
+        const uint32_t brows = pair ? PAIR_B_ROWS : MG_BN;
+        uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
             return rc;
@@ -640,9 +554,9 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
     args.G = G;
     args.K = static_cast<int>(K);
     args.KB = static_cast<int>(K / BK);
-    args.num_nb = static_cast<int>(N / MG_BN);
     args.n128 = static_cast<int>(N / 128);
-    return dispatch_mgrouped<Layout::Masked>(out_dtype, sf_format, tA, tB, tD, tD8, args,
+    args.N = N;
+    return dispatch_mgrouped<Layout::Masked>(pair, out_dtype, sf_format, tA, tB, tD, tD8, args,
                                              static_cast<cudaStream_t>(stream));
 }
 
@@ -659,6 +573,7 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
     DG_CHECK_SUPPORTED((M + BM - 1) / BM <= DG_MAX_M_BLOCKS, "M too large (at most %d rows)", DG_MAX_M_BLOCKS * BM);
     const int esize = out_dtype == DG_OUT_FP32 ? 4 : 2;
     const int64_t Mp = sf_format == DG_SF_FP32 ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
+    const bool pair = use_pair(out_dtype, false);
     CUtensorMap tA, tB, tD, tD8;
     {
         uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
@@ -671,7 +586,8 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        uint32_t box[3] = {BK, MG_BN, 1};
+        const uint32_t brows = pair ? PAIR_B_ROWS : MG_BN;
+        uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
             return rc;
@@ -699,8 +615,17 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
     args.G = G;
     args.K = static_cast<int>(K);
     args.KB = static_cast<int>(K / BK);
-    args.num_nb = static_cast<int>(N / MG_BN);
     args.n128 = static_cast<int>(N / 128);
-    return dispatch_mgrouped<Layout::Contiguous>(out_dtype, sf_format, tA, tB, tD, tD8, args,
+    args.N = N;
+    return dispatch_mgrouped<Layout::Contiguous>(pair, out_dtype, sf_format, tA, tB, tD, tD8, args,
                                                  static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------------- test hook
+// Selects the m-grouped kernel of later bf16-output calls in this process: 0 automatic,
+// 1 single-CTA 128 x 128 tiles, 2 CTA pairs.  Lets the tests hold both kernels to the oracle.
+extern "C" int dg_testing_mgrouped_kernel(int which) {
+    DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0, 1 or 2");
+    g_force_kernel.store(which, std::memory_order_relaxed);
+    return DG_OK;
 }

@@ -1,0 +1,168 @@
+// mgrouped.cuh - pieces shared by the two m-grouped FP8 GEMM kernels (gemm.cu: one CTA per
+// 128 x 128 tile; gemm_pair.cu: a CTA pair per 256 x 192 tile): the layouts, the kernel
+// arguments, and the on-device tile schedule that every CTA rebuilds at the start of a launch
+// from the routing tensor ("SM120 m_grouped_fp8 contiguous kernel: illegal memory access at
+// CUDA graph replay", #444 - nothing derived from routing is cached across launches).
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "dg.h"
+#include "kernel_common.cuh"
+
+namespace dg {
+
+enum class Layout : int { Contiguous = 0, Masked = 1 };
+
+constexpr int BM = 128;        // rows of an m-block (TMEM lanes)
+constexpr int BK = 128;        // K per pipeline stage = scale-block size
+constexpr int MAX_RUNS = 1024;  // runs of consecutive same-expert m-blocks kept in shared memory
+
+struct GemmArgs {
+    const int32_t* routing;      // m_indices [M] | counts [G]
+    const void* sfa;             // see the layout notes of each entry point
+    const void* sfb;
+    void* d;                     // output base (owner-thread stores of tail rows)
+    int32_t* status;
+    uint64_t wait_limit_ns;
+    int64_t M;       // Contiguous: rows; Masked: cap
+    int64_t sfa_ld;  // Mp of the [K/128][Mp] activation scales
+    int64_t ldd;     // output row length in elements
+    int64_t N;       // output columns
+    int G;
+    int K;           // m-grouped K
+    int KB;          // m-grouped K / 128
+    int num_nb;      // output column tiles of the launched kernel
+    int n128;        // N / 128 (sfb row count)
+};
+
+// Shared-memory bytes of the run table used by build_runs / tile_prefix.
+constexpr int SCHED_BYTES = (MAX_RUNS + 1) * 4 + 4 * MAX_RUNS * 4;
+
+struct RunTable {
+    int* prefix;  // [MAX_RUNS + 1] first tile of each run
+    int* first;   // [MAX_RUNS] Contiguous: first m-block of the run; Masked: group
+    int* L;       // [MAX_RUNS] m-blocks of the run
+    int* e;       // [MAX_RUNS] expert of the run
+    int* x;       // [MAX_RUNS] Masked: valid rows of the group (count clamped to [0, cap])
+    __device__ static RunTable at(uint8_t* base) {
+        RunTable t;
+        t.prefix = reinterpret_cast<int*>(base);
+        t.first = t.prefix + (MAX_RUNS + 1);
+        t.L = t.first + MAX_RUNS;
+        t.e = t.L + MAX_RUNS;
+        t.x = t.e + MAX_RUNS;
+        return t;
+    }
+};
+
+// Builds the runs of the launch from the routing tensor; every thread of the CTA calls it and
+// gets the run count.  Masked: one run per group, L = ceil(count / 128).  Contiguous: maximal
+// sequences of consecutive 128-row blocks whose first row carries the same expert (blocks
+// whose first row is -1 are padding and skipped).  `scratch` holds one int16 per m-block.
+template <Layout L, int NT>
+__device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, void* scratch) {
+    const int tid = threadIdx.x;
+    int R = 0;
+    if constexpr (L == Layout::Masked) {
+        R = a.G;
+        int bad = 0;
+        for (int g = tid; g < a.G; g += NT) {
+            int c = a.routing[g];
+            if (c < 0) { bad |= DG_STATUS_COUNT_GT_CAP; c = 0; }
+            if (c > a.M) { bad |= DG_STATUS_COUNT_GT_CAP; c = static_cast<int>(a.M); }
+            rt.first[g] = g;
+            rt.e[g] = g;
+            rt.x[g] = c;
+            rt.L[g] = (c + BM - 1) / BM;
+        }
+        if (bad && blockIdx.x == 0) status_or(a.status, bad);
+        __syncthreads();
+    } else {
+        const int nblk = static_cast<int>((a.M + BM - 1) / BM);
+        int16_t* blk_e = static_cast<int16_t*>(scratch);
+        int bad = 0;
+        for (int b = tid; b < nblk; b += NT) {
+            int e = a.routing[static_cast<int64_t>(b) * BM];
+            if (e < -1 || e >= a.G) { bad |= DG_STATUS_BAD_INDEX; e = -1; }
+            blk_e[b] = static_cast<int16_t>(e);
+        }
+        if (bad && blockIdx.x == 0) status_or(a.status, bad);
+        __syncthreads();
+        const int ch = (nblk + NT - 1) / NT;
+        const int lo = tid * ch, hi = min(nblk, lo + ch);
+        int cnt = 0;
+        for (int b = lo; b < hi; ++b) {
+            const int e = blk_e[b];
+            cnt += (e >= 0 && (b == 0 || blk_e[b - 1] != e)) ? 1 : 0;
+        }
+        int total = 0;
+        int r = cta_excl_scan<NT>(cnt, s_scan, &total);
+        for (int b = lo; b < hi; ++b) {
+            const int e = blk_e[b];
+            if (e >= 0 && (b == 0 || blk_e[b - 1] != e)) {
+                if (r < MAX_RUNS) {
+                    rt.first[r] = b;
+                    rt.e[r] = e;
+                }
+                ++r;
+            }
+        }
+        int cnt2 = 0;
+        for (int b = lo; b < hi; ++b) {
+            const int e = blk_e[b];
+            cnt2 += (e >= 0 && (b == nblk - 1 || blk_e[b + 1] != e)) ? 1 : 0;
+        }
+        int total2 = 0;
+        int r2 = cta_excl_scan<NT>(cnt2, s_scan, &total2);  // its barriers order the rt.first writes
+        for (int b = lo; b < hi; ++b) {
+            const int e = blk_e[b];
+            if (e >= 0 && (b == nblk - 1 || blk_e[b + 1] != e)) {
+                if (r2 < MAX_RUNS) rt.L[r2] = b - rt.first[r2] + 1;
+                ++r2;
+            }
+        }
+        R = total;
+        if (R > MAX_RUNS) {
+            if (blockIdx.x == 0 && tid == 0) status_or(a.status, DG_STATUS_TOO_MANY_RUNS);
+            R = MAX_RUNS;
+        }
+        __syncthreads();
+    }
+    return R;
+}
+
+// Tiles per run -> prefix; returns the tile count of the launch (all threads call).  A run of
+// L m-blocks holds ceil(L / MB) m-tiles of MB blocks each, times num_nb column tiles.
+template <int NT, int MB>
+__device__ int tile_prefix(int R, int num_nb, const RunTable& rt, int* s_scan, int* s_ntiles) {
+    const int tid = threadIdx.x;
+    const int ch = (R + NT - 1) / NT;
+    const int lo = tid * ch, hi = min(R, lo + ch);
+    int sum = 0;
+    for (int r = lo; r < hi; ++r) sum += (rt.L[r] + MB - 1) / MB * num_nb;
+    int total = 0;
+    int p = cta_excl_scan<NT>(sum, s_scan, &total);
+    for (int r = lo; r < hi; ++r) {
+        rt.prefix[r] = p;
+        p += (rt.L[r] + MB - 1) / MB * num_nb;
+    }
+    if (tid == 0) {
+        rt.prefix[R] = total;
+        *s_ntiles = total;
+    }
+    __syncthreads();
+    return *s_ntiles;
+}
+
+// The CTA-pair kernel (bf16 output only), defined in gemm_pair.cu: output tiles of 256 rows x
+// PAIR_BN columns; its B tensor map has boxes of 128 (K) x PAIR_B_ROWS rows.
+constexpr int PAIR_BN = 192;
+constexpr int PAIR_B_ROWS = PAIR_BN / 2;
+// Returns DG_OK or an error.
+int launch_mgrouped_pair(Layout L, bool sf_ue8m0, const CUtensorMap& tA, const CUtensorMap& tB,
+                         const CUtensorMap& tD, const CUtensorMap& tD8, GemmArgs args, void* stream);
+
+}  // namespace dg

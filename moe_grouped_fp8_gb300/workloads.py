@@ -100,6 +100,7 @@ class Masked:
     a_scale: float = 1.0
     b_scale: float = 1.0
     name: str = "masked"
+    expected_m: int = 0  # the caller's hint of rows per group (what a decode step passes)
 
     def draw(self, device="cpu"):
         a = randn_bf16((self.G, self.cap, self.K), self.seed, self.a_scale, device)
@@ -203,7 +204,7 @@ def contiguous_prefill() -> Contiguous:
 def masked_decode() -> Masked:
     G, cap = 32, 4096
     return Masked(G=G, cap=cap, N=6144, K=7168, counts=poisson_counts(G, 192.0, cap, 1004),
-                  seed=1004, b_scale=0.02)
+                  seed=1004, b_scale=0.02, expected_m=192)
 
 
 def many_expert(E: int, which: str = "w13", seed: int = 1005) -> Contiguous:

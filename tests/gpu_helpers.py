@@ -7,7 +7,7 @@ import numpy as np
 import torch
 
 import oracle
-from moe_grouped_fp8_gb300 import DG_SF_FP32, api
+from moe_grouped_fp8_gb300 import DG_SF_FP32, _lib, api
 
 # Acceptance thresholds: calc_diff <= 2e-5 for bf16 outputs and <= 1e-6 for fp32 outputs, and
 # max |err| <= 1e-2 * max |ref| on the valid elements.
@@ -104,3 +104,10 @@ def ref_out(d64: np.ndarray, fp32_out: bool) -> np.ndarray:
     if fp32_out:
         return d64.astype(np.float32).astype(np.float64)
     return oracle.bf16_bits_to_f64(oracle.round_bf16(d64))
+
+
+def set_mgrouped_kernel(which: str) -> None:
+    """Test hook: the m-grouped kernel of later bf16-output calls ("auto", "single" 128 x 128
+    CTA tiles, "pair" 256 x 192 CTA-pair tiles)."""
+    lib = _lib.load()
+    _lib.check(lib.dg_testing_mgrouped_kernel({"auto": 0, "single": 1, "pair": 2}[which]))

@@ -9,9 +9,19 @@ from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_BAD_INDEX, 
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
-                         sentinel_value, sync, to_f64)
+                         sentinel_value, set_mgrouped_kernel, sync, to_f64)
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["pair", "single"], autouse=True)
+def mgrouped_kernel(request):
+    """bf16 outputs run on CTA pairs by default; every small case also runs on single-CTA tiles."""
+    if request.param == "single" and request.node.get_closest_marker("slow"):
+        pytest.skip("full-size cases run on the default kernel")
+    set_mgrouped_kernel(request.param)
+    yield request.param
+    set_mgrouped_kernel("auto")
 
 
 def contiguous_case(a, b, m_indices, fmt=DG_SF_FP32, out=torch.bfloat16, calls=1):
@@ -74,6 +84,16 @@ def test_all_padding_and_ragged_last_block():
     mi2 = np.full(200, -1, np.int32)
     mi2[128:133] = 1                                   # ragged final block (rows 128..199 of a 256 block)
     contiguous_case(a, b, mi2)
+
+
+def test_pair_tiles_odd_runs_and_column_tail():
+    """Runs of 5, 1, 3 and 1 m-blocks (a CTA pair's odd block is computed, never stored) and
+    N = 640 (three 192-column tiles and a 64-column tail)."""
+    counts = [640, 1, 0, 300, 128]
+    mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
+    a = wl.randn_bf16((mi.size, 256), 95)
+    b = wl.randn_bf16((5, 640, 256), 96, 0.05)
+    contiguous_case(a, b, mi)
 
 
 def test_segments_out_of_expert_order():

@@ -9,9 +9,19 @@ from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_COUNT_GT_CA
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
-                         sentinel_value, sync, to_f64)
+                         sentinel_value, set_mgrouped_kernel, sync, to_f64)
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["pair", "single"], autouse=True)
+def mgrouped_kernel(request):
+    """bf16 outputs run on CTA pairs by default; every small case also runs on single-CTA tiles."""
+    if request.param == "single" and request.node.get_closest_marker("slow"):
+        pytest.skip("full-size cases run on the default kernel")
+    set_mgrouped_kernel(request.param)
+    yield request.param
+    set_mgrouped_kernel("auto")
 
 
 def masked_case(a, b, counts, fmt=DG_SF_FP32, out=torch.bfloat16, expected_m=0, calls=1):
@@ -81,6 +91,14 @@ def test_formats_and_output_dtypes(fmt, out):
     masked_case(a, b, [200, 77, 129], fmt=fmt, out=out)
 
 
+def test_pair_tiles_odd_blocks_and_column_tail():
+    """Groups of 5 and 4 m-blocks (the last pair of the first is half empty), N = 640."""
+    G, cap, N, K = 2, 640, 640, 256
+    a = wl.randn_bf16((G, cap, K), 97)
+    b = wl.randn_bf16((G, N, K), 98, 0.05)
+    masked_case(a, b, [640, 385])
+
+
 def test_single_expert_and_all_empty():
     a = wl.randn_bf16((1, 130, 256), 21)
     b = wl.randn_bf16((1, 128, 256), 22)
@@ -96,6 +114,22 @@ def test_expected_m_does_not_change_result():
     d1, _ = masked_case(a, b, w.counts, expected_m=1)
     d2, _ = masked_case(a, b, w.counts, expected_m=4096)
     assert np.array_equal(out_bits(d1), out_bits(d2))
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+def test_single_and_pair_kernels_bitwise_equal(mgrouped_kernel, fmt):
+    """Both m-grouped kernels give the same bits, which is what lets expected_m choose one."""
+    if mgrouped_kernel == "single":
+        pytest.skip("runs both kernels itself")
+    G, cap, N, K = 3, 300, 640, 512
+    a = wl.randn_bf16((G, cap, K), 13, 2.0)
+    b = wl.randn_bf16((G, N, K), 14, 0.02)
+    outs = []
+    for which in ("single", "pair"):
+        set_mgrouped_kernel(which)
+        d, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
+        outs.append(out_bits(d))
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_counts_out_of_range_are_clamped_and_flagged():
