@@ -322,6 +322,10 @@ class MGroupedWorkload:
             self.w = wl.masked_repro()
         elif kind == "contiguous_prefill":
             self.w = wl.contiguous_prefill()
+        elif kind == "masked_decode_g8":
+            self.w = wl.masked_decode_g8()
+        elif kind == "contiguous_prefill_g8":
+            self.w = wl.contiguous_prefill_g8()
         elif kind.startswith("many_expert_"):
             _, _, which, e = kind.split("_")
             self.w = wl.many_expert(int(e[1:]), which)
@@ -592,7 +596,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="kgrouped_wgrad",
                     help="kgrouped_wgrad | masked_decode | masked_repro | contiguous_prefill | "
-                         "many_expert_{w13,w2}_E{1,32,113}")
+                         "many_expert_{w13,w2}_E{1,32,113} | masked_decode_g8 | contiguous_prefill_g8 "
+                         "(the last two: 8-expert cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

@@ -207,6 +207,21 @@ def masked_decode() -> Masked:
                   seed=1004, b_scale=0.02, expected_m=192)
 
 
+# Reduced cases for profiler captures: the per-expert shapes above with 8 experts, so that the
+# inputs still exceed L2 (weights 235 / 352 MB) while a capture holds well under a few GB.
+def contiguous_prefill_g8() -> Contiguous:
+    G, T = 8, 2048
+    counts = zipf_counts(T, G, 1.1, 1003)
+    return Contiguous(G=G, N=4096, K=7168, counts=counts, m_max=contiguous_capacity(T, G),
+                      seed=1003, b_scale=0.02, name="contiguous_prefill_g8")
+
+
+def masked_decode_g8() -> Masked:
+    G, cap = 8, 1024
+    return Masked(G=G, cap=cap, N=6144, K=7168, counts=poisson_counts(G, 192.0, cap, 1004),
+                  seed=1004, b_scale=0.02, expected_m=192, name="masked_decode_g8")
+
+
 def many_expert(E: int, which: str = "w13", seed: int = 1005) -> Contiguous:
     G = 288
     N, K = (512, 4096) if which == "w13" else (4096, 256)
