@@ -62,6 +62,8 @@ def _load():
             lib.oracle_dot_rows.argtypes = [P, P, P, P, i64, i64, P]
             lib.oracle_gemm_masked.argtypes = [P, P, P, P, P, i32, i64, i64, i64, P]
             lib.oracle_gemm_kgrouped.argtypes = [P, P, P, P, P, P, i32, i64, i64, i64, P]
+            lib.oracle_gemm_masked_bf16.argtypes = [P, P, P, i32, i64, i64, i64, P]
+            lib.oracle_gemm_contiguous_bf16.argtypes = [P, P, P, i64, i32, i64, i64, P]
             lib.oracle_round_bf16.restype = ctypes.c_uint16
             lib.oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.oracle_round_bf16_array.argtypes = [P, i64, P]
@@ -203,6 +205,36 @@ def gemm_masked(qa, sfa, qb, sfb, counts) -> np.ndarray:
     N = qb.shape[1]
     d = np.full((G, cap, N), np.nan, np.float64)
     _load().oracle_gemm_masked(_p(qa), _p(sfa), _p(qb), _p(sfb), _p(cnt), G, cap, N, K, _p(d))
+    return d
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """uint16 bit patterns of a bf16 torch tensor (or of a uint16 array)."""
+    if hasattr(x, "view") and not isinstance(x, np.ndarray):
+        import torch
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return np.ascontiguousarray(x, np.uint16)
+
+
+def gemm_masked_bf16(a, b, counts) -> np.ndarray:
+    """BF16 masked GEMM in fp64: D [G, cap, N]; rows at or past min(count, cap) are NaN."""
+    a, b = _bf16_bits(a), _bf16_bits(b)
+    cnt = _c(counts, np.int32)
+    G, cap, K = a.shape
+    N = b.shape[1]
+    d = np.full((G, cap, N), np.nan, np.float64)
+    _load().oracle_gemm_masked_bf16(_p(a), _p(b), _p(cnt), G, cap, N, K, _p(d))
+    return d
+
+
+def gemm_contiguous_bf16(a, b, m_indices) -> np.ndarray:
+    """BF16 contiguous GEMM in fp64: D [M, N]; rows not routed are NaN."""
+    a, b = _bf16_bits(a), _bf16_bits(b)
+    mi = _c(m_indices, np.int32)
+    M, K = a.shape
+    G, N, _ = b.shape
+    d = np.full((M, N), np.nan, np.float64)
+    _load().oracle_gemm_contiguous_bf16(_p(a), _p(b), _p(mi), M, G, N, K, _p(d))
     return d
 
 

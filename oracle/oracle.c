@@ -369,6 +369,49 @@ void oracle_gemm_kgrouped(const uint8_t* a_packed, const float* sfa, const uint8
  * Output rounding and comparison.
  * --------------------------------------------------------------------------------------*/
 
+/* ----------------------------------------------------------------------------------------
+ * BF16 m-grouped GEMMs (#469 reproduction: `m_grouped_bf16_gemm_nt_masked`, checked against
+ * torch.bmm(a.double(), b.double().mT) rounded to bf16).  No scales: the bf16 inputs are
+ * exact in fp64 and the products accumulate in fp64.
+ *   masked:     D[g][r][n] = sum_k a[g][r][k] b[g][n][k] for r < min(max(counts[g], 0), cap)
+ *   contiguous: D[m][n]    = sum_k a[m][k] b[e][n][k]    for e = m_indices[m] in [0, G)
+ * Rows that are not valid are not written.
+ * --------------------------------------------------------------------------------------*/
+void oracle_gemm_masked_bf16(const uint16_t* a, const uint16_t* b, const int32_t* counts, int G,
+                             int64_t cap, int64_t N, int64_t K, double* d) {
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t g = 0; g < G; ++g) {
+        for (int64_t r = 0; r < cap; ++r) {
+            int64_t v = counts[g];
+            if (v < 0) v = 0;
+            if (v > cap) v = cap;
+            if (r >= v) continue;
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += (double)bf16_to_float(a[(g * cap + r) * K + k]) *
+                           (double)bf16_to_float(b[(g * N + n) * K + k]);
+                d[(g * cap + r) * N + n] = acc;
+            }
+        }
+    }
+}
+
+void oracle_gemm_contiguous_bf16(const uint16_t* a, const uint16_t* b, const int32_t* m_indices,
+                                 int64_t M, int G, int64_t N, int64_t K, double* d) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        int64_t e = m_indices[m];
+        if (e < 0 || e >= G) continue;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)bf16_to_float(a[m * K + k]) * (double)bf16_to_float(b[(e * N + n) * K + k]);
+            d[m * N + n] = acc;
+        }
+    }
+}
+
 /* fp64 -> bf16 bits, a single round-to-nearest-even (no intermediate fp32 rounding).
  * bf16: 8 exponent bits (bias 127), 7 mantissa bits; min normal 2^-126, subnormal step
  * 2^-133; overflow past the largest finite value plus half an ulp gives inf. */

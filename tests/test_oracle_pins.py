@@ -500,3 +500,54 @@ def test_calc_diff_closed_forms():
     eps = 1e-3
     want = eps ** 2 / (2 + 2 * eps + eps ** 2)
     assert abs(oracle.calc_diff(x, (1 + eps) * x) - want) < 1e-12
+
+
+# ---------------------------------------------------------------------------- BF16 grouped GEMM
+# "Fix cross-expert output overwrites in SM90 masked GEMM" (#469), reproduction: the reference
+# of m_grouped_bf16_gemm_nt_masked is bmm(a.double(), b.double().mT) on the valid rows.
+
+def _bf16(shape, seed, scale=1.0):
+    return wl.randn_bf16(shape, seed, scale)
+
+
+@pytest.mark.parametrize("G,cap,N,K", [(3, 7, 5, 9), (2, 33, 16, 40)])
+def test_bf16_masked_equals_batched_matmul_on_valid_rows(G, cap, N, K):
+    a, b = _bf16((G, cap, K), 71), _bf16((G, N, K), 72)
+    counts = np.array([cap, 0, 3][:G], np.int32)
+    d = oracle.gemm_masked_bf16(a, b, counts)
+    ref = np.einsum("grk,gnk->grn", a.double().numpy(), b.double().numpy())   # library routine
+    for g in range(G):
+        v = int(np.clip(counts[g], 0, cap))
+        np.testing.assert_allclose(d[g, :v], ref[g, :v], rtol=1e-12, atol=1e-12)
+        assert np.all(np.isnan(d[g, v:])), "rows past the count must stay untouched"
+
+
+def test_bf16_masked_counts_clamped():
+    a, b = _bf16((2, 4, 8), 73), _bf16((2, 3, 8), 74)
+    d = oracle.gemm_masked_bf16(a, b, np.array([-3, 99], np.int32))
+    assert np.all(np.isnan(d[0])) and not np.any(np.isnan(d[1]))
+
+
+def test_bf16_products_exact_closed_form():
+    """One nonzero K term per output: D is the exact product of two bf16 values; a permutation
+    matrix as B permutes A's columns (a transposed operand or a wrong index fails here)."""
+    G, cap, K = 1, 4, 8
+    a = _bf16((G, cap, K), 75)
+    perm = np.random.default_rng(3).permutation(K)
+    b = torch.zeros((G, K, K), dtype=torch.bfloat16)
+    b[0, np.arange(K), perm] = 1.0                    # row n of B selects A column perm[n]
+    d = oracle.gemm_masked_bf16(a, b, np.array([cap], np.int32))
+    np.testing.assert_array_equal(d[0], a[0].double().numpy()[:, perm])
+
+
+def test_bf16_contiguous_routing():
+    M, G, N, K = 10, 3, 6, 12
+    a, b = _bf16((M, K), 76), _bf16((G, N, K), 77)
+    mi = np.array([0, 0, 2, -1, 1, 7, 2, 2, -1, 0], np.int32)
+    d = oracle.gemm_contiguous_bf16(a, b, mi)
+    an, bn = a.double().numpy(), b.double().numpy()
+    for m in range(M):
+        if 0 <= mi[m] < G:
+            np.testing.assert_allclose(d[m], bn[mi[m]] @ an[m], rtol=1e-12, atol=1e-12)
+        else:
+            assert np.all(np.isnan(d[m]))
