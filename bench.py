@@ -462,11 +462,106 @@ class MGroupedWorkload:
         return c
 
 
+class BF16GroupedWorkload:
+    """BF16 m-grouped GEMM ("Fix cross-expert output overwrites in SM90 masked GEMM", #469: the
+    reproduction's m_grouped_bf16_gemm_nt_masked); a step = the GEMM (no casts)."""
+
+    metric = "grouped BF16 GEMM TFLOP/s on valid rows; % of GB300 BF16 tensor/HBM roofline"
+    dtype = "bf16 (fp32 accumulate)"
+    has_casts = False
+    launches_per_step = 1
+
+    def __init__(self, kind, device, ours=True):
+        from moe_grouped_fp8_gb300 import workloads as wl
+        base = kind[:-len("_bf16")]
+        self.w = {"masked_repro": wl.masked_repro, "masked_decode": wl.masked_decode,
+                  "contiguous_prefill": wl.contiguous_prefill}[base]()
+        w = self.w
+        self.masked = isinstance(w, wl.Masked)
+        self.kernel_name = "k_grouped_gemm_bf16"
+        G, N, K = w.G, w.N, w.K
+        a, b = w.draw(device=device)
+        self.M = G * w.cap if self.masked else w.m_max
+        self.a, self.b = a, b
+        if self.masked:
+            self.e_sample = int(np.argmax(w.counts))
+            self.a_rows = a[self.e_sample, :4].cpu()
+        else:
+            rows = np.nonzero(w.m_indices >= 0)[0][:4]
+            self.e_sample = int(w.m_indices[rows[0]])
+            self.a_rows = a[torch.from_numpy(rows).to(a.device)].cpu()
+        self.b_block = b[self.e_sample, :128].cpu()
+        self.R = 1
+        self.name = f"{kind}_G{G}_N{N}_K{K}"
+        if not ours:
+            return
+        from moe_grouped_fp8_gb300 import api
+        self.api = api
+        if self.masked:
+            self.counts = torch.tensor(w.counts, dtype=torch.int32, device=device)
+            self.d = torch.empty(G, w.cap, N, dtype=torch.bfloat16, device=device)
+        else:
+            self.mi = torch.from_numpy(w.m_indices).to(device)
+            self.d = torch.empty(self.M, N, dtype=torch.bfloat16, device=device)
+
+    @property
+    def flops(self):
+        return self.w.flops
+
+    def peak_tflops(self, peaks):
+        return peaks["bf16_tflops"]
+
+    def casts(self, r):
+        pass
+
+    def gemm_only(self, r):
+        if self.masked:
+            self.api.dg_m_grouped_bf16_masked(self.a, self.b, self.d, self.counts, self.w.expected_m)
+        else:
+            self.api.dg_m_grouped_bf16_contiguous(self.a, self.b, self.d, self.mi)
+
+    wgrad = gemm_only
+    step = gemm_only
+
+    def gemm_bytes(self):
+        w = self.w
+        counts = np.clip(np.asarray(w.counts), 0, getattr(w, "cap", 1 << 30))
+        live, valid = int((counts > 0).sum()), int(counts.sum())
+        return 2 * (live * w.N * w.K + valid * w.K + valid * w.N)
+
+    def cast_bytes(self):
+        return 0
+
+    def e2e(self, steps, stream):
+        return None
+
+    def oracle_step(self, channels=None):
+        """Oracle on a bounded sample: 4 routed rows x the expert's first 128 output columns."""
+        import oracle
+        t0 = time.perf_counter()
+        oracle.gemm_contiguous_bf16(self.a_rows, self.b_block.unsqueeze(0), np.zeros(4, np.int32))
+        return time.perf_counter() - t0, 2.0 * 4 * 128 * self.w.K
+
+    def config(self):
+        w = self.w
+        c = {"workload": self.name, "experts": w.G, "N": w.N, "K": w.K, "valid_rows": w.valid_rows,
+             "operands": "bf16", "l2": "weights exceed L2" if 2 * w.G * w.N * w.K > 2 * L2_BYTES
+             else "L2-resident (launch-latency-bound shape)", "graphs": "each step replayed from a CUDA graph"}
+        if self.masked:
+            c["capacity"] = w.cap
+            c["expected_m"] = w.expected_m
+        else:
+            c["m_rows"] = self.M
+        return c
+
+
 # ----------------------------------------------------------------------------- arms
 
 def make_workload(kind, device, ours=True):
     if kind == "kgrouped_wgrad":
         return KGroupedWorkload(device, sets=None if ours else 1, ours=ours)
+    if kind.endswith("_bf16"):
+        return BF16GroupedWorkload(kind, device, ours=ours)
     return MGroupedWorkload(kind, device, ours=ours)
 
 
@@ -485,7 +580,8 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         step_graphs = [capture(lambda r=r: wk.step(r), stream) for r in range(wk.R)]
         gemm_graphs = [capture(lambda r=r: wk.gemm_only(r), stream) for r in range(wk.R)]
-        cast_graphs = [capture(lambda r=r: wk.casts(r), stream) for r in range(wk.R)]
+        has_casts = getattr(wk, "has_casts", True)
+        cast_graphs = [capture(lambda r=r: wk.casts(r), stream) for r in range(wk.R)] if has_casts else []
         torch.cuda.synchronize()
 
         for i in range(args.warmup):
@@ -508,7 +604,7 @@ def run_ours(args, ws, rank, local):
 
         n_kernel = max(200, min(args.steps, 5000))
         ms_gemm = time_graphs(gemm_graphs, n_kernel, stream)
-        ms_cast = time_graphs(cast_graphs, n_kernel, stream)
+        ms_cast = time_graphs(cast_graphs, n_kernel, stream) if has_casts else 0.0
         e2e = wk.e2e(min(args.steps, 50), stream)
         torch.cuda.synchronize()
 
@@ -517,7 +613,8 @@ def run_ours(args, ws, rank, local):
     value = job_throughput(ws, wk.flops, ms_step)
 
     gemm_bytes = wk.gemm_bytes()
-    fp8_peak = peaks["bf16_tflops"] * 2.0  # nominal fp8 : bf16 dense ratio 4.5 : 2.25
+    # the contraction's own peak: FP8 = measured bf16 x 2 (nominal 4.5 : 2.25); BF16 = measured bf16
+    fp8_peak = wk.peak_tflops(peaks) if hasattr(wk, "peak_tflops") else peaks["bf16_tflops"] * 2.0
     t_hbm = gemm_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = wk.flops / (fp8_peak * 1e12)
     if t_hbm >= t_tc:
@@ -531,18 +628,20 @@ def run_ours(args, ws, rank, local):
     traffic = profiled_traffic(f"{args.workload}_gemm")
     roof.update({"traffic": traffic, "kernel": wk.kernel_name, "algorithmic_bytes": gemm_bytes,
                  "kernel_ms": round(ms_gemm, 5), "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json "
-                 f"hbm_gbs; fp8 peak = bf16 x 2)" if peaks["source"] == "measured" else "fallback",
+                 f"hbm_gbs; {'bf16 peak' if hasattr(wk, 'peak_tflops') else 'fp8 peak = bf16 x 2'})"
+                 if peaks["source"] == "measured" else "fallback",
                  "tensor_frac": round(wk.flops / (ms_gemm * 1e-3) / 1e12 / fp8_peak, 4),
                  "hbm_frac": round(gemm_bytes / (ms_gemm * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
 
-    line = {"metric": "grouped FP8 GEMM TFLOP/s on valid rows; % of GB300 FP8 tensor/HBM roofline",
+    line = {"metric": getattr(wk, "metric", "grouped FP8 GEMM TFLOP/s on valid rows; % of GB300 FP8 tensor/HBM roofline"),
             "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic (seeded randn, shapes of the source pages)",
+            "dtype": getattr(wk, "dtype", "e4m3 (fp32 accumulate)"),
+            "data": "synthetic (seeded randn, shapes of the source pages)",
             "config": wk.config() | {"parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "roofline": roof,
             "breakdown_ms": {"casts": round(ms_cast, 5), "gemm_kernel": round(ms_gemm, 5),
-                             "cast_gbs": round(wk.cast_bytes() / (ms_cast * 1e-3) / 1e9, 1)},
+                             "cast_gbs": round(wk.cast_bytes() / (ms_cast * 1e-3) / 1e9, 1) if ms_cast > 0 else None},
             "gpu_launches": wk.launches_per_step * args.steps,
             "clocks": clocks}
     if e2e is not None:
@@ -598,10 +697,11 @@ def run_reference(args, ws, rank, local):
     value = flops / dt / 1e12
     sample = (f"{n} of {wk.N} grad_y channels x all {wk.T} tokens x {wk.H} act channels per step"
               if n is not None else "4 routed rows x one 128-column block per step")
-    line = {"impl": "reference", "metric": "grouped FP8 GEMM TFLOP/s on valid rows; % of GB300 FP8 tensor/HBM roofline",
+    line = {"impl": "reference", "metric": getattr(wk, "metric", "grouped FP8 GEMM TFLOP/s on valid rows; % of GB300 FP8 tensor/HBM roofline"),
             "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / max(1, args.steps) * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64 (oracle accumulation of e4m3 codes)", "data": "synthetic",
+            "vs_baseline": None, "data": "synthetic",
+            "dtype": "f64 (oracle accumulation of " + ("bf16 values)" if hasattr(wk, "peak_tflops") else "e4m3 codes)"),
             "config": wk.config() | {"parallelism": "single process (rank 0)"},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
@@ -618,7 +718,8 @@ def main():
     ap.add_argument("--workload", default="kgrouped_wgrad",
                     help="kgrouped_wgrad | masked_decode | masked_repro | contiguous_prefill | "
                          "many_expert_{w13,w2}_E{1,32,113} | masked_decode_g8 | contiguous_prefill_g8 "
-                         "(the last two: 8-expert cases for profiler captures)")
+                         "(the last two: 8-expert cases for profiler captures) | "
+                         "{masked_repro,masked_decode,contiguous_prefill}_bf16 (BF16 grouped GEMM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

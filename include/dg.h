@@ -162,6 +162,33 @@ int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const uint8_t* b,
                             size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * m-grouped masked BF16 GEMM ([P2] m_grouped_bf16_gemm_nt_masked(a, b, d, masked_m, expected_m),
+ * the GEMM of the pages' reproduction, checked there against bmm(a.double(), b.double().mT)
+ * rounded to bf16):
+ *   D[g, r, n] = sum_k A[g, r, k] * B[g, n, k]   (fp32 accumulation)   for r < min(counts[g], cap)
+ * with the same per-expert output boundary as the FP8 masked GEMM: rows at or past the count
+ * are never written.
+ *   a: bf16 [G, cap, K].  b: bf16 [G, N, K].  d: [G, cap, N] bf16 or fp32 (out_dtype).
+ *   counts: int32 [G] device (clamped to [0, cap]; out-of-range counts set
+ *   DG_STATUS_COUNT_GT_CAP).  N % 128 == 0, K % 64 == 0; a, b, d 16-byte aligned.
+ *   expected_m: a hint only; it never changes the result.
+ */
+int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, int out_dtype, const int32_t* counts,
+                             int G, int64_t cap, int64_t N, int64_t K, int expected_m, int32_t* status,
+                             void* stream);
+
+/*
+ * m-grouped contiguous BF16 GEMM: the BF16 GEMM of [P2] on the contiguous layout of [P3]
+ * (rows routed by m_indices, -1 = padding, segments aligned to 128 rows):
+ *   D[m, n] = sum_k A[m, k] * B[m_indices[m], n, k]   for rows with m_indices[m] in [0, G).
+ *   a: bf16 [M, K].  b: bf16 [G, N, K].  d: [M, N] bf16 or fp32.  m_indices: int32 [M] device.
+ *   Row validity, the skipping of all-padding blocks and the status bits are those of
+ *   dg_m_grouped_fp8_contiguous.  N % 128 == 0, K % 64 == 0.
+ */
+int dg_m_grouped_bf16_contiguous(const void* a, const void* b, void* d, int out_dtype, const int32_t* m_indices,
+                                 int64_t M, int G, int64_t N, int64_t K, int32_t* status, void* stream);
+
+/*
  * k-grouped FP8 weight-gradient GEMM ([P1] k_grouped_fp8_gemm_nt_contiguous with
  * recipe (1, 1, 128)): for each expert e with token span [o_e, o_e + K_e) along K,
  *   D_e[n, h] = C_e[n, h] + sum_{t < K_e} A_e[n, t] sfa[(o_e+t)/128, n] * B_e[h, t] sfb[(o_e+t)/128, h]

@@ -162,6 +162,32 @@ def dg_m_grouped_fp8_masked(a, sfa, b, sfb, d, counts, expected_m=0, sf_format=D
                                          _s(stream)))
 
 
+def dg_m_grouped_bf16_masked(a, b, d, counts, expected_m=0, status=None, stream=None):
+    """a [G, cap, K] bf16, b [G, N, K] bf16, d [G, cap, N] bf16/fp32, counts int32 [G]."""
+    _dev(a, b, d, counts, status)
+    G, cap, K = a.shape
+    G2, N, K2 = b.shape
+    _need(G == G2 and K == K2 and tuple(d.shape) == (G, cap, N), "shapes")
+    _need(a.dtype == torch.bfloat16 and b.dtype == torch.bfloat16, "a and b must be bf16")
+    _need(a.is_contiguous() and b.is_contiguous() and d.is_contiguous(), "contiguity")
+    _need(counts.dtype == torch.int32 and counts.numel() == G, "counts must be int32 [G]")
+    check(load().dg_m_grouped_bf16_masked(_p(a), _p(b), _p(d), _out_code(d), _p(counts), G, cap, N, K,
+                                          int(expected_m), _p(status), _s(stream)))
+
+
+def dg_m_grouped_bf16_contiguous(a, b, d, m_indices, status=None, stream=None):
+    """a [M, K] bf16, b [G, N, K] bf16, d [M, N] bf16/fp32, m_indices int32 [M] (-1 = padding)."""
+    _dev(a, b, d, m_indices, status)
+    M, K = a.shape
+    G, N, K2 = b.shape
+    _need(K == K2 and tuple(d.shape) == (M, N), "shapes")
+    _need(a.dtype == torch.bfloat16 and b.dtype == torch.bfloat16, "a and b must be bf16")
+    _need(a.is_contiguous() and b.is_contiguous() and d.is_contiguous(), "contiguity")
+    _need(m_indices.dtype == torch.int32 and m_indices.numel() == M, "m_indices must be int32 [M]")
+    check(load().dg_m_grouped_bf16_contiguous(_p(a), _p(b), _p(d), _out_code(d), _p(m_indices), M, G, N, K,
+                                              _p(status), _s(stream)))
+
+
 def dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, workspace, status=None, stream=None):
     """D_e = C_e + A_e^T B_e.  a_packed/b_packed: per-expert K-major codes; sfa [K_cap/128][N],
     sfb [K_cap/128][H]; c (or None, may be d) and d fp32 [G, N, H]; ks int32 [G]."""

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdg.so")
-SOURCES = ["host_common.cu", "quant.cu", "gemm.cu", "gemm_pair.cu", "kgrouped.cu"]
+SOURCES = ["host_common.cu", "quant.cu", "gemm.cu", "gemm_pair.cu", "gemm_bf16.cu", "kgrouped.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}"]
 
