@@ -65,6 +65,17 @@ def multinomial_counts(T: int, G: int, seed: int) -> np.ndarray:
     return rng.multinomial(T, np.full(G, 1.0 / G)).astype(np.int32)
 
 
+def contiguous_psum(counts, align: int = BLOCK) -> np.ndarray:
+    """The expert segments of contiguous_m_indices as per-expert end rows: expert e's rows start
+    at the previous end rounded up to `align` and end at start + counts[e]."""
+    psum = np.empty(len(counts), np.int32)
+    start = 0
+    for e, c in enumerate(np.asarray(counts, np.int64)):
+        psum[e] = start + c
+        start += (int(c) + align - 1) // align * align
+    return psum
+
+
 def contiguous_m_indices(counts, m_max: int | None = None, align: int = BLOCK) -> np.ndarray:
     """Stack expert segments in expert order, each padded to a multiple of `align` rows with
     -1; the buffer is m_max rows (default: the padded total), tail rows -1."""

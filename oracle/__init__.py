@@ -63,6 +63,8 @@ def _load():
             lib.oracle_gemm_masked.argtypes = [P, P, P, P, P, i32, i64, i64, i64, P]
             lib.oracle_gemm_kgrouped.argtypes = [P, P, P, P, P, P, i32, i64, i64, i64, P]
             lib.oracle_gemm_masked_bf16.argtypes = [P, P, P, i32, i64, i64, i64, P]
+            lib.oracle_sizes_from_psum.argtypes = [P, i32, P]
+            lib.oracle_m_indices_from_psum.argtypes = [P, i32, i64, P]
             lib.oracle_gemm_contiguous_bf16.argtypes = [P, P, P, i64, i32, i64, i64, P]
             lib.oracle_round_bf16.restype = ctypes.c_uint16
             lib.oracle_round_bf16.argtypes = [ctypes.c_double]
@@ -236,6 +238,22 @@ def gemm_contiguous_bf16(a, b, m_indices) -> np.ndarray:
     d = np.full((M, N), np.nan, np.float64)
     _load().oracle_gemm_contiguous_bf16(_p(a), _p(b), _p(mi), M, G, N, K, _p(d))
     return d
+
+
+def sizes_from_psum(psum) -> np.ndarray:
+    """K_e from inclusive prefix sums (k-grouped psum layout)."""
+    ps = _c(psum, np.int32)
+    ks = np.empty_like(ps)
+    _load().oracle_sizes_from_psum(_p(ps), ps.size, _p(ks))
+    return ks
+
+
+def m_indices_from_psum(psum, M) -> np.ndarray:
+    """Per-row expert of the contiguous psum layout (-1 = unrouted)."""
+    ps = _c(psum, np.int32)
+    mi = np.empty(M, np.int32)
+    _load().oracle_m_indices_from_psum(_p(ps), ps.size, M, _p(mi))
+    return mi
 
 
 def gemm_kgrouped(a_packed, sfa, b_packed, sfb, ks, N, H, K_cap=None, c=None) -> np.ndarray:

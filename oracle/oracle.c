@@ -412,6 +412,31 @@ void oracle_gemm_contiguous_bf16(const uint16_t* a, const uint16_t* b, const int
     }
 }
 
+/* ----------------------------------------------------------------------------------------
+ * Prefix-sum ("psum") grouped layouts: `use_psum_layout` of the k-grouped call in #365's
+ * repro listing, and the m_indices / psum / masked modes of #444's graph-mutation test.
+ * Readings (the pages name the option but not its encoding):
+ *  - k-grouped: psum[e] = K_0 + ... + K_e, so K_e = psum[e] - psum[e-1] (psum[-1] = 0); a
+ *    decreasing entry gives a negative K_e, which stops the walk of oracle_gemm_kgrouped;
+ *  - m-grouped contiguous: psum[e] is the exclusive end row of expert e, whose rows start at
+ *    the previous end rounded up to 128 (the 128-aligned segments of the m_indices layout).
+ *    An entry below its predecessor, past M, or ending inside the rounding gap stops the walk:
+ *    that expert and every later one stay unrouted (-1).
+ * --------------------------------------------------------------------------------------*/
+void oracle_sizes_from_psum(const int32_t* psum, int G, int32_t* ks) {
+    for (int e = 0; e < G; ++e) ks[e] = psum[e] - (e > 0 ? psum[e - 1] : 0);
+}
+
+void oracle_m_indices_from_psum(const int32_t* psum, int G, int64_t M, int32_t* m_indices) {
+    for (int64_t m = 0; m < M; ++m) m_indices[m] = -1;
+    for (int e = 0; e < G; ++e) {
+        int64_t prev = e > 0 ? psum[e - 1] : 0, end = psum[e];
+        int64_t start = (prev + 127) / 128 * 128;
+        if (prev < 0 || end < prev || end > M || (end > prev && end < start)) break;
+        for (int64_t m = start; m < end; ++m) m_indices[m] = e;
+    }
+}
+
 /* fp64 -> bf16 bits, a single round-to-nearest-even (no intermediate fp32 rounding).
  * bf16: 8 exponent bits (bias 127), 7 mantissa bits; min normal 2^-126, subnormal step
  * 2^-133; overflow past the largest finite value plus half an ulp gives inf. */

@@ -551,3 +551,29 @@ def test_bf16_contiguous_routing():
             np.testing.assert_allclose(d[m], bn[mi[m]] @ an[m], rtol=1e-12, atol=1e-12)
         else:
             assert np.all(np.isnan(d[m]))
+
+
+# ---------------------------------------------------------------------------- psum layouts
+
+def test_sizes_from_psum_inverts_cumsum():
+    ks = np.array([256, 0, 128, 384, 0, 128], np.int32)
+    np.testing.assert_array_equal(oracle.sizes_from_psum(np.cumsum(ks).astype(np.int32)), ks)
+
+
+@pytest.mark.parametrize("counts", [[130, 0, 1, 128, 257], [0, 0, 5], [128, 256, 1], [300]])
+def test_m_indices_from_psum_matches_the_padded_layout(counts):
+    """The psum reading reproduces, row for row, the 128-aligned segments of the m_indices layout."""
+    M = wl.contiguous_capacity(sum(counts), len(counts))
+    np.testing.assert_array_equal(oracle.m_indices_from_psum(wl.contiguous_psum(counts), M),
+                                  wl.contiguous_m_indices(counts, m_max=M))
+
+
+def test_m_indices_from_psum_stops_at_the_first_bad_entry():
+    M = 1024
+    base = wl.contiguous_psum([130, 50, 10])           # [130, 306, 394]
+    for bad, e in ([130, 100, 394], 1), ([130, 306, 2000], 2), ([130, 200, 394], 1):
+        mi = oracle.m_indices_from_psum(np.array(bad, np.int32), M)
+        good = oracle.m_indices_from_psum(base, M)
+        first_row_of_e = {1: 256, 2: 384}[e]
+        np.testing.assert_array_equal(mi[:first_row_of_e], good[:first_row_of_e])
+        assert np.all(mi[first_row_of_e:] == -1)
