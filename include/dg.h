@@ -146,6 +146,22 @@ int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, const uint8_t
                                 void* stream);
 
 /*
+ * dg_m_grouped_fp8_contiguous with the grouped layout given as prefix sums ([P1] and [P3]:
+ * the `use_psum_layout` option of the grouped GEMMs, and the graph-mutation test "across
+ * m_indices/psum/masked modes").  Reading taken: psum[e] is the exclusive end row of expert
+ * e's rows, which start at the previous expert's end rounded up to a multiple of 128
+ * (psum[-1] = 0) - the 128-aligned segments of the m_indices layout, described by G integers.
+ *   psum: int32 [G] device, non-decreasing, psum[G-1] <= M.  An entry below its predecessor,
+ *   past M, or ending inside the rounding gap sets DG_STATUS_BAD_INDEX; that expert and every
+ *   later one are skipped.  Everything else is as dg_m_grouped_fp8_contiguous; the result is
+ *   bitwise that of the equivalent m_indices call.
+ */
+int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d,
+                                     int out_dtype, const int32_t* psum, int64_t M, int G, int64_t N, int64_t K,
+                                     int sf_format, void* workspace, size_t workspace_bytes, int32_t* status,
+                                     void* stream);
+
+/*
  * m-grouped masked FP8 GEMM ([P2] m_grouped_*_gemm_nt_masked(a, b, d, masked_m, expected_m)):
  *   D[g, r, n] = sum_k A[g, r, k] sfa[k/128, g*cap + r] * B[g, n, k] sfb[g, n/128, k/128]
  * for r < min(counts[g], cap).  Rows at or past the count are never written: the output is
@@ -206,6 +222,23 @@ int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa, const uint
                            const float* sfb, const float* c, float* d, const int32_t* ks, int G,
                            int64_t K_cap, int64_t N, int64_t H, void* workspace,
                            size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * dg_k_grouped_fp8_wgrad, dg_quant_per_channel_128 and dg_quant_per_channel_128_pair with the
+ * expert spans given as inclusive prefix sums ([P1] k_grouped_fp8_gemm_nt_contiguous(...,
+ * use_psum_layout=True)): psum[e] = K_0 + ... + K_e, so K_e = psum[e] - psum[e-1] (psum[-1] = 0).
+ * A decreasing entry gives a negative K_e and stops the walk like any bad K_e.  Results are
+ * bitwise those of the equivalent ks calls.
+ */
+int dg_k_grouped_fp8_wgrad_psum(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
+                                const float* sfb, const float* c, float* d, const int32_t* psum, int G,
+                                int64_t K_cap, int64_t N, int64_t H, void* workspace, size_t workspace_bytes,
+                                int32_t* status, void* stream);
+int dg_quant_per_channel_128_psum(const void* x, int64_t K_cap, int64_t C, const int32_t* psum, int G,
+                                  uint8_t* q_packed, float* sf, float sf_zero, int32_t* status, void* stream);
+int dg_quant_per_channel_128_pair_psum(const void* x_a, int64_t C_a, uint8_t* q_a, float* sf_a, const void* x_b,
+                                       int64_t C_b, uint8_t* q_b, float* sf_b, int64_t K_cap, const int32_t* psum,
+                                       int G, float sf_zero, int32_t* status, void* stream);
 
 /* Largest G accepted by dg_k_grouped_fp8_wgrad_noalloc. */
 #define DG_NOALLOC_MAX_GROUPS 256

@@ -33,6 +33,10 @@ SIGNATURES = {
     "dg_quant_block_128x128": (I32, [P, I32, I64, I64, P, P, I32, F32, P]),
     "dg_m_grouped_fp8_contiguous": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, I32, P, SZ, P, P]),
     "dg_m_grouped_fp8_masked": (I32, [P, P, P, P, P, I32, P, I32, I64, I64, I64, I32, I32, P, SZ, P, P]),
+    "dg_m_grouped_fp8_contiguous_psum": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, I32, P, SZ, P, P]),
+    "dg_k_grouped_fp8_wgrad_psum": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
+    "dg_quant_per_channel_128_psum": (I32, [P, I64, I64, P, I32, P, P, F32, P, P]),
+    "dg_quant_per_channel_128_pair_psum": (I32, [P, I64, P, P, P, I64, P, P, I64, P, I32, F32, P, P]),
     "dg_m_grouped_bf16_masked": (I32, [P, P, P, I32, P, I32, I64, I64, I64, I32, P, P]),
     "dg_m_grouped_bf16_contiguous": (I32, [P, P, P, I32, P, I64, I32, I64, I64, P, P]),
     "dg_k_grouped_fp8_wgrad": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),

@@ -83,7 +83,7 @@ def dg_quant_per_token_1x128(x, q, sfa, sf_format=DG_SF_FP32, sf_zero=1e-30, row
                                           _p(row_counts), G, _s(stream)))
 
 
-def dg_quant_per_channel_128(x, ks, q_packed, sf, sf_zero=1e-30, status=None, stream=None):
+def dg_quant_per_channel_128(x, ks, q_packed, sf, sf_zero=1e-30, status=None, stream=None, _fn="dg_quant_per_channel_128"):
     """x bf16 [K_cap, C] token-major -> q_packed [K_cap*C] per-expert K-major, sf fp32 [K_cap/128][C]."""
     _dev(x, ks, q_packed, sf, status)
     _need(x.dim() == 2 and x.dtype == torch.bfloat16 and x.is_contiguous(), "x must be contiguous bf16 [K_cap, C]")
@@ -91,11 +91,17 @@ def dg_quant_per_channel_128(x, ks, q_packed, sf, sf_zero=1e-30, status=None, st
     _need(ks.dtype == torch.int32 and ks.is_contiguous(), "ks must be int32")
     _need(q_packed.is_contiguous() and q_packed.numel() >= K_cap * C and q_packed.element_size() == 1, "q_packed size")
     _need(sf.is_contiguous() and sf.dtype == torch.float32 and sf.numel() >= (K_cap // 128) * C, "sf size")
-    check(load().dg_quant_per_channel_128(_p(x), K_cap, C, _p(ks), ks.numel(), _p(q_packed), _p(sf), sf_zero,
-                                          _p(status), _s(stream)))
+    check(getattr(load(), _fn)(_p(x), K_cap, C, _p(ks), ks.numel(), _p(q_packed), _p(sf), sf_zero, _p(status),
+                               _s(stream)))
 
 
-def dg_quant_per_channel_128_pair(x_a, x_b, ks, q_a, sf_a, q_b, sf_b, sf_zero=1e-30, status=None, stream=None):
+def dg_quant_per_channel_128_psum(x, psum, q_packed, sf, sf_zero=1e-30, status=None, stream=None):
+    """dg_quant_per_channel_128 with expert spans as inclusive prefix sums psum int32 [G]."""
+    dg_quant_per_channel_128(x, psum, q_packed, sf, sf_zero, status, stream, _fn="dg_quant_per_channel_128_psum")
+
+
+def dg_quant_per_channel_128_pair(x_a, x_b, ks, q_a, sf_a, q_b, sf_b, sf_zero=1e-30, status=None, stream=None,
+                                  _fn="dg_quant_per_channel_128_pair"):
     """Both wgrad operands in one launch: same results as two dg_quant_per_channel_128 calls."""
     _dev(x_a, x_b, ks, q_a, sf_a, q_b, sf_b, status)
     for x, q, sf in ((x_a, q_a, sf_a), (x_b, q_b, sf_b)):
@@ -104,9 +110,14 @@ def dg_quant_per_channel_128_pair(x_a, x_b, ks, q_a, sf_a, q_b, sf_b, sf_zero=1e
         _need(sf.is_contiguous() and sf.dtype == torch.float32 and sf.numel() >= x.numel() // 128, "sf size")
     _need(x_a.shape[0] == x_b.shape[0], "both operands need the same K_cap")
     _need(ks.dtype == torch.int32 and ks.is_contiguous(), "ks must be int32")
-    check(load().dg_quant_per_channel_128_pair(_p(x_a), x_a.shape[1], _p(q_a), _p(sf_a), _p(x_b), x_b.shape[1], _p(q_b),
-                                               _p(sf_b), x_a.shape[0], _p(ks), ks.numel(), sf_zero, _p(status),
-                                               _s(stream)))
+    check(getattr(load(), _fn)(_p(x_a), x_a.shape[1], _p(q_a), _p(sf_a), _p(x_b), x_b.shape[1], _p(q_b), _p(sf_b),
+                               x_a.shape[0], _p(ks), ks.numel(), sf_zero, _p(status), _s(stream)))
+
+
+def dg_quant_per_channel_128_pair_psum(x_a, x_b, psum, q_a, sf_a, q_b, sf_b, sf_zero=1e-30, status=None, stream=None):
+    """dg_quant_per_channel_128_pair with expert spans as inclusive prefix sums psum int32 [G]."""
+    dg_quant_per_channel_128_pair(x_a, x_b, psum, q_a, sf_a, q_b, sf_b, sf_zero, status, stream,
+                                  _fn="dg_quant_per_channel_128_pair_psum")
 
 
 def dg_quant_block_128x128(w, q, sfb, sf_format=DG_SF_FP32, sf_zero=1e-30, stream=None):
@@ -128,20 +139,31 @@ def _out_code(d):
 
 
 def dg_m_grouped_fp8_contiguous(a, sfa, b, sfb, d, m_indices, sf_format=DG_SF_FP32, status=None, workspace=None,
-                                stream=None):
+                                stream=None, _psum=False):
     """a [M, K] e4m3, b [G, N, K] e4m3, d [M, N] bf16/fp32, m_indices int32 [M]."""
     _dev(a, sfa, b, sfb, d, m_indices, status)
     M, K = a.shape
     G, N, K2 = b.shape
     _need(K == K2 and tuple(d.shape) == (M, N) and d.is_contiguous() and a.is_contiguous() and b.is_contiguous(),
           "shapes")
-    _need(m_indices.dtype == torch.int32 and m_indices.numel() == M, "m_indices must be int32 [M]")
+    if _psum:
+        _need(m_indices.dtype == torch.int32 and m_indices.numel() == G, "psum must be int32 [G]")
+    else:
+        _need(m_indices.dtype == torch.int32 and m_indices.numel() == M, "m_indices must be int32 [M]")
     _need(sfa.dtype == _sf_dtype(sf_format) and sfb.dtype == _sf_dtype(sf_format), "scale dtype")
     _need(sfa.numel() >= (K // 128) * sfa_padded_rows(M, sf_format), "sfa size")
     _need(sfb.numel() >= G * (N // 128) * (K // 128), "sfb size")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    check(load().dg_m_grouped_fp8_contiguous(_p(a), _p(sfa), _p(b), _p(sfb), _p(d), _out_code(d), _p(m_indices), M, G,
-                                             N, K, sf_format, _p(workspace), ws_bytes, _p(status), _s(stream)))
+    fn = load().dg_m_grouped_fp8_contiguous_psum if _psum else load().dg_m_grouped_fp8_contiguous
+    check(fn(_p(a), _p(sfa), _p(b), _p(sfb), _p(d), _out_code(d), _p(m_indices), M, G, N, K, sf_format, _p(workspace),
+             ws_bytes, _p(status), _s(stream)))
+
+
+def dg_m_grouped_fp8_contiguous_psum(a, sfa, b, sfb, d, psum, sf_format=DG_SF_FP32, status=None, workspace=None,
+                                     stream=None):
+    """dg_m_grouped_fp8_contiguous routed by psum int32 [G]: expert e owns rows
+    [round_up(psum[e-1], 128), psum[e])."""
+    dg_m_grouped_fp8_contiguous(a, sfa, b, sfb, d, psum, sf_format, status, workspace, stream, _psum=True)
 
 
 def dg_m_grouped_fp8_masked(a, sfa, b, sfb, d, counts, expected_m=0, sf_format=DG_SF_FP32, status=None,
@@ -188,7 +210,8 @@ def dg_m_grouped_bf16_contiguous(a, b, d, m_indices, status=None, stream=None):
                                               _p(status), _s(stream)))
 
 
-def dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, workspace, status=None, stream=None):
+def dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, workspace, status=None, stream=None,
+                           _fn="dg_k_grouped_fp8_wgrad"):
     """D_e = C_e + A_e^T B_e.  a_packed/b_packed: per-expert K-major codes; sfa [K_cap/128][N],
     sfb [K_cap/128][H]; c (or None, may be d) and d fp32 [G, N, H]; ks int32 [G]."""
     _dev(a_packed, sfa, b_packed, sfb, c, d, ks, workspace, status)
@@ -200,8 +223,14 @@ def dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, worksp
     _need(sfb.dtype == torch.float32 and sfb.numel() >= (K_cap // 128) * H, "sfb")
     _need(a_packed.numel() >= K_cap * N and b_packed.numel() >= K_cap * H, "packed operand size")
     ws_bytes = workspace.numel() * workspace.element_size()
-    check(load().dg_k_grouped_fp8_wgrad(_p(a_packed), _p(sfa), _p(b_packed), _p(sfb), _p(c), _p(d), _p(ks), G, K_cap,
-                                        N, H, _p(workspace), ws_bytes, _p(status), _s(stream)))
+    check(getattr(load(), _fn)(_p(a_packed), _p(sfa), _p(b_packed), _p(sfb), _p(c), _p(d), _p(ks), G, K_cap, N, H,
+                               _p(workspace), ws_bytes, _p(status), _s(stream)))
+
+
+def dg_k_grouped_fp8_wgrad_psum(a_packed, sfa, b_packed, sfb, c, d, psum, K_cap, workspace, status=None, stream=None):
+    """dg_k_grouped_fp8_wgrad with expert spans as inclusive prefix sums psum int32 [G]."""
+    dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, psum, K_cap, workspace, status, stream,
+                           _fn="dg_k_grouped_fp8_wgrad_psum")
 
 
 def dg_k_grouped_fp8_wgrad_noalloc(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, status=None, stream=None):

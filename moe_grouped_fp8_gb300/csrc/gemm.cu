@@ -96,6 +96,10 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const RunTable& rt, int R
     ti.kbt = a.KB;
     if constexpr (L == Layout::Contiguous) {
         ti.row0 = (rt.first[r] + j) * BM;
+        if (a.psum) {
+            const int v = rt.x[r] - ti.row0;
+            ti.valid = v < BM ? v : BM;
+        }
     } else {
         ti.row0 = j * BM;
         const int v = rt.x[r] - ti.row0;
@@ -255,6 +259,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (L == Layout::Masked) {
                 row_ok = row < ti.valid;
                 grow = static_cast<int64_t>(ti.e) * a.M + ti.row0 + row;
+            } else if (a.psum) {
+                grow = static_cast<int64_t>(ti.row0) + row;
+                row_ok = row < ti.valid;
             } else {
                 grow = static_cast<int64_t>(ti.row0) + row;
                 const int mi = grow < a.M ? a.routing[grow] : -1;
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
             // ---- store: TMA for the leading 8-row-aligned valid rows, owner threads for the rest
             int v = BM;
-            if constexpr (L == Layout::Masked) {
+            if (L == Layout::Masked || a.psum) {
                 v = ti.valid;
             } else {
                 v = 0;
@@ -560,15 +567,16 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
                                              static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
-                                           void* d, int out_dtype, const int32_t* m_indices, int64_t M, int G,
-                                           int64_t N, int64_t K, int sf_format, void* workspace,
-                                           size_t workspace_bytes, int32_t* status, void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
+namespace dg {
+namespace {
+
+// The contiguous layout, routed by m_indices [M] or (psum) by per-expert end rows [G].
+int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d,
+                         int out_dtype, const int32_t* routing, bool psum, int64_t M, int G, int64_t N, int64_t K,
+                         int sf_format, int32_t* status, void* stream) {
     DG_CHECK_ARG(M >= 0, "M must be >= 0");
     if (int rc = check_common_mg(a, sfa, b, sfb, d, out_dtype, G, N, K, sf_format)) return rc;
-    DG_CHECK_ARG(m_indices != nullptr, "m_indices is null");
+    DG_CHECK_ARG(routing != nullptr, psum ? "psum is null" : "m_indices is null");
     if (M == 0) return DG_OK;
     DG_CHECK_SUPPORTED((M + BM - 1) / BM <= DG_MAX_M_BLOCKS, "M too large (at most %d rows)", DG_MAX_M_BLOCKS * BM);
     const int esize = out_dtype == DG_OUT_FP32 ? 4 : 2;
@@ -603,7 +611,8 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
             return rc;
     }
     GemmArgs args{};
-    args.routing = m_indices;
+    args.routing = routing;
+    args.psum = psum ? 1 : 0;
     args.sfa = sfa;
     args.sfb = sfb;
     args.d = d;
@@ -619,6 +628,29 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
     args.N = N;
     return dispatch_mgrouped<Layout::Contiguous>(pair, out_dtype, sf_format, tA, tB, tD, tD8, args,
                                                  static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
+                                           void* d, int out_dtype, const int32_t* m_indices, int64_t M, int G,
+                                           int64_t N, int64_t K, int sf_format, void* workspace,
+                                           size_t workspace_bytes, int32_t* status, void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return m_grouped_contiguous(a, sfa, b, sfb, d, out_dtype, m_indices, false, M, G, N, K, sf_format, status,
+                                stream);
+}
+
+extern "C" int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sfa, const uint8_t* b,
+                                                const void* sfb, void* d, int out_dtype, const int32_t* psum,
+                                                int64_t M, int G, int64_t N, int64_t K, int sf_format,
+                                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                                void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return m_grouped_contiguous(a, sfa, b, sfb, d, out_dtype, psum, true, M, G, N, K, sf_format, status, stream);
 }
 
 // ------------------------------------------------------------------------- test hook

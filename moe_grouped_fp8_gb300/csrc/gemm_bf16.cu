@@ -67,7 +67,7 @@ struct HTile {
 };
 
 template <Layout L>
-__device__ __forceinline__ HTile decode_h(int t, const RunTable& rt, int R) {
+__device__ __forceinline__ HTile decode_h(int t, const RunTable& rt, int R, const GemmArgs& a) {
     const int r = find_run(rt.prefix, R, t);
     const int local = t - rt.prefix[r];
     const int Lr = rt.L[r];
@@ -78,6 +78,10 @@ __device__ __forceinline__ HTile decode_h(int t, const RunTable& rt, int R) {
     ti.valid = 0;
     if constexpr (L == Layout::Contiguous) {
         ti.row0 = (rt.first[r] + j) * BM;
+        if (a.psum) {
+            const int v = rt.x[r] - ti.row0;
+            ti.valid = v < BM ? v : BM;
+        }
     } else {
         ti.row0 = j * BM;
         const int v = rt.x[r] - ti.row0;
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const HTile ti = decode_h<L>(t, rt, R);
+                const HTile ti = decode_h<L>(t, rt, R, a);
                 for (int kb = 0; kb < a.KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     uint8_t* sa = ring + stage * P::STAGE_BYTES;
@@ -223,12 +227,15 @@ __global__ void __launch_bounds__(H_THREADS, 1)
         bool have_store = false;
         int parity_slot = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            const HTile ti = decode_h<L>(t, rt, R);
+            const HTile ti = decode_h<L>(t, rt, R, a);
             bool row_ok = false;
             int64_t grow = 0;
             if constexpr (L == Layout::Masked) {
                 row_ok = row < ti.valid;
                 grow = static_cast<int64_t>(ti.e) * a.M + ti.row0 + row;
+            } else if (a.psum) {
+                grow = static_cast<int64_t>(ti.row0) + row;
+                row_ok = row < ti.valid;
             } else {
                 grow = static_cast<int64_t>(ti.row0) + row;
                 const int mi = grow < a.M ? a.routing[grow] : -1;
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
 
             // ---- store: TMA for the leading 8-row-aligned valid rows, owner threads for the rest
             int v = BM;
-            if constexpr (L == Layout::Masked) {
+            if (L == Layout::Masked || a.psum) {
                 v = ti.valid;
             } else {
                 v = 0;

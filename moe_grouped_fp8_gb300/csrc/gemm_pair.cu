@@ -90,7 +90,7 @@ struct PairTile {
 
 // Tiles of a run: ceil(L / 2) m-pairs (fastest) x num_nb column tiles.
 template <Layout L>
-__device__ __forceinline__ PairTile decode_pair(int t, const RunTable& rt, int R, uint32_t rank) {
+__device__ __forceinline__ PairTile decode_pair(int t, const RunTable& rt, int R, uint32_t rank, const GemmArgs& a) {
     const int r = find_run(rt.prefix, R, t);
     const int local = t - rt.prefix[r];
     const int Lr = rt.L[r];
@@ -104,6 +104,10 @@ __device__ __forceinline__ PairTile decode_pair(int t, const RunTable& rt, int R
     ti.valid = 0;
     if constexpr (L == Layout::Contiguous) {
         ti.row0 = (rt.first[r] + blk) * BM;
+        if (a.psum) {
+            const int v = rt.x[r] - ti.row0;
+            ti.valid = (!ti.blk_ok || v < 0) ? 0 : (v < BM ? v : BM);
+        }
     } else {
         ti.row0 = blk * BM;
         const int v = rt.x[r] - ti.row0;
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             int issued = 0;
             bool ok = true;
             for (int t = cid; t < num_tiles && ok; t += ncl) {
-                const PairTile ti = decode_pair<L>(t, rt, R, rank);
+                const PairTile ti = decode_pair<L>(t, rt, R, rank, a);
                 const int brow = ti.nb * P_BN + static_cast<int>(rank) * P_BHALF;
                 for (int kb = 0; kb < a.KB; ++kb) {
                     if (!mbar_wait_cl(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
@@ -269,13 +273,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         bool have_store = false;
         int parity_slot = 0;
         for (int t = cid; t < num_tiles; t += ncl) {
-            const PairTile ti = decode_pair<L>(t, rt, R, rank);
+            const PairTile ti = decode_pair<L>(t, rt, R, rank, a);
             bool failed = false;
             bool row_ok = false;
             int64_t grow = 0;
             if constexpr (L == Layout::Masked) {
                 row_ok = row < ti.valid;
                 grow = static_cast<int64_t>(ti.e) * a.M + ti.row0 + row;
+            } else if (a.psum) {
+                grow = static_cast<int64_t>(ti.row0) + row;
+                row_ok = row < ti.valid;
             } else {
                 grow = static_cast<int64_t>(ti.row0) + row;
                 const int mi = (ti.blk_ok && grow < a.M) ? a.routing[grow] : -1;
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
             // ---- store: TMA for the leading 8-row-aligned valid rows, owner threads for the rest
             int v = 0;
-            if constexpr (L == Layout::Masked) {
+            if (L == Layout::Masked || a.psum) {
                 v = ti.valid;
             } else {
                 for (int qq = 0; qq < 4; ++qq) {

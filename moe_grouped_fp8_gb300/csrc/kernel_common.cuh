@@ -12,6 +12,12 @@ __device__ __forceinline__ float ue8m0_to_float(uint8_t b) {
     return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(b) << 23);
 }
 
+// K_e of expert e from per-expert sizes ks, or (psum != 0) from inclusive prefix sums
+// (K_e = psum[e] - psum[e-1], psum[-1] = 0); a negative difference reads as a bad K_e.
+__device__ __forceinline__ long long expert_k(const int32_t* ks, int e, int psum) {
+    return psum ? static_cast<long long>(ks[e]) - (e > 0 ? ks[e - 1] : 0) : static_cast<long long>(ks[e]);
+}
+
 // Exclusive prefix sum of one int per thread over a CTA of NT threads (all must call).
 template <int NT>
 __device__ int cta_excl_scan(int v, int* scratch, int* total) {

@@ -83,6 +83,7 @@ struct Args {
     int N;
     int H;
     int c_mode;  // 0: no C, 1: separate C, 2: C aliases D
+    int psum;    // ks holds inclusive prefix sums of K_e
 };
 
 struct Tile {
@@ -178,23 +179,23 @@ __global__ void __launch_bounds__(NT, 1) k_kgrouped_gemm(const __grid_constant__
         const int lo = tid * ch, hi = min(a.G, lo + ch);
         int sum = 0;
         for (int e = lo; e < hi; ++e) {
-            const int k = a.ks[e];
-            if (k >= 0 && (k % BK) == 0) sum += k;
+            const long long k = expert_k(a.ks, e, a.psum);
+            if (k >= 0 && (k % BK) == 0) sum += static_cast<int>(k);
         }
         int total = 0;
         int o = cta_excl_scan<NT>(sum, s_scan, &total);
         for (int e = lo; e < hi; ++e) {
-            const int k = a.ks[e];
+            const long long k = expert_k(a.ks, e, a.psum);
             int bits = 0;
             if (k < 0 || (k % BK) != 0) bits = DG_STATUS_K_NOT_ALIGNED;
             else if (static_cast<int64_t>(o) + k > a.K_cap) bits = DG_STATUS_K_OVERFLOW;
             s_off[e] = o;
-            s_k[e] = bits ? 0 : k;
+            s_k[e] = bits ? 0 : static_cast<int>(k);
             if (bits) {
                 atomicMin(s_first_bad, e);
                 if (blockIdx.x == 0) status_or(a.status, bits);
             }
-            if (k >= 0 && (k % BK) == 0) o += k;
+            if (k >= 0 && (k % BK) == 0) o += static_cast<int>(k);
         }
         __syncthreads();
         const int first_bad = *s_first_bad;
@@ -440,8 +441,8 @@ struct Templates {
 
 __global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant__ Templates tmpl,
                                                            const uint8_t* a_packed, const uint8_t* b_packed,
-                                                           const int32_t* ks, int G, int64_t K_cap, int64_t N,
-                                                           int64_t H, CUtensorMap* ws) {
+                                                           const int32_t* ks, int psum, int G, int64_t K_cap,
+                                                           int64_t N, int64_t H, CUtensorMap* ws) {
     __shared__ __align__(128) CUtensorMap s_maps[8][2];
     __shared__ long long s_warp[8];
     __shared__ long long s_carry;
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant
     __syncthreads();
     for (int base = 0; base < G; base += blockDim.x) {
         const int e = base + t;
-        const long long k = (e < G) ? ks[e] : 0;
+        const long long k = (e < G) ? expert_k(ks, e, psum) : 0;
         bool bad = (e < G) && (k < 0 || (k % BK) != 0);
         const long long kk = bad ? 0 : k;
         long long incl = kk;
@@ -576,7 +577,7 @@ int check_args(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packe
 // i.e. the workspace already holds this call's descriptors) and the GEMM.
 int launch(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, const float* sfb, const float* c,
            float* d, const int32_t* ks, int G, int64_t K_cap, int64_t N, int64_t H, void* workspace,
-           size_t workspace_bytes, int32_t* status, cudaStream_t s, bool prologue) {
+           size_t workspace_bytes, int32_t* status, cudaStream_t s, bool prologue, int psum = 0) {
     if (int rc = check_args(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes))
         return rc;
     auto* ws = static_cast<CUtensorMap*>(workspace);
@@ -594,8 +595,8 @@ int launch(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, c
     if (prologue) {
         Templates tmpl;
         if (int rc = make_templates(a_packed, b_packed, N, H, &tmpl)) return rc;
-        if (int rc = launch_pdl(k_kgrouped_prologue, dim3(1), dim3(256), 0, s, tmpl, a_packed, b_packed, ks, G, K_cap,
-                                N, H, ws))
+        if (int rc = launch_pdl(k_kgrouped_prologue, dim3(1), dim3(256), 0, s, tmpl, a_packed, b_packed, ks, psum, G,
+                                K_cap, N, H, ws))
             return rc;
     }
     Args args{};
@@ -610,6 +611,7 @@ int launch(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, c
     args.N = static_cast<int>(N);
     args.H = static_cast<int>(H);
     args.c_mode = c == nullptr ? 0 : (c == d ? 2 : 1);
+    args.psum = psum;
     int sms = 0;
     if (int rc = device_sm_count(&sms)) return rc;
     // One promotion group measured faster than two on GB300 (32.9 us vs 34.6 us, wgrad repro).
@@ -628,6 +630,14 @@ extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa,
                                       int32_t* status, void* stream) {
     return kg::launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes, status,
                       static_cast<cudaStream_t>(stream), true);
+}
+
+extern "C" int dg_k_grouped_fp8_wgrad_psum(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
+                                           const float* sfb, const float* c, float* d, const int32_t* psum, int G,
+                                           int64_t K_cap, int64_t N, int64_t H, void* workspace,
+                                           size_t workspace_bytes, int32_t* status, void* stream) {
+    return kg::launch(a_packed, sfa, b_packed, sfb, c, d, psum, G, K_cap, N, H, workspace, workspace_bytes, status,
+                      static_cast<cudaStream_t>(stream), true, 1);
 }
 
 // ------------------------------------------------------------------------- allocation-free variant
@@ -693,7 +703,7 @@ extern "C" int dg_testing_kgrouped_prologue(const uint8_t* a_packed, const uint8
     kg::Templates tmpl;
     if (int rc = kg::make_templates(a_packed, b_packed, N, H, &tmpl)) return rc;
     return launch_pdl(kg::k_kgrouped_prologue, dim3(1), dim3(256), 0, static_cast<cudaStream_t>(stream), tmpl, a_packed,
-                      b_packed, ks, G, K_cap, N, H, static_cast<CUtensorMap*>(workspace));
+                      b_packed, ks, 0, G, K_cap, N, H, static_cast<CUtensorMap*>(workspace));
 }
 
 extern "C" int dg_testing_kgrouped_gemm_only(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,

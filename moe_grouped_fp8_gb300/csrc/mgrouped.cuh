@@ -21,7 +21,7 @@ constexpr int BK = 128;        // K per pipeline stage = scale-block size
 constexpr int MAX_RUNS = 1024;  // runs of consecutive same-expert m-blocks kept in shared memory
 
 struct GemmArgs {
-    const int32_t* routing;      // m_indices [M] | counts [G]
+    const int32_t* routing;      // m_indices [M] | psum [G] (psum != 0) | counts [G]
     const void* sfa;             // see the layout notes of each entry point
     const void* sfb;
     void* d;                     // output base (owner-thread stores of tail rows)
@@ -36,6 +36,7 @@ struct GemmArgs {
     int KB;          // m-grouped K / 128
     int num_nb;      // output column tiles of the launched kernel
     int n128;        // N / 128 (sfb row count)
+    int psum;        // Contiguous: routing holds per-expert end rows (prefix sums), not m_indices
 };
 
 // Shared-memory bytes of the run table used by build_runs / tile_prefix.
@@ -61,7 +62,11 @@ struct RunTable {
 // Builds the runs of the launch from the routing tensor; every thread of the CTA calls it and
 // gets the run count.  Masked: one run per group, L = ceil(count / 128).  Contiguous: maximal
 // sequences of consecutive 128-row blocks whose first row carries the same expert (blocks
-// whose first row is -1 are padding and skipped).  `scratch` holds one int16 per m-block.
+// whose first row is -1 are padding and skipped).  Contiguous with prefix sums (a.psum): one
+// run per expert; expert e owns rows [round_up(psum[e-1], 128), psum[e]) (psum[-1] = 0) and
+// rt.x holds the end row; an expert whose end is below its predecessor's, past M, or inside the
+// rounding gap is flagged DG_STATUS_BAD_INDEX and it and every later expert are skipped.
+// `scratch` holds one int16 per m-block.
 template <Layout L, int NT>
 __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, void* scratch) {
     const int tid = threadIdx.x;
@@ -79,6 +84,32 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
             rt.L[g] = (c + BM - 1) / BM;
         }
         if (bad && blockIdx.x == 0) status_or(a.status, bad);
+        __syncthreads();
+    } else if (a.psum) {
+        int* s_first_bad = s_scan + NT / 32;  // scan scratch is free here
+        if (tid == 0) *s_first_bad = a.G;
+        __syncthreads();
+        for (int e = tid; e < a.G; e += NT) {
+            const int64_t prev = e > 0 ? a.routing[e - 1] : 0;
+            const int64_t end = a.routing[e];
+            const int64_t start = (prev + BM - 1) / BM * BM;
+            const bool bad = prev < 0 || end < prev || end > a.M || (end > prev && end < start);
+            if (bad) atomicMin(s_first_bad, e);
+        }
+        __syncthreads();
+        const int first_bad = *s_first_bad;
+        if (first_bad < a.G && blockIdx.x == 0 && tid == 0) status_or(a.status, DG_STATUS_BAD_INDEX);
+        for (int e = tid; e < a.G; e += NT) {
+            const int64_t prev = e > 0 ? a.routing[e - 1] : 0;
+            const int64_t end = a.routing[e];
+            const int64_t start = (prev + BM - 1) / BM * BM;
+            const bool live = e < first_bad && end > start;
+            rt.first[e] = live ? static_cast<int>(start / BM) : 0;
+            rt.L[e] = live ? static_cast<int>((end - start + BM - 1) / BM) : 0;
+            rt.e[e] = e;
+            rt.x[e] = live ? static_cast<int>(end) : 0;
+        }
+        R = a.G;
         __syncthreads();
     } else {
         const int nblk = static_cast<int>((a.M + BM - 1) / BM);

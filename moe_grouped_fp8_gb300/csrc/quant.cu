@@ -11,6 +11,7 @@
 #include <cuda_fp8.h>
 
 #include "host_common.hpp"
+#include "kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace dg {
@@ -202,8 +203,8 @@ constexpr int CH_PITCH = 132;  // bytes per transposed column row (128 tokens + 
 // -1 when the token lies past the last valid expert.  Walks ks with a block-wide scan in
 // chunks of blockDim.x (<= 256 threads) and stops at the first bad expert (K_e < 0,
 // K_e % 128 != 0, or a span past K_cap); *bad_bits gets the DG_STATUS_* bits it met.
-__device__ int find_expert(const int32_t* __restrict__ ks, int G, int64_t K_cap, int64_t tok, int64_t* o_out,
-                           int64_t* k_out, int* bad_bits) {
+__device__ int find_expert(const int32_t* __restrict__ ks, int psum, int G, int64_t K_cap, int64_t tok,
+                           int64_t* o_out, int64_t* k_out, int* bad_bits) {
     __shared__ long long s_warp[8];
     __shared__ long long s_carry, s_o, s_k;
     __shared__ int s_found, s_first_bad, s_bad;
@@ -218,7 +219,7 @@ __device__ int find_expert(const int32_t* __restrict__ ks, int G, int64_t K_cap,
     __syncthreads();
     for (int base = 0; base < G; base += blockDim.x) {
         const int e = base + t;
-        const long long k = (e < G) ? ks[e] : 0;
+        const long long k = (e < G) ? expert_k(ks, e, psum) : 0;
         int bad = (e < G && (k < 0 || (k % 128) != 0)) ? DG_STATUS_K_NOT_ALIGNED : 0;
         const long long kk = bad ? 0 : k;
         long long incl = kk;
@@ -274,7 +275,7 @@ struct ChannelOperand {
 
 __global__ void __launch_bounds__(256) k_quant_channel_128(const ChannelOperand op0, const ChannelOperand op1,
                                                            int nblk0, int64_t K_cap, const int32_t* __restrict__ ks,
-                                                           int G, float sf_zero, int32_t* status) {
+                                                           int psum, int G, float sf_zero, int32_t* status) {
     __shared__ float s_part[8][CH_COLS];
     __shared__ float s_r[CH_COLS];
     __shared__ __align__(16) uint8_t s_t[CH_COLS * CH_PITCH];
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(256) k_quant_channel_128(const ChannelOperand 
         raw[j] = __ldg(reinterpret_cast<const uint4*>(x + (tb * 128 + rb + j) * C + c0) + c);
     int64_t o_e = 0, k_e = 0;
     int bad = 0;
-    const int e = find_expert(ks, G, K_cap, tb * 128, &o_e, &k_e, &bad);
+    const int e = find_expert(ks, psum, G, K_cap, tb * 128, &o_e, &k_e, &bad);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) status_or(status, bad);
     if (e < 0) return;
     uint8_t* __restrict__ qp = op.q;
@@ -403,9 +404,11 @@ extern "C" int dg_quant_block_128x128(const void* w, int G, int64_t N, int64_t K
     return launch_pdl(k_quant_block_128x128<false>, grid, dim3(256), 0, s, wp, N, K, q, sfb, sf_zero);
 }
 
-extern "C" int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C, const int32_t* ks, int G,
-                                        uint8_t* q_packed, float* sf, float sf_zero, int32_t* status,
-                                        void* stream) {
+namespace dg {
+namespace {
+
+int quant_channel(const void* x, int64_t K_cap, int64_t C, const int32_t* ks, int psum, int G, uint8_t* q_packed,
+                  float* sf, float sf_zero, int32_t* status, void* stream) {
     DG_CHECK_ARG(K_cap >= 0 && K_cap % 128 == 0, "K_cap must be a multiple of 128 (%lld)", (long long)K_cap);
     DG_CHECK_ARG(C > 0 && C % CH_COLS == 0, "C must be a positive multiple of %d (%lld)", CH_COLS, (long long)C);
     DG_CHECK_ARG(G >= 1 && G <= DG_MAX_GROUPS, "G must be in [1, %d] (%d)", DG_MAX_GROUPS, G);
@@ -416,13 +419,12 @@ extern "C" int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C,
     dim3 grid(static_cast<unsigned>(C / CH_COLS), static_cast<unsigned>(K_cap / 128));
     const ChannelOperand op{static_cast<const uint16_t*>(x), C, q_packed, sf};
     return launch_pdl(k_quant_channel_128, grid, dim3(256), 0, static_cast<cudaStream_t>(stream), op, op,
-                      static_cast<int>(C / CH_COLS), K_cap, ks, G, sf_zero, status);
+                      static_cast<int>(C / CH_COLS), K_cap, ks, psum, G, sf_zero, status);
 }
 
-extern "C" int dg_quant_per_channel_128_pair(const void* x_a, int64_t C_a, uint8_t* q_a, float* sf_a, const void* x_b,
-                                             int64_t C_b, uint8_t* q_b, float* sf_b, int64_t K_cap,
-                                             const int32_t* ks, int G, float sf_zero, int32_t* status,
-                                             void* stream) {
+int quant_channel_pair(const void* x_a, int64_t C_a, uint8_t* q_a, float* sf_a, const void* x_b, int64_t C_b,
+                       uint8_t* q_b, float* sf_b, int64_t K_cap, const int32_t* ks, int psum, int G, float sf_zero,
+                       int32_t* status, void* stream) {
     DG_CHECK_ARG(K_cap >= 0 && K_cap % 128 == 0, "K_cap must be a multiple of 128 (%lld)", (long long)K_cap);
     DG_CHECK_ARG(C_a > 0 && C_a % CH_COLS == 0 && C_b > 0 && C_b % CH_COLS == 0,
                  "C_a and C_b must be positive multiples of %d", CH_COLS);
@@ -437,5 +439,34 @@ extern "C" int dg_quant_per_channel_128_pair(const void* x_a, int64_t C_a, uint8
     const int nblk0 = static_cast<int>(C_a / CH_COLS);
     dim3 grid(static_cast<unsigned>(nblk0 + C_b / CH_COLS), static_cast<unsigned>(K_cap / 128));
     return launch_pdl(k_quant_channel_128, grid, dim3(256), 0, static_cast<cudaStream_t>(stream), op0, op1, nblk0,
-                      K_cap, ks, G, sf_zero, status);
+                      K_cap, ks, psum, G, sf_zero, status);
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" int dg_quant_per_channel_128(const void* x, int64_t K_cap, int64_t C, const int32_t* ks, int G,
+                                        uint8_t* q_packed, float* sf, float sf_zero, int32_t* status,
+                                        void* stream) {
+    return quant_channel(x, K_cap, C, ks, 0, G, q_packed, sf, sf_zero, status, stream);
+}
+
+extern "C" int dg_quant_per_channel_128_psum(const void* x, int64_t K_cap, int64_t C, const int32_t* psum, int G,
+                                             uint8_t* q_packed, float* sf, float sf_zero, int32_t* status,
+                                             void* stream) {
+    return quant_channel(x, K_cap, C, psum, 1, G, q_packed, sf, sf_zero, status, stream);
+}
+
+extern "C" int dg_quant_per_channel_128_pair(const void* x_a, int64_t C_a, uint8_t* q_a, float* sf_a, const void* x_b,
+                                             int64_t C_b, uint8_t* q_b, float* sf_b, int64_t K_cap,
+                                             const int32_t* ks, int G, float sf_zero, int32_t* status,
+                                             void* stream) {
+    return quant_channel_pair(x_a, C_a, q_a, sf_a, x_b, C_b, q_b, sf_b, K_cap, ks, 0, G, sf_zero, status, stream);
+}
+
+extern "C" int dg_quant_per_channel_128_pair_psum(const void* x_a, int64_t C_a, uint8_t* q_a, float* sf_a,
+                                                  const void* x_b, int64_t C_b, uint8_t* q_b, float* sf_b,
+                                                  int64_t K_cap, const int32_t* psum, int G, float sf_zero,
+                                                  int32_t* status, void* stream) {
+    return quant_channel_pair(x_a, C_a, q_a, sf_a, x_b, C_b, q_b, sf_b, K_cap, psum, 1, G, sf_zero, status, stream);
 }

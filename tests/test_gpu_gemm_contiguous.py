@@ -131,8 +131,56 @@ def test_bad_indices_flagged_and_skipped():
     assert_close(to_f64(d)[:10], ref_out(ref[:10], False), False, "rows before the bad ones")
 
 
-def replay_case(G, N, K, E, replays, check_every, seed):
-    """Capture cast + GEMM once; replay with routing re-drawn in place (same buffers)."""
+def test_psum_layout_bitwise_equals_m_indices():
+    """Routing by per-expert end rows: the same rows, bitwise the same results as the m_indices
+    call; the oracle routes by its own reading of psum."""
+    counts = [130, 0, 1, 128, 257]
+    M = wl.contiguous_capacity(sum(counts), len(counts))
+    mi = wl.contiguous_m_indices(counts, m_max=M)
+    psum = wl.contiguous_psum(counts)
+    a, b = wl.randn_bf16((M, 384), 53, 1.5), wl.randn_bf16((5, 256, 384), 54, 0.02)
+    d_mi, _ = contiguous_case(a, b, mi)
+    qa, sfa = gpu_quant_tokens(a.cuda(), DG_SF_FP32)
+    qb, sfb = gpu_quant_blocks(b.cuda(), DG_SF_FP32)
+    d = sentinel_like((M, 256), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dg_m_grouped_fp8_contiguous_psum(qa, sfa, qb, sfb, d, torch.tensor(psum, device="cuda"), DG_SF_FP32, status)
+    sync()
+    assert status.item() == 0
+    assert np.array_equal(out_bits(d), out_bits(d_mi))
+    routed = oracle.m_indices_from_psum(psum, M)
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a)
+    oqb, osfb, _ = oracle.quant_block_128x128(b)
+    ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, routed)
+    ok = routed >= 0
+    assert_close(to_f64(d)[ok], ref_out(ref[ok], False), False, "psum routed rows")
+    assert np.all(out_bits(d)[~ok] == 0xFFFF)
+
+
+def test_psum_bad_entry_flagged_and_walk_stops():
+    psum = np.array([130, 100, 394], np.int32)           # expert 1 ends before expert 0
+    M, K, N = 512, 256, 128
+    a, b = wl.randn_bf16((M, K), 55), wl.randn_bf16((3, N, K), 56)
+    qa, sfa = gpu_quant_tokens(a.cuda(), DG_SF_FP32)
+    qb, sfb = gpu_quant_blocks(b.cuda(), DG_SF_FP32)
+    d = sentinel_like((M, N), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dg_m_grouped_fp8_contiguous_psum(qa, sfa, qb, sfb, d, torch.tensor(psum, device="cuda"), DG_SF_FP32, status)
+    sync()
+    assert status.item() & DG_STATUS_BAD_INDEX
+    routed = oracle.m_indices_from_psum(psum, M)
+    assert np.all(routed[130:] == -1)
+    bits = out_bits(d)
+    assert np.all(bits[130:] == 0xFFFF)
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a)
+    oqb, osfb, _ = oracle.quant_block_128x128(b)
+    ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, routed)
+    assert_close(to_f64(d)[:130], ref_out(ref[:130], False), False, "expert 0")
+
+
+def replay_case(G, N, K, E, replays, check_every, seed, mode="m_indices"):
+    """Capture cast + GEMM once; replay with routing re-drawn in place (same buffers), routed by
+    m_indices or by psum (the modes of the pages' graph-mutation test)."""
     T = G * E
     m_max = wl.contiguous_capacity(T, G)
     a = wl.randn_bf16((m_max, K), seed, 1.0, device="cuda")
@@ -141,15 +189,22 @@ def replay_case(G, N, K, E, replays, check_every, seed):
     qa = torch.empty(m_max, K, dtype=torch.uint8, device="cuda")
     sfa = api.empty_sfa(m_max, K, fmt, "cuda")
     qb, sfb = gpu_quant_blocks(b, fmt)
-    mi_dev = torch.full((m_max,), -1, dtype=torch.int32, device="cuda")
+    psum_mode = mode == "psum"
+    mi_dev = torch.full((G if psum_mode else m_max,), -1, dtype=torch.int32, device="cuda")
     d = torch.empty(m_max, N, dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
+    def routing(counts):
+        return wl.contiguous_psum(counts) if psum_mode else wl.contiguous_m_indices(counts, m_max)
+
     def step():
         api.dg_quant_per_token_1x128(a, qa, sfa, fmt)
-        api.dg_m_grouped_fp8_contiguous(qa, sfa, qb, sfb, d, mi_dev, fmt, status)
+        if psum_mode:
+            api.dg_m_grouped_fp8_contiguous_psum(qa, sfa, qb, sfb, d, mi_dev, fmt, status)
+        else:
+            api.dg_m_grouped_fp8_contiguous(qa, sfa, qb, sfb, d, mi_dev, fmt, status)
 
-    mi_dev.copy_(torch.from_numpy(wl.contiguous_m_indices(wl.multinomial_counts(T, G, seed), m_max)))
+    mi_dev.copy_(torch.from_numpy(routing(wl.multinomial_counts(T, G, seed))))
     step()                                             # eager warm-up before capture
     sync()
     g = torch.cuda.CUDAGraph()
@@ -174,8 +229,9 @@ def replay_case(G, N, K, E, replays, check_every, seed):
         counts = wl.multinomial_counts(T, G, seed + 1 + it)
         if it == replays // 2:
             counts = np.zeros(G, np.int32)             # an all-empty phase
-        mi_np = wl.contiguous_m_indices(counts, m_max)
-        mi_dev.copy_(torch.from_numpy(mi_np))          # same pointer, new values
+        r_np = routing(counts)
+        mi_dev.copy_(torch.from_numpy(r_np))           # same pointer, new values
+        mi_np = oracle.m_indices_from_psum(r_np, m_max) if psum_mode else r_np
         d.view(torch.int16).fill_(-1)
         g.replay()
         if it % check_every == 0 or it == replays // 2:
@@ -196,8 +252,9 @@ def replay_case(G, N, K, E, replays, check_every, seed):
     assert checked >= replays // check_every
 
 
-def test_graph_replay_with_changed_routing_small():
-    replay_case(G=16, N=256, K=256, E=20, replays=30, check_every=3, seed=7)
+@pytest.mark.parametrize("mode", ["m_indices", "psum"])
+def test_graph_replay_with_changed_routing_small(mode):
+    replay_case(G=16, N=256, K=256, E=20, replays=30, check_every=3, seed=7, mode=mode)
 
 
 @pytest.mark.slow

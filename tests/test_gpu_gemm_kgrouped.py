@@ -128,6 +128,69 @@ def test_capacity_beyond_sum_of_ks():
     kgrouped_case([128, 256], 128, 256, "separate", seed=17, K_cap=1024)
 
 
+def test_psum_layout_bitwise_equals_ks():
+    """Spans given as inclusive prefix sums (use_psum_layout): the pair cast and the wgrad give
+    bitwise the results of the ks calls; the oracle recovers K_e by its own reading of psum."""
+    ks = [256, 0, 128, 384]
+    G, N, H = len(ks), 256, 384
+    T = sum(ks)
+    psum = np.cumsum(ks).astype(np.int32)
+    gy, act = wl.randn_bf16((T, N), 61, 1e-3).cuda(), wl.randn_bf16((T, H), 62, 0.4).cuda()
+    outs = []
+    for fn_cast, fn_gemm, spans in ((api.dg_quant_per_channel_128_pair, api.dg_k_grouped_fp8_wgrad, ks),
+                                    (api.dg_quant_per_channel_128_pair_psum, api.dg_k_grouped_fp8_wgrad_psum, psum)):
+        sp = torch.tensor(np.asarray(spans, np.int32), device="cuda")
+        ap = torch.zeros(T * N, dtype=torch.uint8, device="cuda")
+        bp = torch.zeros(T * H, dtype=torch.uint8, device="cuda")
+        sfa = torch.zeros(T // 128, N, device="cuda")
+        sfb = torch.zeros(T // 128, H, device="cuda")
+        fn_cast(gy, act, sp, ap, sfa, bp, sfb)
+        d = torch.full((G, N, H), 0.5, dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fn_gemm(ap, sfa, bp, sfb, d, d, sp, T, api.kgrouped_workspace(G, "cuda"), status)
+        sync()
+        assert status.item() == 0
+        outs.append((ap.clone(), sfa.clone(), d.clone()))
+    for x, y in zip(outs[0], outs[1]):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    ks_o = oracle.sizes_from_psum(psum)
+    oqa, osfa = oracle.quant_per_channel_128(gy.cpu(), 1e-30)
+    oqb, osfb = oracle.quant_per_channel_128(act.cpu(), 1e-30)
+    c = np.full((G, N, H), 0.5, np.float32)
+    ref = oracle.gemm_kgrouped(oracle.pack_kmajor(oqa, ks_o), osfa, oracle.pack_kmajor(oqb, ks_o), osfb, ks_o, N, H,
+                               c=c)
+    got = outs[1][2].double().cpu().numpy()
+    for e in range(G):
+        assert_close(got[e], ref[e].astype(np.float32), True, f"expert {e}")
+
+
+def test_psum_decreasing_entry_stops_the_walk():
+    psum = np.array([128, 384, 256, 512], np.int32)     # K_2 = -128
+    G, N, H, K_cap = 4, 128, 128, 512
+    gy, act = wl.randn_bf16((K_cap, N), 63).cuda(), wl.randn_bf16((K_cap, H), 64).cuda()
+    sp = torch.tensor(psum, device="cuda")
+    ap = torch.zeros(K_cap * N, dtype=torch.uint8, device="cuda")
+    bp = torch.zeros(K_cap * H, dtype=torch.uint8, device="cuda")
+    sfa = torch.zeros(K_cap // 128, N, device="cuda")
+    sfb = torch.zeros(K_cap // 128, H, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dg_quant_per_channel_128_pair_psum(gy, act, sp, ap, sfa, bp, sfb, status=status)
+    d = torch.zeros(G, N, H, dtype=torch.float32, device="cuda")
+    api.dg_k_grouped_fp8_wgrad_psum(ap, sfa, bp, sfb, None, d, sp, K_cap, api.kgrouped_workspace(G, "cuda"), status)
+    sync()
+    assert status.item() & DG_STATUS_K_NOT_ALIGNED
+    ks_o = oracle.sizes_from_psum(psum)
+    assert ks_o[2] < 0
+    got = d.double().cpu().numpy()
+    assert np.all(got[2:] == 0), "experts from the bad one on are not computed"
+    oqa, osfa = oracle.quant_per_channel_128(gy[:384].cpu(), 1e-30)
+    oqb, osfb = oracle.quant_per_channel_128(act[:384].cpu(), 1e-30)
+    ref = oracle.gemm_kgrouped(oracle.pack_kmajor(oqa, ks_o[:2]), osfa, oracle.pack_kmajor(oqb, ks_o[:2]), osfb,
+                               ks_o[:2], N, H)
+    for e in range(2):
+        assert_close(got[e], ref[e].astype(np.float32), True, f"expert {e}")
+
+
 def test_bad_ks_flagged_and_walk_stops():
     ks = [128, 100, 128]
     G, N, H, K_cap = 3, 128, 128, 512
