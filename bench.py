@@ -353,10 +353,8 @@ class MGroupedWorkload:
             raise SystemExit(f"unknown workload {kind}")
         self.kind = kind
         self.masked = isinstance(self.w, wl.Masked)
-        # the kernel the library picks for this call (bf16 output): CTA pairs when a masked call's
-        # expected_m hint spans more than one 128-row block
-        self.kernel_name = ("k_grouped_gemm_pair" if self.masked and self.w.expected_m > 128
-                            else "k_grouped_gemm")
+        # the kernel the library runs for these calls (bf16 output, single-CTA tiles)
+        self.kernel_name = "k_grouped_gemm"
         w = self.w
         self.fmt = DG_SF_UE8M0 if getattr(w, "ue8m0", False) else DG_SF_FP32
         a, b = w.draw(device=device)

@@ -169,8 +169,7 @@ int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sfa, const ui
  * next expert's rows, and rows in [count, cap) inside a tile are not stored either.
  *   a: e4m3 [G, cap, K].  b: e4m3 [G, N, K].  d: [G, cap, N] bf16 or fp32.
  *   sfa: [K/128][Mp] with M = G*cap.  counts: int32 [G] device.
- *   expected_m: a hint only; it never changes the result.  (Above 128 it selects the CTA-pair
- *   kernel, whose outputs are bitwise identical to the single-CTA kernel's.)
+ *   expected_m: a hint only; it never changes the result.
  */
 int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
                             void* d, int out_dtype, const int32_t* counts, int G, int64_t cap,

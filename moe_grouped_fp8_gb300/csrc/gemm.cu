@@ -42,11 +42,14 @@ constexpr int MMA_WARP = 9;
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_BAR = 1;  // named barrier of the 256 promotion/store threads
 
-constexpr int TBUFS = 4;          // TMEM partial buffers: the tensor core runs up to 3 blocks ahead
-constexpr int SF_GROUP = 4;       // 128-K blocks whose scales a promotion thread loads together
 
 template <Layout L, int BN, int STAGES, bool OUT_FP32>
 struct Plan {
+    // TMEM partial buffers (the tensor core runs up to TB - 1 blocks ahead of the promotion) and
+    // the 128-K blocks whose scales a promotion thread prefetches together; a 256-column tile
+    // keeps 128 accumulators per thread, which leaves room for fewer of both.
+    static constexpr int TB = BN == 256 ? 2 : 4;
+    static constexpr int SFG = BN == 256 ? 2 : 4;
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -59,17 +62,19 @@ struct Plan {
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
     static constexpr int BAR_OFF = (SCHED_OFF + SCHED_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * TB;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int MISC_BYTES = 256;
     static constexpr int TOTAL = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
-    static constexpr uint32_t TMEM_COLS = TBUFS * BN;
+    static constexpr uint32_t TMEM_COLS = TB * BN;
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
     static_assert(CPT % 32 == 0, "promotion threads read 32-column groups");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
     static_assert(STG_OFF % 1024 == 0 && SCHED_OFF % 1024 == 0, "TMA / swizzle buffers are 1024-byte aligned");
     static_assert(BAR_OFF % 8 == 0 && MISC_OFF % 8 == 0, "mbarrier objects are 8-byte aligned");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two <= 512");
+    static_assert(CPT <= 64 || CPT % 16 == 0, "chunked promotion");
+    static_assert(BN == 128 || (BN == 256 && !OUT_FP32), "256-column tiles stage bf16 output only");
     static_assert(TOTAL <= 232448, "shared memory");
 };
 
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* tempty = tfull + TBUFS;
+    uint64_t* tempty = tfull + P::TB;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + P::MISC_OFF + 4);
     int* s_ntiles = reinterpret_cast<int*>(smem + P::MISC_OFF + 12);
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < TBUFS; ++b) {
+        for (int b = 0; b < P::TB; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], NUM_EPI_WARPS);
         }
@@ -229,14 +234,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     umma_commit(&tfull[tb]);
                     any = true;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    if (++tb == TBUFS) { tb = 0; tphase ^= 1u; }
+                    if (++tb == P::TB) { tb = 0; tphase ^= 1u; }
                 }
             }
             if (any) {
                 // the last commit: wait until the tensor core is done with every MMA issued
                 int lt = tb - 1;
                 uint32_t lp = tphase;
-                if (lt < 0) { lt = TBUFS - 1; lp ^= 1u; }
+                if (lt < 0) { lt = P::TB - 1; lp ^= 1u; }
                 drain_wait(&tfull[lt], lp, a.wait_limit_ns);
             }
         }
@@ -280,10 +285,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int sbi0 = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB;
             // raw scale bits (fp32, or the UE8M0 byte): converted where used, so that no
             // instruction waits on the loads until the group's first block is promoted
-            auto load_group = [&](int g, uint32_t (&sa)[SF_GROUP], uint32_t (&sb)[SF_GROUP]) {
+            auto load_group = [&](int g, uint32_t (&sa)[P::SFG], uint32_t (&sb)[P::SFG]) {
 #pragma unroll
-                for (int u = 0; u < SF_GROUP; ++u) {
-                    const int kbi = g * SF_GROUP + u;
+                for (int u = 0; u < P::SFG; ++u) {
+                    const int kbi = g * P::SFG + u;
                     sa[u] = 0u;
                     sb[u] = 0u;
                     if (row_ok && kbi < ti.kbt) {
@@ -304,40 +309,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else
                     return __uint_as_float(sa) * __uint_as_float(sb);
             };
-            uint32_t sa_c[SF_GROUP], sb_c[SF_GROUP], sa_n[SF_GROUP], sb_n[SF_GROUP];
+            uint32_t sa_c[P::SFG], sb_c[P::SFG], sa_n[P::SFG], sb_n[P::SFG];
             load_group(0, sa_c, sb_c);
             load_group(1, sa_n, sb_n);
-            for (int kb0 = 0; kb0 < ti.kbt && !failed; kb0 += SF_GROUP) {
+            for (int kb0 = 0; kb0 < ti.kbt && !failed; kb0 += P::SFG) {
 #pragma unroll
-                for (int u = 0; u < SF_GROUP; ++u) {
+                for (int u = 0; u < P::SFG; ++u) {
                     if (kb0 + u >= ti.kbt) break;
                     const float s = scale_of(sa_c[u], sb_c[u]);
                     if (!mbar_wait(&tfull[tb], tphase, wc)) { failed = true; break; }
                     tc_fence_after();
-                    uint32_t v[P::CPT / 32][32];
+                    if constexpr (P::CPT <= 64) {
+                        uint32_t v[P::CPT / 32][32];
 #pragma unroll
-                    for (int c2 = 0; c2 < P::CPT / 32; ++c2)
-                        tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32), v[c2]);
+                        for (int c2 = 0; c2 < P::CPT / 32; ++c2)
+                            tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32),
+                                        v[c2]);
 #pragma unroll
-                    for (int c2 = 0; c2 < P::CPT / 32; ++c2) tmem_wait_ld(v[c2]);
-                    // the partial is in registers: hand the TMEM buffer back before the FMAs
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[tb]);
-                    if (++tb == TBUFS) { tb = 0; tphase ^= 1u; }
+                        for (int c2 = 0; c2 < P::CPT / 32; ++c2) tmem_wait_ld(v[c2]);
+                        // the partial is in registers: hand the TMEM buffer back before the FMAs
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[tb]);
+                        if (++tb == P::TB) { tb = 0; tphase ^= 1u; }
 #pragma unroll
-                    for (int c2 = 0; c2 < P::CPT / 32; ++c2)
+                        for (int c2 = 0; c2 < P::CPT / 32; ++c2)
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2)
-                            ffma2(acc[c2 * 32 + i], acc[c2 * 32 + i + 1], s, __uint_as_float(v[c2][i]),
-                                  __uint_as_float(v[c2][i + 1]));
+                            for (int i = 0; i < 32; i += 2)
+                                ffma2(acc[c2 * 32 + i], acc[c2 * 32 + i + 1], s, __uint_as_float(v[c2][i]),
+                                      __uint_as_float(v[c2][i + 1]));
+                    } else {
+                        // 128 accumulators leave room for 16 loaded columns at a time; the buffer
+                        // is handed back after the last load
+#pragma unroll
+                        for (int c2 = 0; c2 < P::CPT / 16; ++c2) {
+                            uint32_t v[16];
+                            tmem_ld_x16(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 16), v);
+                            tmem_wait_ld(v);
+                            if (c2 == P::CPT / 16 - 1) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&tempty[tb]);
+                                if (++tb == P::TB) { tb = 0; tphase ^= 1u; }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2)
+                                ffma2(acc[c2 * 16 + i], acc[c2 * 16 + i + 1], s, __uint_as_float(v[i]),
+                                      __uint_as_float(v[i + 1]));
+                        }
+                    }
                 }
 #pragma unroll
-                for (int u = 0; u < SF_GROUP; ++u) {
+                for (int u = 0; u < P::SFG; ++u) {
                     sa_c[u] = sa_n[u];
                     sb_c[u] = sb_n[u];
                 }
-                load_group(kb0 / SF_GROUP + 2, sa_n, sb_n);
+                load_group(kb0 / P::SFG + 2, sa_n, sb_n);
             }
 
             // ---- stage the tile in shared memory
@@ -455,34 +482,49 @@ int launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap&
 constexpr int MG_BN = 128;
 constexpr int MG_STAGES = 4;
 constexpr int MG_STAGES_BF16 = 5;
+constexpr int MG_BN_WIDE = 256;      // bf16 output with N % 256 == 0: 128 x 256 tiles
+constexpr int MG_STAGES_WIDE = 3;    // 48 KB stages
+
+// Columns of a single-CTA tile: 256 when the output is bf16 and N is a multiple of 256 of at
+// least 1024 (half the MMA instructions and TMEM handshakes per FLOP, 25% fewer operand bytes
+// through shared memory; measured 0.408 -> 0.329 ms on the prefill shape, 0.478 -> 0.419 ms on
+// decode), else 128 (narrow N: twice the tiles for the same weights, measured faster at N = 512).
+// Both tile widths give bitwise the same results.
+int single_bn(int out, int64_t N) {
+    return (out == DG_OUT_BF16 && N % MG_BN_WIDE == 0 && N >= 4 * MG_BN_WIDE) ? MG_BN_WIDE : MG_BN;
+}
 
 CUtensorMapDataType out_tmap_type(int out) {
     return out == DG_OUT_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
-// Kernel choice.  Both kernels promote the same fp32 tensor-core partials in the same K order
-// with the same FMAs, so their outputs are bitwise identical and the choice may follow a hint.
-// CTA pairs (256 x PAIR_BN tiles, gemm_pair.cu, bf16 output only) halve the weight bytes
-// fetched per row pair but compute a run's odd last block for nothing, so they are chosen when
-// groups are expected to span two or more 128-row blocks (the masked layout's expected_m hint);
-// every other call runs on single CTAs (128 x 128 tiles).  A test hook can force either.
+// Kernel choice.  The single-CTA kernel (128 x 128 or 128 x 256 tiles) and the CTA-pair kernel
+// (256 x PAIR_BN tiles, gemm_pair.cu, bf16 output only) promote the same fp32 tensor-core
+// partials in the same K order with the same FMAs, so their outputs are bitwise identical.  With
+// 128 x 256 tiles the single-CTA kernel measured faster than the pairs on every configured shape
+// (decode 0.419 vs 0.425 ms, prefill 0.329 vs 0.457 ms), so calls run on single CTAs; the pair
+// kernel is reached through the test hook, which keeps it under the parity tests.
 std::atomic<int> g_force_kernel{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA pairs
 
-bool use_pair(int out, bool prefer_pair) {
+bool use_pair(int out, bool /*prefer_pair*/) {
     if (out != DG_OUT_BF16) return false;
-    const int f = g_force_kernel.load(std::memory_order_relaxed);
-    return f == 0 ? prefer_pair : f == 2;
+    return g_force_kernel.load(std::memory_order_relaxed) == 2;
 }
 
 template <Layout L>
 int dispatch_mgrouped(bool pair, int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB,
                       const CUtensorMap& tD, const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
     if (pair) return launch_mgrouped_pair(L, fmt == DG_SF_UE8M0, tA, tB, tD, tD8, args, s);
-    args.num_nb = static_cast<int>(args.N / MG_BN);
+    const int bn = single_bn(out, args.N);
+    args.num_nb = static_cast<int>(args.N / bn);
     // bf16 output stages half as much as fp32, which leaves room for a fifth ring stage
     if (out == DG_OUT_FP32) {
         if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES, true, true>(tA, tB, tD, tD8, args, s);
         return launch_gemm<L, MG_BN, MG_STAGES, true, false>(tA, tB, tD, tD8, args, s);
+    }
+    if (bn == MG_BN_WIDE) {
+        if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN_WIDE, MG_STAGES_WIDE, false, true>(tA, tB, tD, tD8, args, s);
+        return launch_gemm<L, MG_BN_WIDE, MG_STAGES_WIDE, false, false>(tA, tB, tD, tD8, args, s);
     }
     if (fmt == DG_SF_UE8M0) return launch_gemm<L, MG_BN, MG_STAGES_BF16, false, true>(tA, tB, tD, tD8, args, s);
     return launch_gemm<L, MG_BN, MG_STAGES_BF16, false, false>(tA, tB, tD, tD8, args, s);
@@ -532,7 +574,7 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = pair ? PAIR_B_ROWS : MG_BN;
+        const uint32_t brows = pair ? PAIR_B_ROWS : static_cast<uint32_t>(single_bn(out_dtype, N));
         uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
@@ -594,7 +636,7 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = pair ? PAIR_B_ROWS : MG_BN;
+        const uint32_t brows = pair ? PAIR_B_ROWS : static_cast<uint32_t>(single_bn(out_dtype, N));
         uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))

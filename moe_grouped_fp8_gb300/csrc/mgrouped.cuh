@@ -39,22 +39,25 @@ struct GemmArgs {
     int psum;        // Contiguous: routing holds per-expert end rows (prefix sums), not m_indices
 };
 
-// Shared-memory bytes of the run table used by build_runs / tile_prefix.
-constexpr int SCHED_BYTES = (MAX_RUNS + 1) * 4 + 4 * MAX_RUNS * 4;
+// Shared-memory bytes of the run table used by build_runs / tile_prefix: int32 prefix and x,
+// int16 first / L / e (m-blocks < DG_MAX_M_BLOCKS, experts < DG_MAX_GROUPS).
+constexpr int SCHED_BYTES = (MAX_RUNS + 1) * 4 + MAX_RUNS * 4 + 3 * MAX_RUNS * 2;
+static_assert(DG_MAX_M_BLOCKS <= 32767 && DG_MAX_GROUPS <= 32767, "int16 run-table fields");
 
 struct RunTable {
-    int* prefix;  // [MAX_RUNS + 1] first tile of each run
-    int* first;   // [MAX_RUNS] Contiguous: first m-block of the run; Masked: group
-    int* L;       // [MAX_RUNS] m-blocks of the run
-    int* e;       // [MAX_RUNS] expert of the run
-    int* x;       // [MAX_RUNS] Masked: valid rows of the group (count clamped to [0, cap])
+    int* prefix;     // [MAX_RUNS + 1] first tile of each run
+    int* x;          // [MAX_RUNS] Masked: valid rows of the group (count clamped to [0, cap]);
+                     //            Contiguous with prefix sums: end row of the expert
+    int16_t* first;  // [MAX_RUNS] Contiguous: first m-block of the run; Masked: group
+    int16_t* L;      // [MAX_RUNS] m-blocks of the run
+    int16_t* e;      // [MAX_RUNS] expert of the run
     __device__ static RunTable at(uint8_t* base) {
         RunTable t;
         t.prefix = reinterpret_cast<int*>(base);
-        t.first = t.prefix + (MAX_RUNS + 1);
+        t.x = t.prefix + (MAX_RUNS + 1);
+        t.first = reinterpret_cast<int16_t*>(t.x + MAX_RUNS);
         t.L = t.first + MAX_RUNS;
         t.e = t.L + MAX_RUNS;
-        t.x = t.e + MAX_RUNS;
         return t;
     }
 };
@@ -78,10 +81,10 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
             int c = a.routing[g];
             if (c < 0) { bad |= DG_STATUS_COUNT_GT_CAP; c = 0; }
             if (c > a.M) { bad |= DG_STATUS_COUNT_GT_CAP; c = static_cast<int>(a.M); }
-            rt.first[g] = g;
-            rt.e[g] = g;
+            rt.first[g] = static_cast<int16_t>(g);
+            rt.e[g] = static_cast<int16_t>(g);
             rt.x[g] = c;
-            rt.L[g] = (c + BM - 1) / BM;
+            rt.L[g] = static_cast<int16_t>((c + BM - 1) / BM);
         }
         if (bad && blockIdx.x == 0) status_or(a.status, bad);
         __syncthreads();
@@ -104,9 +107,9 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
             const int64_t end = a.routing[e];
             const int64_t start = (prev + BM - 1) / BM * BM;
             const bool live = e < first_bad && end > start;
-            rt.first[e] = live ? static_cast<int>(start / BM) : 0;
-            rt.L[e] = live ? static_cast<int>((end - start + BM - 1) / BM) : 0;
-            rt.e[e] = e;
+            rt.first[e] = static_cast<int16_t>(live ? start / BM : 0);
+            rt.L[e] = static_cast<int16_t>(live ? (end - start + BM - 1) / BM : 0);
+            rt.e[e] = static_cast<int16_t>(e);
             rt.x[e] = live ? static_cast<int>(end) : 0;
         }
         R = a.G;
@@ -135,8 +138,8 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
             const int e = blk_e[b];
             if (e >= 0 && (b == 0 || blk_e[b - 1] != e)) {
                 if (r < MAX_RUNS) {
-                    rt.first[r] = b;
-                    rt.e[r] = e;
+                    rt.first[r] = static_cast<int16_t>(b);
+                    rt.e[r] = static_cast<int16_t>(e);
                 }
                 ++r;
             }
@@ -151,7 +154,7 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
         for (int b = lo; b < hi; ++b) {
             const int e = blk_e[b];
             if (e >= 0 && (b == nblk - 1 || blk_e[b + 1] != e)) {
-                if (r2 < MAX_RUNS) rt.L[r2] = b - rt.first[r2] + 1;
+                if (r2 < MAX_RUNS) rt.L[r2] = static_cast<int16_t>(b - rt.first[r2] + 1);
                 ++r2;
             }
         }

@@ -14,10 +14,11 @@ from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_b
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["pair", "single"], autouse=True)
+@pytest.fixture(params=["auto", "pair"], autouse=True)
 def mgrouped_kernel(request):
-    """bf16 outputs run on CTA pairs by default; every small case also runs on single-CTA tiles."""
-    if request.param == "single" and request.node.get_closest_marker("slow"):
+    """Every case runs on the kernel the library picks ("auto": single-CTA tiles, 128 x 256 when
+    N % 256 == 0 and N >= 1024); small cases also run on the CTA-pair kernel."""
+    if request.param == "pair" and request.node.get_closest_marker("slow"):
         pytest.skip("full-size cases run on the default kernel")
     set_mgrouped_kernel(request.param)
     yield request.param
@@ -66,6 +67,15 @@ def test_small_ragged_segments(fmt, out):
     a = wl.randn_bf16((mi.size, 384), 51, 1.5)
     b = wl.randn_bf16((5, 256, 384), 52, 0.02)
     contiguous_case(a, b, mi, fmt, out)
+
+
+def test_wide_tiles_ragged_segments():
+    """N = 1024: 128 x 256 tiles on ragged segments, repeated calls bitwise identical."""
+    counts = [130, 0, 257, 1]
+    mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
+    a = wl.randn_bf16((mi.size, 256), 57, 1.0)
+    b = wl.randn_bf16((4, 1024, 256), 58, 0.02)
+    contiguous_case(a, b, mi, calls=4)
 
 
 def test_single_expert_plain_gemm_and_repeat_bitwise():

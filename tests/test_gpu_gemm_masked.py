@@ -14,10 +14,11 @@ from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_b
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["pair", "single"], autouse=True)
+@pytest.fixture(params=["auto", "pair"], autouse=True)
 def mgrouped_kernel(request):
-    """bf16 outputs run on CTA pairs by default; every small case also runs on single-CTA tiles."""
-    if request.param == "single" and request.node.get_closest_marker("slow"):
+    """Every case runs on the kernel the library picks ("auto": single-CTA tiles, 128 x 256 when
+    N % 256 == 0 and N >= 1024); small cases also run on the CTA-pair kernel."""
+    if request.param == "pair" and request.node.get_closest_marker("slow"):
         pytest.skip("full-size cases run on the default kernel")
     set_mgrouped_kernel(request.param)
     yield request.param
@@ -99,6 +100,20 @@ def test_pair_tiles_odd_blocks_and_column_tail():
     masked_case(a, b, [640, 385])
 
 
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+def test_wide_tiles(fmt):
+    """N = 1024: the single-CTA kernel runs 128 x 256 tiles (bitwise equal to the pair kernel,
+    checked in the test above for the narrow case)."""
+    G, cap, N, K = 3, 300, 1024, 384
+    a = wl.randn_bf16((G, cap, K), 15, 2.0)
+    b = wl.randn_bf16((G, N, K), 16, 0.02)
+    d, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
+    set_mgrouped_kernel("pair")
+    d2, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
+    set_mgrouped_kernel("auto")
+    assert np.array_equal(out_bits(d), out_bits(d2))
+
+
 def test_single_expert_and_all_empty():
     a = wl.randn_bf16((1, 130, 256), 21)
     b = wl.randn_bf16((1, 128, 256), 22)
@@ -118,8 +133,8 @@ def test_expected_m_does_not_change_result():
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
 def test_single_and_pair_kernels_bitwise_equal(mgrouped_kernel, fmt):
-    """Both m-grouped kernels give the same bits, which is what lets expected_m choose one."""
-    if mgrouped_kernel == "single":
+    """Both m-grouped kernels give the same bits, so the choice between them has no numerical effect."""
+    if mgrouped_kernel == "pair":
         pytest.skip("runs both kernels itself")
     G, cap, N, K = 3, 300, 640, 512
     a = wl.randn_bf16((G, cap, K), 13, 2.0)
