@@ -118,15 +118,25 @@ class ClockSampler:
         return out
 
 
-def kernel_source_sha() -> str:
+# The sources each GEMM kernel is compiled from: a profile summary stays valid while they are
+# unchanged (its kernel_source_sha line records their hash at capture time).
+KERNEL_SOURCES = {
+    "k_kgrouped_gemm": ["kgrouped.cu", "kernel_common.cuh", "ptx.cuh"],
+    "k_grouped_gemm": ["gemm.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
+    "k_grouped_gemm_pair": ["gemm_pair.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
+    "k_grouped_gemm_bf16": ["gemm_bf16.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in ["gemm.cu", "gemm_pair.cu", "mgrouped.cuh", "kgrouped.cu", "kernel_common.cuh", "ptx.cuh"]:
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(ROOT, "moe_grouped_fp8_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name: str):
-    """dram bytes per launch recorded under profiles/<name>.txt, if the kernel source is unchanged."""
+def profiled_traffic(name: str, kernel: str):
+    """dram bytes per launch recorded under profiles/<name>.txt, if the kernel's sources are unchanged."""
     p = os.path.join(ROOT, "profiles", f"{name}.txt")
     if not os.path.exists(p):
         return None
@@ -135,7 +145,7 @@ def profiled_traffic(name: str):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("kernel_source_sha") != kernel_source_sha():
+    if kv.get("kernel_source_sha") != kernel_source_sha(kernel):
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -473,7 +483,8 @@ class BF16GroupedWorkload:
         from moe_grouped_fp8_gb300 import workloads as wl
         base = kind[:-len("_bf16")]
         self.w = {"masked_repro": wl.masked_repro, "masked_decode": wl.masked_decode,
-                  "contiguous_prefill": wl.contiguous_prefill}[base]()
+                  "contiguous_prefill": wl.contiguous_prefill, "masked_decode_g8": wl.masked_decode_g8,
+                  "contiguous_prefill_g8": wl.contiguous_prefill_g8}[base]()
         w = self.w
         self.masked = isinstance(w, wl.Masked)
         self.kernel_name = "k_grouped_gemm_bf16"
@@ -623,7 +634,7 @@ def run_ours(args, ws, rank, local):
         achieved = wk.flops / (ms_gemm * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp8_peak, 4)}
-    traffic = profiled_traffic(f"{args.workload}_gemm")
+    traffic = profiled_traffic(f"{args.workload}_gemm", wk.kernel_name)
     roof.update({"traffic": traffic, "kernel": wk.kernel_name, "algorithmic_bytes": gemm_bytes,
                  "kernel_ms": round(ms_gemm, 5), "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json "
                  f"hbm_gbs; {'bf16 peak' if hasattr(wk, 'peak_tflops') else 'fp8 peak = bf16 x 2'})"
