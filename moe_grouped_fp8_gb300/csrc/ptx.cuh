@@ -407,6 +407,24 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mas
 }
 
 // acc0 += s * v0 and acc1 += s * v1 as one packed fp32 FMA; each lane rounds exactly like fmaf.
+// (y0, y1) = (x0 * s, x1 * s): one packed fp32 multiply, each lane rounded to nearest.
+__device__ __forceinline__ void fmul2(float& y0, float& y1, float x0, float x1, float s) {
+    asm("{\n\t.reg .b64 d, a, b;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %4};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(x0), "f"(x1), "f"(s));
+}
+
+// Hardware reciprocal approximation (at most 1 ulp from 1/x for normal x).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void ffma2(float& acc0, float& acc1, float s, float v0, float v1) {
     asm("{\n\t.reg .b64 d, a, b;\n\t"
         "mov.b64 a, {%2, %3};\n\t"

@@ -36,6 +36,53 @@ __device__ __forceinline__ uint8_t to_e4m3(float v, float r) {
     return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fmul_rn(v, r), __NV_SATFINITE, __NV_E4M3));
 }
 
+// The scale of a block and its reciprocal: bit-identical to scale_rule, ue8m0_round_up and
+// __frcp_rn, with fewer instructions on the common path.  When amax lies in [1e-27, FLT_MAX] the
+// clamps of scale_rule are inactive and the quotient is normal, so amax / 448 is formed by
+// Markstein's FMA-corrected division (the product with the rounded reciprocal of 448, its exact
+// residual, one corrective FMA), and 1/sf is exact from the exponent for UE8M0 scales (a power of
+// two) or one Newton-Raphson step from the hardware approximation for fp32 scales.  Both shortcuts
+// were checked in exact rational arithmetic for every finite bf16 amax on that path (the cast's
+// amax is a bf16 value), the reciprocal for every start within 1 ulp of 1/sf.  Every other amax
+// (zero, tiny, inf, NaN) takes the IEEE operations.
+template <bool UE8M0>
+__device__ __forceinline__ void block_scale(float amax, float sf_zero, float& sf, float& r, uint8_t& byte) {
+    constexpr float kInv448 = 1.0f / 448.0f;
+    if (amax >= 1e-27f && amax <= 3.40282347e38f) {
+        const float q0 = __fmul_rn(amax, kInv448);
+        sf = __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), kInv448, q0);
+        if constexpr (UE8M0) {
+            const uint32_t b = __float_as_uint(sf);
+            const uint32_t e = (b >> 23) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u);
+            byte = static_cast<uint8_t>(e);
+            sf = __uint_as_float(e << 23);
+            r = __uint_as_float((254u - e) << 23);
+        } else {
+            const float y = rcp_approx(sf);
+            r = __fmaf_rn(__fmaf_rn(-sf, y, 1.0f), y, y);
+        }
+    } else {
+        sf = scale_rule(amax, sf_zero);
+        if constexpr (UE8M0) sf = ue8m0_round_up(sf, &byte);
+        r = __frcp_rn(sf);
+    }
+}
+
+// Codes of 8 values scaled by r, as two little-endian words (value i in byte i).
+__device__ __forceinline__ uint2 e4m3x8(const float (&f)[8], float r) {
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float p[4];
+        fmul2(p[0], p[1], f[4 * h], f[4 * h + 1], r);
+        fmul2(p[2], p[3], f[4 * h + 2], f[4 * h + 3], r);
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
+        w[h] = lo | (hi << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
 __device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -73,26 +120,29 @@ __global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __res
     if (r_begin >= lim) return;
     const int64_t r_end = min(lim, r_begin + rows_per_cta);
     const int64_t m_base = g * rpg + r_begin;
-    const int64_t items = (r_end - r_begin) * KB;
+    const int items = static_cast<int>((r_end - r_begin) * KB);
+    const int KBi = static_cast<int>(KB);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hw = lane >> 4;   // half-warp
     const int sub = lane & 15;  // 16-byte chunk within the 256-byte block
     constexpr int PER_WARP = 2 * TOKEN_ITEMS_PER_HW;
-    const int nwarps = blockDim.x >> 5;
-
-    for (int64_t base = static_cast<int64_t>(warp) * PER_WARP; base < items; base += nwarps * PER_WARP) {
+    const int step = (blockDim.x >> 5) * PER_WARP;  // items a CTA pass covers
+    const int step_m = step / KBi, step_kb = step - step_m * KBi;
+    // item it <-> (row m_base + mr, column block kb), advanced incrementally by `step`
+    int it[TOKEN_ITEMS_PER_HW], mr[TOKEN_ITEMS_PER_HW], kb[TOKEN_ITEMS_PER_HW];
+#pragma unroll
+    for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
+        it[j] = warp * PER_WARP + 2 * j + hw;
+        mr[j] = it[j] / KBi;
+        kb[j] = it[j] - mr[j] * KBi;
+    }
+    for (int base = warp * PER_WARP; base < items; base += step) {
         uint4 raw[TOKEN_ITEMS_PER_HW];
-        bool live[TOKEN_ITEMS_PER_HW];
-        int64_t m_of[TOKEN_ITEMS_PER_HW], kb_of[TOKEN_ITEMS_PER_HW];
 #pragma unroll
         for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
-            const int64_t it = base + 2 * j + hw;
-            const bool ok = it < items;
-            const int64_t m = m_base + (ok ? it / KB : 0), kb = ok ? it % KB : 0;
-            live[j] = ok;
-            m_of[j] = m;
-            kb_of[j] = kb;
-            raw[j] = ok ? __ldg(reinterpret_cast<const uint4*>(x + m * ldx + kb * 128) + sub) : make_uint4(0, 0, 0, 0);
+            const int64_t m = m_base + mr[j];
+            raw[j] = it[j] < items ? __ldg(reinterpret_cast<const uint4*>(x + m * ldx + kb[j] * 128) + sub)
+                                   : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
@@ -103,23 +153,25 @@ __global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __res
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            if (!live[j]) continue;
-            float sf = scale_rule(amax, sf_zero);
-            uint8_t byte = 0;
-            if constexpr (UE8M0) sf = ue8m0_round_up(sf, &byte);
-            const float r = __frcp_rn(sf);
-            uint32_t lo = 0, hi = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(to_e4m3(f[i], r)) << (8 * i);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(to_e4m3(f[4 + i], r)) << (8 * i);
-            const int64_t m = m_of[j], kb = kb_of[j];
-            *reinterpret_cast<uint2*>(q + m * K + kb * 128 + sub * 8) = make_uint2(lo, hi);
-            if (sub == 0) {
-                if constexpr (UE8M0)
-                    static_cast<uint8_t*>(sfa)[kb * Mp + m] = byte;
-                else
-                    static_cast<float*>(sfa)[kb * Mp + m] = sf;
+            if (it[j] < items) {
+                float sf, r;
+                uint8_t byte = 0;
+                block_scale<UE8M0>(amax, sf_zero, sf, r, byte);
+                const int64_t m = m_base + mr[j];
+                *reinterpret_cast<uint2*>(q + m * K + kb[j] * 128 + sub * 8) = e4m3x8(f, r);
+                if (sub == 0) {
+                    if constexpr (UE8M0)
+                        static_cast<uint8_t*>(sfa)[kb[j] * Mp + m] = byte;
+                    else
+                        static_cast<float*>(sfa)[kb[j] * Mp + m] = sf;
+                }
+            }
+            it[j] += step;
+            mr[j] += step_m;
+            kb[j] += step_kb;
+            if (kb[j] >= KBi) {
+                kb[j] -= KBi;
+                ++mr[j];
             }
         }
     }
@@ -375,7 +427,7 @@ extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int
     const int64_t KB = K / 128;
     const int64_t rows_per_cta = KB >= TOKEN_ITEMS_PER_CTA ? 1 : TOKEN_ITEMS_PER_CTA / KB;
     const int64_t gx = (rpg + rows_per_cta - 1) / rows_per_cta;
-    DG_CHECK_SUPPORTED(gx < (1ll << 31) && groups < 65536, "too many rows or groups");
+    DG_CHECK_SUPPORTED(gx < (1ll << 31) && groups < 65536 && KB < (1ll << 30), "too many rows, groups or columns");
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(groups));
     auto s = static_cast<cudaStream_t>(stream);
     const auto* xp = static_cast<const uint16_t*>(x);

@@ -30,6 +30,39 @@ def test_per_token_codes_and_scales_bit_exact(fmt, M, K, scale):
         np.testing.assert_array_equal(got, oue)
 
 
+def every_bf16_magnitude_blocks(seed: int) -> torch.Tensor:
+    """One 128-value block per finite positive bf16 value v (subnormals included): one element is
+    +-v, the others are v * u (|u| < 1) truncated to bf16, so v is the block's amax.  Rows of 64
+    blocks; the last block repeats 1.0."""
+    vals = np.arange(1, 0x7F80, dtype=np.uint32)
+    vals = np.concatenate([vals, np.full((-vals.size) % 64, 0x3F80, np.uint32)])
+    n = vals.size
+    v = (vals << 16).view(np.float32)
+    rng = np.random.default_rng(seed)
+    blk = (v[:, None] * rng.uniform(-1.0, 1.0, (n, 128)).astype(np.float32)).astype(np.float32)
+    bits = (blk.view(np.uint32) >> 16).astype(np.uint16)
+    pos = (np.arange(n) * 37) % 128
+    bits[np.arange(n), pos] = vals.astype(np.uint16) | np.where(rng.random(n) < 0.5, 0x8000, 0).astype(np.uint16)
+    return torch.from_numpy(bits.view(np.int16).reshape(n // 64, 64 * 128)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+def test_per_token_every_bf16_magnitude_as_block_amax(fmt):
+    """Each finite bf16 magnitude is the amax of one block, so every scale (and its reciprocal)
+    the cast can form from bf16 input is checked against the oracle's IEEE arithmetic."""
+    x = every_bf16_magnitude_blocks(61)
+    M = x.shape[0]
+    q, sfa = gpu_quant_tokens(x.cuda(), fmt, sf_zero=0.25)
+    sync()
+    oq, osf, oue = oracle.quant_per_token_1x128(x, sf_zero=0.25, ue8m0=(fmt == DG_SF_UE8M0))
+    np.testing.assert_array_equal(q.cpu().numpy(), oq)
+    got = sfa_rows(sfa, M)
+    if fmt == DG_SF_FP32:
+        np.testing.assert_array_equal(got.view(np.uint32), osf.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(got, oue)
+
+
 def test_per_token_strided_input_and_row_counts():
     G, cap, K = 5, 40, 512
     x = wl.randn_bf16((G, cap, K + 64), 7)             # padded rows: ldx = K + 64
