@@ -341,7 +341,8 @@ class KGroupedWorkload:
 # ----------------------------------------------------------------------------- m-grouped workloads
 
 class MGroupedWorkload:
-    """Masked or contiguous m-grouped GEMM; a step = activation 1x128 cast + GEMM."""
+    """Masked or contiguous m-grouped GEMM; a step = activation 1x128 cast of the rows that carry
+    tokens (rows under each group's count; rows with m_indices >= 0) + GEMM."""
 
     def __init__(self, kind, device, ours=True):
         from moe_grouped_fp8_gb300 import workloads as wl
@@ -409,7 +410,7 @@ class MGroupedWorkload:
         if self.masked:
             self.api.dg_quant_per_token_1x128(self.a, self.qa, self.sfa, self.fmt, row_counts=self.counts)
         else:
-            self.api.dg_quant_per_token_1x128(self.a, self.qa, self.sfa, self.fmt)
+            self.api.dg_quant_per_token_1x128_routed(self.a, self.qa, self.sfa, self.mi, self.fmt)
 
     def gemm_only(self, r):
         w = self.w
@@ -438,9 +439,8 @@ class MGroupedWorkload:
 
     def cast_bytes(self):
         w = self.w
-        valid = int(np.clip(np.asarray(w.counts), 0, getattr(w, "cap", 1 << 30)).sum())
-        rows = valid if self.masked else self.M
-        return rows * w.K * 3 + rows * (w.K // 128) * 4
+        rows = int(np.clip(np.asarray(w.counts), 0, getattr(w, "cap", 1 << 30)).sum())  # routed rows only
+        return rows * w.K * 3 + rows * (w.K // 128) * (4 if self.fmt == 0 else 1)
 
     def e2e(self, steps, stream):
         return None

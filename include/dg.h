@@ -88,6 +88,19 @@ int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, u
                              int G, void* stream);
 
 /*
+ * The same 1x128 per-token cast over the rows of a contiguous m-grouped activation that are
+ * routed to an expert ([P3] m_grouped_fp8_fp4_gemm_nt_contiguous: rows whose m_indices entry is
+ * -1 are padding that the GEMM never writes).  Rows m < M with m_indices[m] >= 0 are cast
+ * exactly as by dg_quant_per_token_1x128; rows with m_indices[m] < 0 are neither read nor
+ * written (their codes and scales keep whatever the buffers held).
+ *   x, ldx, q, sfa, sf_format, sf_zero: as for dg_quant_per_token_1x128.
+ *   m_indices: int32 [M] device array, the contiguous GEMM's routing (only its sign is used).
+ */
+int dg_quant_per_token_1x128_routed(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                    void* sfa, int sf_format, float sf_zero,
+                                    const int32_t* m_indices, void* stream);
+
+/*
  * Per-channel cast over 128-token blocks with the per-expert K-major pack ([P1] repro:
  * `_per_channel_cast_to_fp8(x, gran_k=128, sf_val)` then `_pack_kmajor`).  For every
  * 128-token block tb inside sum(ks) and every column c: amax over the 128 tokens, then the

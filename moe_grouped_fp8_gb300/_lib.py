@@ -28,6 +28,7 @@ SIGNATURES = {
     "dg_last_error": (ctypes.c_char_p, []),
     "dg_workspace_size": (SZ, [I32, I32, I64, I64, I64]),
     "dg_quant_per_token_1x128": (I32, [P, I64, I64, I64, P, P, I32, F32, P, I32, P]),
+    "dg_quant_per_token_1x128_routed": (I32, [P, I64, I64, I64, P, P, I32, F32, P, P]),
     "dg_quant_per_channel_128": (I32, [P, I64, I64, P, I32, P, P, F32, P, P]),
     "dg_quant_per_channel_128_pair": (I32, [P, I64, P, P, P, I64, P, P, I64, P, I32, F32, P, P]),
     "dg_quant_block_128x128": (I32, [P, I32, I64, I64, P, P, I32, F32, P]),
@@ -48,6 +49,7 @@ TESTING_SIGNATURES = {
     "dg_testing_kgrouped_host_maps": (I32, [P, P, P, I32, I64, I64, P]),
     "dg_testing_kgrouped_gemm_only": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
     "dg_testing_mgrouped_kernel": (I32, [I32]),
+    "dg_testing_token_items_per_cta": (I32, [I32]),
 }
 
 _lock = threading.Lock()

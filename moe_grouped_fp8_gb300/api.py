@@ -14,7 +14,7 @@ import torch
 from ._lib import DG_OP_K_GROUPED_WGRAD, DG_OUT_BF16, DG_OUT_FP32, DG_SF_FP32, DGError, check, load
 
 __all__ = [
-    "dg_quant_per_token_1x128", "dg_quant_per_channel_128", "dg_quant_per_channel_128_pair",
+    "dg_quant_per_token_1x128", "dg_quant_per_token_1x128_routed", "dg_quant_per_channel_128", "dg_quant_per_channel_128_pair",
     "dg_quant_block_128x128",
     "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad",
     "dg_k_grouped_fp8_wgrad_noalloc",
@@ -67,20 +67,36 @@ def kgrouped_workspace(G: int, device) -> torch.Tensor:
     return torch.empty(dg_workspace_size(DG_OP_K_GROUPED_WGRAD, G), dtype=torch.uint8, device=device)
 
 
-def dg_quant_per_token_1x128(x, q, sfa, sf_format=DG_SF_FP32, sf_zero=1e-30, row_counts=None, stream=None):
-    """x bf16 [M, K] (row stride >= K) -> q e4m3/uint8 [M, K], sfa [K/128][Mp]."""
-    _dev(x, q, sfa, row_counts)
+def _token_cast_shapes(x, q, sfa, sf_format):
     _need(x.dim() == 2 and x.dtype == torch.bfloat16 and x.stride(1) == 1, "x must be a 2-D bf16 row-major view")
     M, K = x.shape
     _need(q.is_contiguous() and q.numel() == M * K and q.element_size() == 1, "q must be a contiguous 1-byte [M, K]")
     _need(sfa.is_contiguous() and sfa.dtype == _sf_dtype(sf_format)
           and sfa.numel() >= (K // 128) * sfa_padded_rows(M, sf_format), "sfa has the wrong dtype or size")
+    return M, K
+
+
+def dg_quant_per_token_1x128(x, q, sfa, sf_format=DG_SF_FP32, sf_zero=1e-30, row_counts=None, stream=None):
+    """x bf16 [M, K] (row stride >= K) -> q e4m3/uint8 [M, K], sfa [K/128][Mp]."""
+    _dev(x, q, sfa, row_counts)
+    M, K = _token_cast_shapes(x, q, sfa, sf_format)
     G = 0
     if row_counts is not None:
         _need(row_counts.dtype == torch.int32 and row_counts.is_contiguous(), "row_counts must be int32")
         G = row_counts.numel()
     check(load().dg_quant_per_token_1x128(_p(x), M, K, x.stride(0), _p(q), _p(sfa), sf_format, sf_zero,
                                           _p(row_counts), G, _s(stream)))
+
+
+def dg_quant_per_token_1x128_routed(x, q, sfa, m_indices, sf_format=DG_SF_FP32, sf_zero=1e-30, stream=None):
+    """dg_quant_per_token_1x128 over the rows with m_indices >= 0 only (int32 [M]); the other rows
+    of q and sfa are left as they were."""
+    _dev(x, q, sfa, m_indices)
+    M, K = _token_cast_shapes(x, q, sfa, sf_format)
+    _need(m_indices.dtype == torch.int32 and m_indices.is_contiguous() and m_indices.numel() == M,
+          "m_indices must be int32 [M]")
+    check(load().dg_quant_per_token_1x128_routed(_p(x), M, K, x.stride(0), _p(q), _p(sfa), sf_format, sf_zero,
+                                                 _p(m_indices), _s(stream)))
 
 
 def dg_quant_per_channel_128(x, ks, q_packed, sf, sf_zero=1e-30, status=None, stream=None, _fn="dg_quant_per_channel_128"):

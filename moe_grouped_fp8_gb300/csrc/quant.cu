@@ -7,6 +7,9 @@
 // casts): sf = amax / 448 in fp32; sf == 0 -> sf_zero; sf = max(sf, 1e-30); UE8M0 rounds sf up
 // to a power of two.  Codes: e4m3(x * (1/sf)), an IEEE fp32 reciprocal and product, then
 // round-to-nearest-even with saturation to +-448.
+#include <algorithm>
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -94,78 +97,81 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
 
 // ---------------------------------------------------------------------------------------
 // 1x128 per-token cast.  An item is one (row, 128-column block); a half-warp handles one item
-// (16 lanes x 8 bf16) and takes TOKEN_ITEMS_PER_HW items per pass so that several 16-byte loads
-// are in flight per thread.  CTA (x, y) owns rows [x*rows_per_cta, (x+1)*rows_per_cta) of row
-// group y and returns at once when they lie past the group's count, so padding rows of the
-// masked layout cost neither traffic nor work.
+// (16 lanes x 8 bf16) and a warp takes TOKEN_ITEMS_PER_HW items per half-warp per pass, so
+// several 16-byte loads are in flight per thread.  Item indices advance incrementally by the
+// items a pass covers (no division in the loop).  Three launch shapes share the item code:
+//   rows:    one CTA per chunk of rows_per_cta rows of one row group; it returns at once when
+//            the chunk lies past the group's count.  With several groups the group is the grid's
+//            x axis, so the chunks that hold rows (the first ones of every group) are dispatched
+//            first and the empty ones after them;
+//   routed:  CTA x owns rows_per_cta rows and compacts those whose m_indices entry is >= 0.
+// rows_per_cta gives each CTA about TOKEN_ITEMS_PER_CTA items.
 // ---------------------------------------------------------------------------------------
 constexpr int TOKEN_ITEMS_PER_HW = 4;
 constexpr int TOKEN_ITEMS_PER_CTA = 512;
+constexpr int TOKEN_MIN_ITEMS_PER_CTA = 128;
+constexpr int TOKEN_CTAS_PER_SM = 4;  // resident 256-thread CTAs at the kernels' register counts
+constexpr int TOKEN_PER_WARP = 2 * TOKEN_ITEMS_PER_HW;
 
+__device__ __forceinline__ uint4 token_load(const uint16_t* x, int64_t ldx, bool live, int64_t m, int kb, int sub) {
+    return live ? __ldg(reinterpret_cast<const uint4*>(x + m * ldx + static_cast<int64_t>(kb) * 128) + sub)
+                : make_uint4(0, 0, 0, 0);
+}
+
+// amax over the item (all 32 lanes take part in the shuffles), then codes and scale if live.
 template <bool UE8M0>
-__global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __restrict__ x, int64_t K, int64_t ldx,
-                                                           uint8_t* __restrict__ q, void* sfa, int64_t Mp,
-                                                           float sf_zero, const int32_t* __restrict__ row_counts,
-                                                           int64_t rpg, int64_t rows_per_cta) {
-    pdl_trigger();
-    pdl_wait();
-    const int64_t KB = K / 128;
-    const int64_t g = blockIdx.y;
-    int64_t lim = rpg;
-    if (row_counts != nullptr) {
-        lim = row_counts[g];
-        lim = lim < 0 ? 0 : (lim > rpg ? rpg : lim);
+__device__ __forceinline__ void token_item(const uint4& raw, bool live, int64_t m, int kb, int sub, int64_t K,
+                                           uint8_t* __restrict__ q, void* sfa, int64_t Mp, float sf_zero) {
+    float f[8];
+    bf16x8_to_float(raw, f);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (!live) return;
+    float sf, r;
+    uint8_t byte = 0;
+    block_scale<UE8M0>(amax, sf_zero, sf, r, byte);
+    *reinterpret_cast<uint2*>(q + m * K + static_cast<int64_t>(kb) * 128 + sub * 8) = e4m3x8(f, r);
+    if (sub == 0) {
+        if constexpr (UE8M0)
+            static_cast<uint8_t*>(sfa)[kb * Mp + m] = byte;
+        else
+            static_cast<float*>(sfa)[kb * Mp + m] = sf;
     }
-    const int64_t r_begin = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
-    if (r_begin >= lim) return;
-    const int64_t r_end = min(lim, r_begin + rows_per_cta);
-    const int64_t m_base = g * rpg + r_begin;
-    const int items = static_cast<int>((r_end - r_begin) * KB);
-    const int KBi = static_cast<int>(KB);
+}
+
+// The items of `nrows` rows of one CTA: row i is m_base + i, or m_base + s_rows[i] (LIST).
+template <bool UE8M0, bool LIST>
+__device__ __forceinline__ void token_rows(const uint16_t* __restrict__ x, int64_t K, int64_t ldx,
+                                           uint8_t* __restrict__ q, void* sfa, int64_t Mp, float sf_zero,
+                                           int64_t m_base, const int* s_rows, int nrows) {
+    const int KBi = static_cast<int>(K / 128);
+    const int items = nrows * KBi;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int hw = lane >> 4;   // half-warp
-    const int sub = lane & 15;  // 16-byte chunk within the 256-byte block
-    constexpr int PER_WARP = 2 * TOKEN_ITEMS_PER_HW;
-    const int step = (blockDim.x >> 5) * PER_WARP;  // items a CTA pass covers
+    const int hw = lane >> 4, sub = lane & 15;
+    const int step = (blockDim.x >> 5) * TOKEN_PER_WARP;
     const int step_m = step / KBi, step_kb = step - step_m * KBi;
-    // item it <-> (row m_base + mr, column block kb), advanced incrementally by `step`
     int it[TOKEN_ITEMS_PER_HW], mr[TOKEN_ITEMS_PER_HW], kb[TOKEN_ITEMS_PER_HW];
 #pragma unroll
     for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
-        it[j] = warp * PER_WARP + 2 * j + hw;
+        it[j] = warp * TOKEN_PER_WARP + 2 * j + hw;
         mr[j] = it[j] / KBi;
         kb[j] = it[j] - mr[j] * KBi;
     }
-    for (int base = warp * PER_WARP; base < items; base += step) {
+    for (int base = warp * TOKEN_PER_WARP; base < items; base += step) {
         uint4 raw[TOKEN_ITEMS_PER_HW];
+        int64_t m[TOKEN_ITEMS_PER_HW];
 #pragma unroll
         for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
-            const int64_t m = m_base + mr[j];
-            raw[j] = it[j] < items ? __ldg(reinterpret_cast<const uint4*>(x + m * ldx + kb[j] * 128) + sub)
-                                   : make_uint4(0, 0, 0, 0);
+            const bool live = it[j] < items;
+            m[j] = m_base + (LIST ? (live ? s_rows[mr[j]] : 0) : mr[j]);
+            raw[j] = token_load(x, ldx, live, m[j], kb[j], sub);
         }
 #pragma unroll
         for (int j = 0; j < TOKEN_ITEMS_PER_HW; ++j) {
-            float f[8];
-            bf16x8_to_float(raw[j], f);
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            if (it[j] < items) {
-                float sf, r;
-                uint8_t byte = 0;
-                block_scale<UE8M0>(amax, sf_zero, sf, r, byte);
-                const int64_t m = m_base + mr[j];
-                *reinterpret_cast<uint2*>(q + m * K + kb[j] * 128 + sub * 8) = e4m3x8(f, r);
-                if (sub == 0) {
-                    if constexpr (UE8M0)
-                        static_cast<uint8_t*>(sfa)[kb[j] * Mp + m] = byte;
-                    else
-                        static_cast<float*>(sfa)[kb[j] * Mp + m] = sf;
-                }
-            }
+            token_item<UE8M0>(raw[j], it[j] < items, m[j], kb[j], sub, K, q, sfa, Mp, sf_zero);
             it[j] += step;
             mr[j] += step_m;
             kb[j] += step_kb;
@@ -175,6 +181,47 @@ __global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __res
             }
         }
     }
+}
+
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __restrict__ x, int64_t K, int64_t ldx,
+                                                           uint8_t* __restrict__ q, void* sfa, int64_t Mp,
+                                                           float sf_zero, const int32_t* __restrict__ row_counts,
+                                                           int64_t rpg, int64_t rows_per_cta, int group_in_x) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t g = group_in_x ? blockIdx.x : blockIdx.y;
+    const int64_t chunk = group_in_x ? blockIdx.y : blockIdx.x;
+    int64_t lim = rpg;
+    if (row_counts != nullptr) {
+        lim = row_counts[g];
+        lim = lim < 0 ? 0 : (lim > rpg ? rpg : lim);
+    }
+    const int64_t r_begin = chunk * rows_per_cta;
+    if (r_begin >= lim) return;
+    const int64_t r_end = min(lim, r_begin + rows_per_cta);
+    token_rows<UE8M0, false>(x, K, ldx, q, sfa, Mp, sf_zero, g * rpg + r_begin, nullptr,
+                             static_cast<int>(r_end - r_begin));
+}
+
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) k_quant_token_routed(const uint16_t* __restrict__ x, int64_t K, int64_t ldx,
+                                                            uint8_t* __restrict__ q, void* sfa, int64_t Mp,
+                                                            float sf_zero, const int32_t* __restrict__ m_indices,
+                                                            int64_t M, int rows_per_cta) {
+    __shared__ int s_rows[256];
+    __shared__ int s_scan[8];
+    pdl_trigger();
+    pdl_wait();
+    const int64_t m_base = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
+    const int t = threadIdx.x;
+    const bool v = t < rows_per_cta && m_base + t < M && m_indices[m_base + t] >= 0;
+    int nrows = 0;
+    const int pos = cta_excl_scan<256>(v ? 1 : 0, s_scan, &nrows);
+    if (v) s_rows[pos] = t;
+    __syncthreads();
+    if (nrows == 0) return;
+    token_rows<UE8M0, true>(x, K, ldx, q, sfa, Mp, sf_zero, m_base, s_rows, nrows);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -406,36 +453,93 @@ __global__ void __launch_bounds__(256) k_quant_channel_128(const ChannelOperand 
 
 using namespace dg;
 
-extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, void* sfa,
-                                        int sf_format, float sf_zero, const int32_t* row_counts, int G,
-                                        void* stream) {
+namespace {
+
+int check_token_args(const void* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* q, const void* sfa,
+                     int sf_format) {
     DG_CHECK_ARG(M >= 0 && K > 0 && K % 128 == 0, "need M >= 0 and K a positive multiple of 128 (M=%lld K=%lld)",
                  (long long)M, (long long)K);
     DG_CHECK_ARG(ldx >= K && (ldx * 2) % 16 == 0, "ldx must be >= K and ldx*2 a multiple of 16 (ldx=%lld)",
                  (long long)ldx);
     DG_CHECK_ARG(sf_format == DG_SF_FP32 || sf_format == DG_SF_UE8M0, "bad sf_format %d", sf_format);
+    DG_CHECK_SUPPORTED(K / 128 < (1ll << 24), "K too large (K=%lld)", (long long)K);
     if (M == 0) return DG_OK;
     DG_CHECK_ARG(x && q && sfa, "null pointer argument");
     DG_CHECK_ARG(aligned16(x) && ((reinterpret_cast<uintptr_t>(q) & 7u) == 0), "x must be 16-byte and q 8-byte aligned");
+    return DG_OK;
+}
+
+int64_t token_mp(int64_t M, int sf_format) {
+    return (sf_format == DG_SF_FP32) ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
+}
+
+}  // namespace
+
+namespace {
+std::atomic<int> g_token_items{0};  // items per CTA of the per-token casts; 0 = TOKEN_ITEMS_PER_CTA
+
+// Rows per CTA.  Masked calls launch a CTA for every chunk up to the capacity, most of them
+// empty in decode, so their chunks stay large (TOKEN_ITEMS_PER_CTA items).  Otherwise the chunks
+// shrink (to 128 items at least) until the grid is about four waves of resident CTAs, which
+// trims the last partial wave on small inputs.
+int token_rows_per_cta(int64_t KB, int64_t rows, bool masked, int64_t cap_rows) {
+    int64_t want = g_token_items.load(std::memory_order_relaxed);
+    if (want <= 0) {
+        want = TOKEN_ITEMS_PER_CTA;
+        int sms = 0;
+        if (!masked && device_sm_count(&sms) == DG_OK && sms > 0) {
+            const int64_t waves = rows * KB / (4ll * TOKEN_CTAS_PER_SM * sms);
+            want = std::max<int64_t>(TOKEN_MIN_ITEMS_PER_CTA, std::min<int64_t>(want, waves));
+        }
+    }
+    const int64_t r = KB >= want ? 1 : want / KB;
+    return static_cast<int>(r < cap_rows ? r : cap_rows);
+}
+}  // namespace
+
+extern "C" int dg_testing_token_items_per_cta(int items) {
+    DG_CHECK_ARG(items >= 0 && items <= (1 << 20), "items per CTA out of range (%d)", items);
+    g_token_items.store(items, std::memory_order_relaxed);
+    return DG_OK;
+}
+
+extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, void* sfa,
+                                        int sf_format, float sf_zero, const int32_t* row_counts, int G,
+                                        void* stream) {
+    if (int rc = check_token_args(x, M, K, ldx, q, sfa, sf_format)) return rc;
+    if (M == 0) return DG_OK;
     int64_t rpg = M;
     if (row_counts != nullptr) {
         DG_CHECK_ARG(G >= 1 && M % G == 0, "row_counts needs G >= 1 dividing M (M=%lld G=%d)", (long long)M, G);
         rpg = M / G;
     }
-    const int64_t Mp = (sf_format == DG_SF_FP32) ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
     const int64_t groups = row_counts != nullptr ? G : 1;
-    const int64_t KB = K / 128;
-    const int64_t rows_per_cta = KB >= TOKEN_ITEMS_PER_CTA ? 1 : TOKEN_ITEMS_PER_CTA / KB;
-    const int64_t gx = (rpg + rows_per_cta - 1) / rows_per_cta;
-    DG_CHECK_SUPPORTED(gx < (1ll << 31) && groups < 65536 && KB < (1ll << 30), "too many rows, groups or columns");
-    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(groups));
-    auto s = static_cast<cudaStream_t>(stream);
-    const auto* xp = static_cast<const uint16_t*>(x);
-    if (sf_format == DG_SF_UE8M0)
-        return launch_pdl(k_quant_token_1x128<true>, grid, dim3(256), 0, s, xp, K, ldx, q, sfa, Mp, sf_zero,
-                          row_counts, rpg, rows_per_cta);
-    return launch_pdl(k_quant_token_1x128<false>, grid, dim3(256), 0, s, xp, K, ldx, q, sfa, Mp, sf_zero, row_counts,
-                      rpg, rows_per_cta);
+    const int64_t rows_per_cta = token_rows_per_cta(K / 128, M, row_counts != nullptr, 1ll << 30);
+    const int64_t chunks = (rpg + rows_per_cta - 1) / rows_per_cta;
+    // groups on x (fastest dispatch) when there are several and the chunks fit the y axis
+    const int group_in_x = groups > 1 && chunks < 65536 ? 1 : 0;
+    DG_CHECK_SUPPORTED(group_in_x || (chunks < (1ll << 31) && groups < 65536), "too many rows or groups");
+    const dim3 grid = group_in_x ? dim3(static_cast<unsigned>(groups), static_cast<unsigned>(chunks))
+                                 : dim3(static_cast<unsigned>(chunks), static_cast<unsigned>(groups));
+    const bool ue = sf_format == DG_SF_UE8M0;
+    return launch_pdl(ue ? k_quant_token_1x128<true> : k_quant_token_1x128<false>, grid, dim3(256), 0,
+                      static_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(x), K, ldx, q, sfa,
+                      token_mp(M, sf_format), sf_zero, row_counts, rpg, rows_per_cta, group_in_x);
+}
+
+extern "C" int dg_quant_per_token_1x128_routed(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                               void* sfa, int sf_format, float sf_zero, const int32_t* m_indices,
+                                               void* stream) {
+    if (int rc = check_token_args(x, M, K, ldx, q, sfa, sf_format)) return rc;
+    if (M == 0) return DG_OK;
+    DG_CHECK_ARG(m_indices != nullptr, "m_indices must not be NULL");
+    const int rows_per_cta = token_rows_per_cta(K / 128, M, false, 256);
+    const int64_t gx = (M + rows_per_cta - 1) / rows_per_cta;
+    DG_CHECK_SUPPORTED(gx < (1ll << 31), "too many rows");
+    const bool ue = sf_format == DG_SF_UE8M0;
+    return launch_pdl(ue ? k_quant_token_routed<true> : k_quant_token_routed<false>, dim3(static_cast<unsigned>(gx)),
+                      dim3(256), 0, static_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(x), K, ldx, q,
+                      sfa, token_mp(M, sf_format), sf_zero, m_indices, M, rows_per_cta);
 }
 
 extern "C" int dg_quant_block_128x128(const void* w, int G, int64_t N, int64_t K, uint8_t* q, void* sfb,

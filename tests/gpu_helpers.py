@@ -111,3 +111,9 @@ def set_mgrouped_kernel(which: str) -> None:
     CTA tiles, "pair" 256 x 192 CTA-pair tiles)."""
     lib = _lib.load()
     _lib.check(lib.dg_testing_mgrouped_kernel({"auto": 0, "single": 1, "pair": 2}[which]))
+
+
+def set_token_items_per_cta(items: int):
+    """Testing hook: items per CTA of the per-token casts (0 restores the automatic choice)."""
+    lib = _lib.load()
+    _lib.check(lib.dg_testing_token_items_per_cta(int(items)))

@@ -5,9 +5,10 @@ import torch
 
 import oracle
 from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_K_NOT_ALIGNED, DG_STATUS_K_OVERFLOW
+from moe_grouped_fp8_gb300 import api
 from moe_grouped_fp8_gb300 import workloads as wl
 
-from gpu_helpers import gpu_quant_blocks, gpu_quant_channels, gpu_quant_tokens, sfa_rows, sync
+from gpu_helpers import gpu_quant_blocks, gpu_quant_channels, gpu_quant_tokens, set_token_items_per_cta, sfa_rows, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +81,92 @@ def test_per_token_strided_input_and_row_counts():
     got = sfa_rows(sfa, G * cap)
     np.testing.assert_array_equal(got[live], osf[live])
     assert np.all(got[~live] == 0)
+
+
+def masked_cast_case(G, cap, K, counts, fmt, seed):
+    x = wl.randn_bf16((G, cap, K), seed)
+    counts = np.asarray(counts, np.int32)
+    q, sfa = gpu_quant_tokens(x.cuda().view(G * cap, K), fmt, row_counts=torch.tensor(counts, device="cuda"))
+    sync()
+    ue = fmt == DG_SF_UE8M0
+    oq, osf, oue = oracle.quant_per_token_1x128(x.view(G * cap, K), ue8m0=ue, row_counts=counts)
+    live = (np.arange(cap)[None, :] < np.clip(counts, 0, cap)[:, None]).reshape(-1)
+    qn = q.cpu().numpy()
+    np.testing.assert_array_equal(qn[live], oq[live])
+    assert np.all(qn[~live] == 0), "rows past the count must not be written"
+    got = sfa_rows(sfa, G * cap)
+    ref = oue if ue else osf
+    np.testing.assert_array_equal(got[live].view(np.uint8), ref[live].view(np.uint8))
+    assert np.all(got[~live] == 0)
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+@pytest.mark.parametrize("G,cap,K", [(300, 5, 384), (6, 1000, 2048), (1100, 2, 128), (1, 77, 7168)])
+def test_per_token_masked_groups(fmt, G, cap, K):
+    """Valid rows of many groups (one index space walked by resident CTAs, several passes for the
+    6 x 1000 case) and more groups than that walk takes (1100: one CTA row per group)."""
+    rng = np.random.default_rng(G * 7 + cap)
+    counts = rng.integers(-2, cap + 3, G)
+    counts[0] = 0
+    counts[-1] = cap
+    masked_cast_case(G, cap, K, counts, fmt, 500 + G)
+
+
+def routed_cast_case(counts, K, fmt, m_max=None, seed=3):
+    mi = wl.contiguous_m_indices(counts, m_max=m_max)
+    M = mi.size
+    x = wl.randn_bf16((M, K), seed, 2.0)
+    q = torch.full((M, K), 0xA5, dtype=torch.uint8, device="cuda")
+    sfa = api.empty_sfa(M, K, fmt, "cuda")
+    sfa.view(torch.uint8).fill_(0x5A)
+    api.dg_quant_per_token_1x128_routed(x.cuda(), q, sfa, torch.tensor(mi, device="cuda"), fmt, 0.5)
+    sync()
+    ue = fmt == DG_SF_UE8M0
+    oq, osf, oue = oracle.quant_per_token_1x128(x, sf_zero=0.5, ue8m0=ue)
+    live = mi >= 0
+    qn = q.cpu().numpy()
+    np.testing.assert_array_equal(qn[live], oq[live])
+    assert np.all(qn[~live] == 0xA5), "a padding row was written"
+    got = sfa_rows(sfa, M)
+    ref = oue if ue else osf
+    np.testing.assert_array_equal(got[live].view(np.uint8), ref[live].view(np.uint8))
+    assert np.all(got[~live].view(np.uint8) == 0x5A), "a padding row's scale was written"
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+@pytest.mark.parametrize("counts,K", [([130, 0, 1, 128, 257], 384), ([3, 300, 0, 0, 45], 7168),
+                                      ([1] * 40, 256), ([700], 65536)])
+def test_per_token_routed_skips_padding_rows(fmt, counts, K):
+    """Routed rows (m_indices >= 0) bit-exact against the oracle; padding rows inside expert
+    segments and past the last segment keep the buffers' previous bytes."""
+    routed_cast_case(counts, K, fmt, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
+
+
+@pytest.mark.parametrize("items", [1, 56, 64, 300, 5000])
+def test_per_token_any_chunk_size(items):
+    """The CTA chunk size (items per CTA) only changes the grid: plain, masked and routed casts
+    stay bit-exact for chunks of one item up to several rows."""
+    set_token_items_per_cta(items)
+    try:
+        x = wl.randn_bf16((301, 7168), 71, 0.5)
+        q, sfa = gpu_quant_tokens(x.cuda(), DG_SF_FP32)
+        sync()
+        oq, osf, _ = oracle.quant_per_token_1x128(x)
+        np.testing.assert_array_equal(q.cpu().numpy(), oq)
+        np.testing.assert_array_equal(sfa_rows(sfa, 301).view(np.uint32), osf.view(np.uint32))
+        masked_cast_case(7, 33, 384, [0, 33, 5, 40, 1, 17, 32], DG_SF_UE8M0, 72)
+        routed_cast_case([130, 0, 1, 128, 9], 256, DG_SF_FP32, m_max=700)
+    finally:
+        set_token_items_per_cta(0)
+
+
+def test_per_token_routed_all_padding_and_empty():
+    routed_cast_case([0, 0, 0], 256, DG_SF_FP32, m_max=300)
+    x = torch.zeros(0, 128, dtype=torch.bfloat16, device="cuda")
+    api.dg_quant_per_token_1x128_routed(x, torch.zeros(0, 128, dtype=torch.uint8, device="cuda"),
+                                        api.empty_sfa(0, 128, DG_SF_FP32, "cuda"),
+                                        torch.zeros(0, dtype=torch.int32, device="cuda"))
+    sync()
 
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
