@@ -35,10 +35,6 @@ __device__ __forceinline__ float ue8m0_round_up(float sf, uint8_t* byte) {
     return __uint_as_float(e << 23);
 }
 
-__device__ __forceinline__ uint8_t to_e4m3(float v, float r) {
-    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fmul_rn(v, r), __NV_SATFINITE, __NV_E4M3));
-}
-
 // The scale of a block and its reciprocal: bit-identical to scale_rule, ue8m0_round_up and
 // __frcp_rn, with fewer instructions on the common path.  When amax lies in [1e-27, FLT_MAX] the
 // clamps of scale_rule are inactive and the quotient is normal, so amax / 448 is formed by
@@ -264,21 +260,15 @@ __global__ void __launch_bounds__(256) k_quant_block_128x128(const uint16_t* __r
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_amax[i]);
 
-    float sf = scale_rule(amax, sf_zero);
+    float sf, r;
     uint8_t byte = 0;
-    if constexpr (UE8M0) sf = ue8m0_round_up(sf, &byte);
-    const float r = __frcp_rn(sf);
+    block_scale<UE8M0>(amax, sf_zero, sf, r, byte);
     uint8_t* qb = q + (g * N + nb * 128) * K + kb * 128;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         float f[8];
         bf16x8_to_float(raw[j], f);
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(to_e4m3(f[i], r)) << (8 * i);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(to_e4m3(f[4 + i], r)) << (8 * i);
-        *reinterpret_cast<uint2*>(qb + static_cast<int64_t>(r0 + 16 * j) * K + c * 8) = make_uint2(lo, hi);
+        *reinterpret_cast<uint2*>(qb + static_cast<int64_t>(r0 + 16 * j) * K + c * 8) = e4m3x8(f, r);
     }
     if (t == 0) {
         const int64_t si = (g * NB + nb) * KB + kb;
@@ -422,18 +412,22 @@ __global__ void __launch_bounds__(256) k_quant_channel_128(const ChannelOperand 
         float amax = s_part[0][t];
 #pragma unroll
         for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_part[w][t]);
-        const float sf = scale_rule(amax, sf_zero);
+        float sf, r;
+        uint8_t unused;
+        block_scale<false>(amax, sf_zero, sf, r, unused);
         sf_out[tb * C + c0 + t] = sf;
-        s_r[t] = __frcp_rn(sf);
+        s_r[t] = r;
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float r = s_r[c * 8 + i];
-        uint32_t word = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) word |= static_cast<uint32_t>(to_e4m3(f[j][i], r)) << (8 * j);
-        *reinterpret_cast<uint32_t*>(&s_t[(c * 8 + i) * CH_PITCH + rb]) = word;
+        float p[4];
+        fmul2(p[0], p[1], f[0][i], f[1][i], r);
+        fmul2(p[2], p[3], f[2][i], f[3][i], r);
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(p[0], p[1]), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(p[2], p[3]), __NV_SATFINITE, __NV_E4M3);
+        *reinterpret_cast<uint32_t*>(&s_t[(c * 8 + i) * CH_PITCH + rb]) = lo | (hi << 16);
     }
     __syncthreads();
     // column `col` of this CTA -> 128 consecutive bytes of row (c0 + col) of expert e's block

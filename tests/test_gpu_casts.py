@@ -31,20 +31,30 @@ def test_per_token_codes_and_scales_bit_exact(fmt, M, K, scale):
         np.testing.assert_array_equal(got, oue)
 
 
-def every_bf16_magnitude_blocks(seed: int) -> torch.Tensor:
-    """One 128-value block per finite positive bf16 value v (subnormals included): one element is
-    +-v, the others are v * u (|u| < 1) truncated to bf16, so v is the block's amax.  Rows of 64
-    blocks; the last block repeats 1.0."""
-    vals = np.arange(1, 0x7F80, dtype=np.uint32)
-    vals = np.concatenate([vals, np.full((-vals.size) % 64, 0x3F80, np.uint32)])
-    n = vals.size
-    v = (vals << 16).view(np.float32)
+FINITE_MAGNITUDES = np.arange(1, 0x7F80, dtype=np.uint32)  # every finite positive bf16, subnormals included
+
+
+def magnitude_blocks(mags: np.ndarray, size: int, seed: int) -> np.ndarray:
+    """bf16 bits [n, size]: block i holds +-mags[i] once and mags[i] * u (|u| < 1, truncated to
+    bf16) elsewhere, so mags[i] is its amax."""
+    n = mags.size
+    v = (mags.astype(np.uint32) << 16).view(np.float32)
     rng = np.random.default_rng(seed)
-    blk = (v[:, None] * rng.uniform(-1.0, 1.0, (n, 128)).astype(np.float32)).astype(np.float32)
+    blk = (v[:, None] * rng.uniform(-1.0, 1.0, (n, size)).astype(np.float32)).astype(np.float32)
     bits = (blk.view(np.uint32) >> 16).astype(np.uint16)
-    pos = (np.arange(n) * 37) % 128
-    bits[np.arange(n), pos] = vals.astype(np.uint16) | np.where(rng.random(n) < 0.5, 0x8000, 0).astype(np.uint16)
-    return torch.from_numpy(bits.view(np.int16).reshape(n // 64, 64 * 128)).view(torch.bfloat16)
+    pos = (np.arange(n) * 37) % size
+    bits[np.arange(n), pos] = mags.astype(np.uint16) | np.where(rng.random(n) < 0.5, 0x8000, 0).astype(np.uint16)
+    return bits
+
+
+def as_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def every_bf16_magnitude_blocks(seed: int) -> torch.Tensor:
+    """Rows of 64 1x128 blocks, one per finite bf16 magnitude (the last block repeats 1.0)."""
+    mags = np.concatenate([FINITE_MAGNITUDES, np.full((-FINITE_MAGNITUDES.size) % 64, 0x3F80, np.uint32)])
+    return as_bf16(magnitude_blocks(mags, 128, seed).reshape(mags.size // 64, 64 * 128))
 
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
@@ -81,6 +91,40 @@ def test_per_token_strided_input_and_row_counts():
     got = sfa_rows(sfa, G * cap)
     np.testing.assert_array_equal(got[live], osf[live])
     assert np.all(got[~live] == 0)
+
+
+def test_per_channel_every_bf16_magnitude_as_column_amax():
+    """Each finite bf16 magnitude is the amax of one (128-token block, column) pair of the
+    per-channel cast, over three experts; codes, pack and scales bit-exact."""
+    mags = np.concatenate([FINITE_MAGNITUDES, np.full(1, 0x3F80, np.uint32)])  # 32640 = 255 * 128
+    C, TB = 128, mags.size // 128
+    bits = magnitude_blocks(mags, 128, 62).reshape(TB, C, 128).transpose(0, 2, 1).reshape(TB * 128, C)
+    x = as_bf16(bits)
+    ks = [128 * 100, 128 * 100, 128 * 55]
+    qp, sf = gpu_quant_channels(x.cuda(), torch.tensor(ks, dtype=torch.int32, device="cuda"), 0.125)
+    sync()
+    oq, osf = oracle.quant_per_channel_128(x, 0.125)
+    np.testing.assert_array_equal(qp.cpu().numpy(), oracle.pack_kmajor(oq, ks))
+    np.testing.assert_array_equal(sf.cpu().numpy().view(np.uint32), osf.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+def test_block_sampled_bf16_magnitudes_as_block_amax(fmt):
+    """Every 16th finite bf16 magnitude plus the 32 smallest and largest as the amax of one
+    128x128 weight block each."""
+    mags = np.unique(np.concatenate([FINITE_MAGNITUDES[::16], FINITE_MAGNITUDES[:32], FINITE_MAGNITUDES[-32:]]))
+    mags = np.concatenate([mags, np.full((-mags.size) % 16, 0x3F80, np.uint32)])
+    NB, KB = mags.size // 16, 16
+    bits = magnitude_blocks(mags, 128 * 128, 63).reshape(NB, KB, 128, 128).transpose(0, 2, 1, 3)
+    w = as_bf16(bits.reshape(1, NB * 128, KB * 128))
+    q, sfb = gpu_quant_blocks(w.cuda(), fmt, sf_zero=4.0)
+    sync()
+    oq, osf, oue = oracle.quant_block_128x128(w, sf_zero=4.0, ue8m0=(fmt == DG_SF_UE8M0))
+    np.testing.assert_array_equal(q.cpu().numpy(), oq)
+    if fmt == DG_SF_FP32:
+        np.testing.assert_array_equal(sfb.cpu().numpy().view(np.uint32), osf.view(np.uint32))
+    else:
+        np.testing.assert_array_equal(sfb.cpu().numpy(), oue)
 
 
 def masked_cast_case(G, cap, K, counts, fmt, seed):
