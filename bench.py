@@ -167,13 +167,34 @@ def job_throughput(world_size: int, flops_per_step: float, ms_per_step: float) -
     return world_size * flops_per_step / (ms_per_step * 1e-3) / 1e12
 
 
+class StepGraphs:
+    """CUDA graphs of `per_graph` consecutive calls fn(r), r cycling through the R input sets
+    (as a training loop issues its steps back to back), plus one single-call graph per set for a
+    count that is not a multiple of per_graph."""
+
+    def __init__(self, fn, R, per_graph, stream):
+        self.R, self.L = R, max(1, per_graph)
+        self.single = [capture(lambda r=r: fn(r), stream) for r in range(R)]
+        self.multi = capture(lambda: [fn(i % R) for i in range(self.L)], stream) if self.L > 1 else None
+
+    def run(self, n):
+        """Issue exactly n calls."""
+        i = 0
+        if self.multi is not None:
+            while n - i >= self.L:
+                self.multi.replay()
+                i += self.L
+        while i < n:
+            self.single[i % self.R].replay()
+            i += 1
+
+
 def time_graphs(graphs, n, stream):
-    """Average ms per replay of n replays cycling through `graphs`, CUDA events on `stream`."""
+    """Average ms per call of n calls (StepGraphs), CUDA events on `stream`."""
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     s.record(stream)
-    for i in range(n):
-        graphs[i % len(graphs)].replay()
+    graphs.run(n)
     e.record(stream)
     e.synchronize()
     return s.elapsed_time(e) / n
@@ -335,7 +356,7 @@ class KGroupedWorkload:
         return {"workload": self.name, "experts": self.G, "tokens": self.T, "ks": self.w.ks, "N": self.N,
                 "H": self.H, "c_aliases_d": True, "input_sets": self.R,
                 "l2": f"{self.R} rotating input sets of {self.bytes_per_set() / 1e6:.0f} MB (> 2x the 129 MB L2)",
-                "graphs": "each step replayed from a CUDA graph"}
+}
 
 
 # ----------------------------------------------------------------------------- m-grouped workloads
@@ -461,7 +482,7 @@ class MGroupedWorkload:
         w = self.w
         c = {"workload": self.name, "experts": w.G, "N": w.N, "K": w.K, "valid_rows": w.valid_rows,
              "scales": "ue8m0" if self.fmt else "fp32", "l2": "weights exceed L2" if w.G * w.N * w.K > 2 * L2_BYTES
-             else "L2-resident (launch-latency-bound shape)", "graphs": "each step replayed from a CUDA graph"}
+             else "L2-resident (launch-latency-bound shape)"}
         if self.masked:
             c["capacity"] = w.cap
             c["expected_m"] = w.expected_m
@@ -555,7 +576,7 @@ class BF16GroupedWorkload:
         w = self.w
         c = {"workload": self.name, "experts": w.G, "N": w.N, "K": w.K, "valid_rows": w.valid_rows,
              "operands": "bf16", "l2": "weights exceed L2" if 2 * w.G * w.N * w.K > 2 * L2_BYTES
-             else "L2-resident (launch-latency-bound shape)", "graphs": "each step replayed from a CUDA graph"}
+             else "L2-resident (launch-latency-bound shape)"}
         if self.masked:
             c["capacity"] = w.cap
             c["expected_m"] = w.expected_m
@@ -587,14 +608,14 @@ def run_ours(args, ws, rank, local):
         for r in range(wk.R):          # eager warm-up of every input set
             wk.step(r)
         torch.cuda.synchronize()
-        step_graphs = [capture(lambda r=r: wk.step(r), stream) for r in range(wk.R)]
-        gemm_graphs = [capture(lambda r=r: wk.gemm_only(r), stream) for r in range(wk.R)]
+        L = args.steps_per_graph
+        step_graphs = StepGraphs(wk.step, wk.R, L, stream)
+        gemm_graphs = StepGraphs(wk.gemm_only, wk.R, L, stream)
         has_casts = getattr(wk, "has_casts", True)
-        cast_graphs = [capture(lambda r=r: wk.casts(r), stream) for r in range(wk.R)] if has_casts else []
+        cast_graphs = StepGraphs(wk.casts, wk.R, L, stream) if has_casts else None
         torch.cuda.synchronize()
 
-        for i in range(args.warmup):
-            step_graphs[i % wk.R].replay()
+        step_graphs.run(args.warmup)
         torch.cuda.synchronize()
 
         sampler = ClockSampler(local)
@@ -647,7 +668,9 @@ def run_ours(args, ws, rank, local):
             "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": getattr(wk, "dtype", "e4m3 (fp32 accumulate)"),
             "data": "synthetic (seeded randn, shapes of the source pages)",
-            "config": wk.config() | {"parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "config": wk.config() | {"parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                                     "graphs": f"{args.steps_per_graph} consecutive steps per CUDA graph replay "
+                                               "(input sets cycling within the graph)"},
             "roofline": roof,
             "breakdown_ms": {"casts": round(ms_cast, 5), "gemm_kernel": round(ms_gemm, 5),
                              "cast_gbs": round(wk.cast_bytes() / (ms_cast * 1e-3) / 1e9, 1) if ms_cast > 0 else None},
@@ -729,6 +752,9 @@ def main():
                          "many_expert_{w13,w2}_E{1,32,113} | masked_decode_g8 | contiguous_prefill_g8 "
                          "(the last two: 8-expert cases for profiler captures) | "
                          "{masked_repro,masked_decode,contiguous_prefill}_bf16 (BF16 grouped GEMM)")
+    ap.add_argument("--steps-per-graph", type=int, default=8,
+                    help="consecutive steps captured in one CUDA graph (the timed region still runs exactly "
+                         "--steps steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
