@@ -38,8 +38,9 @@ namespace dg {
 
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
-constexpr int NUM_THREADS = 320;
+constexpr int MMA_WARP = 9;     // and MMA_WARP + 1: the two MMA issuers
+constexpr int NUM_MMA_WARPS = 2;
+constexpr int NUM_THREADS = 352;
 constexpr int EPI_BAR = 1;  // named barrier of the 256 promotion/store threads
 
 
@@ -210,17 +211,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == MMA_WARP) {
+    } else if (warp >= MMA_WARP && warp < MMA_WARP + NUM_MMA_WARPS) {
+        // Two issuers take alternate 128-K blocks (global block number n of this CTA): an issue
+        // blocks until the tensor core has taken the MMAs, so while one issuer is blocked the
+        // other has already passed its barrier waits and queues its block at once.  A commit
+        // tracks only its own thread's MMAs, so each issuer signals its own blocks' barriers.
+        const uint32_t me = static_cast<uint32_t>(warp - MMA_WARP);
         if (lane == 0 && R > 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int tb = 0;
-            uint32_t tphase = 0;
             bool ok = true, any = false;
+            int last_tb = 0;
+            uint32_t last_tphase = 0;
+            uint32_t n = 0;
             constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile<L>(t, rt, R, a);
-                for (int kb = 0; kb < ti.kbt; ++kb) {
+                for (int kb = 0; kb < ti.kbt; ++kb, ++n) {
+                    if (n % NUM_MMA_WARPS != me) continue;
+                    const int stage = static_cast<int>(n % STAGES);
+                    const uint32_t phase = (n / STAGES) & 1u;
+                    const int tb = static_cast<int>(n % P::TB);
+                    const uint32_t tphase = (n / P::TB) & 1u;
+                    // Order matters.  With an odd stage count a stage's consecutive uses alternate
+                    // between the issuers, and a parity wait cannot tell phase k from k + 2, so
+                    // the full wait of block n is sound only once block n - STAGES has taken its
+                    // phase.  Waiting for the TMEM buffer first ensures that: it comes back after
+                    // the promotion of block n - TB, which runs after block n - TB - 1 >= n - STAGES
+                    // (TB <= STAGES - 1) was promoted, hence after its MMA consumed the stage.
+                    // (Each TMEM buffer belongs to one issuer, which consumes its phases in order.)
+                    static_assert(STAGES % NUM_MMA_WARPS == 0 || P::TB <= STAGES - 1, "stage phase order");
+                    static_assert(P::TB % NUM_MMA_WARPS == 0, "one issuer per TMEM buffer");
                     if (!mbar_wait(&tempty[tb], tphase ^ 1u, wc)) { ok = false; break; }
                     if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
@@ -233,17 +252,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     umma_commit(&empty[stage]);
                     umma_commit(&tfull[tb]);
                     any = true;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    if (++tb == P::TB) { tb = 0; tphase ^= 1u; }
+                    last_tb = tb;
+                    last_tphase = tphase;
                 }
             }
-            if (any) {
-                // the last commit: wait until the tensor core is done with every MMA issued
-                int lt = tb - 1;
-                uint32_t lp = tphase;
-                if (lt < 0) { lt = P::TB - 1; lp ^= 1u; }
-                drain_wait(&tfull[lt], lp, a.wait_limit_ns);
-            }
+            // this issuer's last commit: the tensor core is done with every MMA it issued
+            if (any) drain_wait(&tfull[last_tb], last_tphase, a.wait_limit_ns);
         }
         __syncwarp();
     } else {
