@@ -40,7 +40,10 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;     // and MMA_WARP + 1: the two MMA issuers
 constexpr int NUM_MMA_WARPS = 2;
-constexpr int NUM_THREADS = 352;
+constexpr int STORE_WARP = 11;  // with SEP_STORE: issues the TMA stores of staged tiles
+// Threads of a CTA: 8 promotion warps, the producer, two MMA issuers (+ the store warp).
+template <bool SEP_STORE>
+__host__ __device__ constexpr int num_threads() { return SEP_STORE ? 384 : 352; }
 constexpr int EPI_BAR = 1;  // named barrier of the 256 promotion/store threads
 
 
@@ -63,7 +66,7 @@ struct Plan {
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
     static constexpr int BAR_OFF = (SCHED_OFF + SCHED_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * TB;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * TB + 2;  // + staged, staging free
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int MISC_BYTES = 256;
     static constexpr int TOTAL = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
@@ -114,14 +117,29 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const RunTable& rt, int R
     return ti;
 }
 
+// Valid rows at the start of a tile: the count for masked / psum tiles, else the leading rows
+// whose m_indices entry is the tile's expert (ballots of the four 32-row quarters).
+template <Layout L>
+__device__ __forceinline__ int stored_rows(const TileInfo& ti, const GemmArgs& a, const uint32_t* ballot) {
+    if (L == Layout::Masked || a.psum) return ti.valid;
+    int v = 0;
+    for (int qq = 0; qq < 4; ++qq) {
+        const uint32_t bal = ballot[qq];
+        if (bal == 0xffffffffu) { v += 32; continue; }
+        return v + __ffs(~bal) - 1;
+    }
+    return v;
+}
+
 // ------------------------------------------------------------------------- the kernel
 
-template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, bool SEP_STORE>
+__global__ void __launch_bounds__(num_threads<SEP_STORE>(), 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD8,
                    const GemmArgs a) {
     using P = Plan<L, BN, STAGES, OUT_FP32>;
+    constexpr int NUM_THREADS = num_threads<SEP_STORE>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -134,6 +152,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + P::TB;
+    uint64_t* staged = tempty + P::TB;    // the promotion warps have written a tile's staging
+    uint64_t* stg_free = staged + 1;      // the store warp's TMA stores have read it
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + P::MISC_OFF + 4);
     int* s_ntiles = reinterpret_cast<int*>(smem + P::MISC_OFF + 12);
@@ -154,6 +174,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], NUM_EPI_WARPS);
         }
+        mbar_init(staged, 1);
+        mbar_init(stg_free, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -177,6 +199,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int num_tiles = tile_prefix<NUM_THREADS, 1>(R, a.num_nb, rt, s_scan, s_ntiles);
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
+
+    // TMA stores of a staged tile: the leading v8 valid rows (a multiple of 8)
+    auto issue_stores = [&](const TileInfo& ti, int v8) {
+        for (int c = 0; c < P::CHUNKS; ++c) {
+            const uint8_t* src = stg + c * P::CHUNK_BYTES;
+            const int x = ti.nb * BN + c * (128 / P::ESIZE);
+            if (v8 == BM) {
+                if constexpr (L == Layout::Contiguous) tma_store_2d(&tmD, src, x, ti.row0);
+                else tma_store_3d(&tmD, src, x, ti.row0, ti.e);
+            } else {
+                for (int r8 = 0; r8 < v8; r8 += 8) {
+                    if constexpr (L == Layout::Contiguous)
+                        tma_store_2d(&tmD8, src + r8 * 128, x, ti.row0 + r8);
+                    else
+                        tma_store_3d(&tmD8, src + r8 * 128, x, ti.row0 + r8, ti.e);
+                }
+            }
+        }
+        bulk_commit();
+    };
 
     // ---------------------------------------------------------------- roles
     if (warp == PRODUCER_WARP) {
@@ -260,16 +302,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (any) drain_wait(&tfull[last_tb], last_tphase, a.wait_limit_ns);
         }
         __syncwarp();
+    } else if (SEP_STORE && warp == STORE_WARP) {
+        // ------------------------------------------------------------ tile stores
+        // The promotion warps stage a tile and move on; this thread stores it (TMA for the leading
+        // 8-row-aligned valid rows) and hands the staging back once the stores have read it.
+        if (lane == 0 && R > 0) {
+            bool any = false;
+            int tix = 0;
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tix) {
+                const TileInfo ti = decode_tile<L>(t, rt, R, a);
+                if (!mbar_wait(staged, static_cast<uint32_t>(tix & 1), wc)) break;
+                const int v8 = stored_rows<L>(ti, a, s_ballot + (tix & 1) * 4) & ~7;
+                if (v8 > 0) {
+                    issue_stores(ti, v8);
+                    any = true;
+                }
+                bulk_wait_read_all();
+                mbar_arrive(stg_free);
+            }
+            if (any) bulk_wait_all();
+        }
+        __syncwarp();
     } else {
-        // ------------------------------------------------------------ promotion + store
+        // ------------------------------------------------------------ promotion + staging
         const int q = warp & 3;       // TMEM lane quarter
         const int h2 = warp >> 2;     // column half
         const int row = q * 32 + lane;
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         int tb = 0;
         uint32_t tphase = 0;
-        bool have_store = false;
         int parity_slot = 0;
+        int tix = 0;  // this CTA's tile count so far
+        bool have_store = false;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const TileInfo ti = decode_tile<L>(t, rt, R, a);
             bool failed = false;
@@ -381,8 +445,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 load_group(kb0 / P::SFG + 2, sa_n, sb_n);
             }
 
-            // ---- stage the tile in shared memory
-            if (tid == 0 && have_store) bulk_wait_read_all();  // the previous store has read the staging
+            // ---- stage the tile in shared memory once the previous tile's stores have read it
+            if (tid == 0 && tix > 0) {
+                if constexpr (SEP_STORE) {
+                    if (!mbar_wait(stg_free, static_cast<uint32_t>((tix - 1) & 1), wc)) failed = true;
+                } else {
+                    bulk_wait_read_all();
+                }
+            }
             named_bar_sync(EPI_BAR, NUM_EPI_WARPS * 32);
             if (!failed) {
                 constexpr int PIECES = P::CPT * P::ESIZE / 16;
@@ -408,38 +478,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_async_smem();
             if (bar_or(EPI_BAR, NUM_EPI_WARPS * 32, failed || *s_abort != 0)) break;
 
-            // ---- store: TMA for the leading 8-row-aligned valid rows, owner threads for the rest
-            int v = BM;
-            if (L == Layout::Masked || a.psum) {
-                v = ti.valid;
-            } else {
-                v = 0;
-                for (int qq = 0; qq < 4; ++qq) {
-                    const uint32_t bal = s_ballot[parity_slot * 4 + qq];
-                    if (bal == 0xffffffffu) { v += 32; continue; }
-                    v += __ffs(~bal) - 1;
-                    break;
-                }
-            }
-            const int v8 = v & ~7;
+            // ---- stores: TMA for the leading 8-row-aligned valid rows (by the store warp, or here
+            // by thread 0), owner threads for the rest
+            const int v8 = stored_rows<L>(ti, a, s_ballot + parity_slot * 4) & ~7;
             if (tid == 0) {
-                if (v8 > 0) {
-                    for (int c = 0; c < P::CHUNKS; ++c) {
-                        const uint8_t* src = stg + c * P::CHUNK_BYTES;
-                        const int x = ti.nb * BN + c * (128 / P::ESIZE);
-                        if (v8 == BM) {
-                            if constexpr (L == Layout::Contiguous) tma_store_2d(&tmD, src, x, ti.row0);
-                            else tma_store_3d(&tmD, src, x, ti.row0, ti.e);
-                        } else {
-                            for (int r8 = 0; r8 < v8; r8 += 8) {
-                                if constexpr (L == Layout::Contiguous)
-                                    tma_store_2d(&tmD8, src + r8 * 128, x, ti.row0 + r8);
-                                else
-                                    tma_store_3d(&tmD8, src + r8 * 128, x, ti.row0 + r8, ti.e);
-                            }
-                        }
-                    }
-                    bulk_commit();
+                if constexpr (SEP_STORE) {
+                    mbar_arrive(staged);
+                } else if (v8 > 0) {
+                    issue_stores(ti, v8);
                     have_store = true;
                 }
             }
@@ -465,8 +511,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
             }
             parity_slot ^= 1;
+            ++tix;
         }
-        if (tid == 0 && have_store) bulk_wait_all();
+        if (!SEP_STORE && tid == 0 && have_store) bulk_wait_all();
         __syncwarp();
     }
 
@@ -481,16 +528,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 namespace {
 
+// Tile stores.  With few 128-K blocks per tile the tile transitions dominate, and a separate
+// store warp lets the promotion warps stage a tile and move straight on (w2 of the many-expert
+// shape, K = 256: 0.160 -> 0.136 ms); with long K thread 0 issuing the stores itself measured
+// ~3% faster (the extra warp costs the promotion loop registers / issue slots).  Both paths store
+// the same staged bytes.
+constexpr int SEP_STORE_MAX_KB = 32;
+std::atomic<int> g_force_store{0};  // 0 automatic, 1 thread 0 of the promotion warps, 2 store warp
+
+bool use_sep_store(int KB) {
+    const int f = g_force_store.load(std::memory_order_relaxed);
+    return f == 0 ? KB <= SEP_STORE_MAX_KB : f == 2;
+}
+
 template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0>
 int launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
                 const GemmArgs& args, cudaStream_t stream) {
     using P = Plan<L, BN, STAGES, OUT_FP32>;
-    auto kern = k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0>;
+    const bool sep = use_sep_store(args.KB);
+    auto kern = sep ? k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0, true>
+                    : k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0, false>;
     // The attribute is per device: set it on every call (cheap, host-only, capture-safe).
     DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL));
     int sms = 0;
     if (int rc = device_sm_count(&sms)) return rc;
-    return launch_pdl(kern, dim3(sms), dim3(NUM_THREADS), P::TOTAL, stream, tA, tB, tD, tD8, args);
+    return launch_pdl(kern, dim3(sms), dim3(sep ? num_threads<true>() : num_threads<false>()), P::TOTAL, stream,
+                      tA, tB, tD, tD8, args);
 }
 
 constexpr int MG_BN = 128;
@@ -712,6 +775,12 @@ extern "C" int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sf
 // ------------------------------------------------------------------------- test hook
 // Selects the m-grouped kernel of later bf16-output calls in this process: 0 automatic,
 // 1 single-CTA 128 x 128 tiles, 2 CTA pairs.  Lets the tests hold both kernels to the oracle.
+extern "C" int dg_testing_mgrouped_store(int which) {
+    DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0 (automatic), 1 (thread 0) or 2 (store warp)");
+    g_force_store.store(which, std::memory_order_relaxed);
+    return DG_OK;
+}
+
 extern "C" int dg_testing_mgrouped_kernel(int which) {
     DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0, 1 or 2");
     g_force_kernel.store(which, std::memory_order_relaxed);

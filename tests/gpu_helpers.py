@@ -117,3 +117,10 @@ def set_token_items_per_cta(items: int):
     """Testing hook: items per CTA of the per-token casts (0 restores the automatic choice)."""
     lib = _lib.load()
     _lib.check(lib.dg_testing_token_items_per_cta(int(items)))
+
+
+def set_mgrouped_store(which: str) -> None:
+    """Test hook: who issues the tile stores of the single-CTA m-grouped kernel ("auto", "thread0"
+    of the promotion warps, or a separate "warp")."""
+    lib = _lib.load()
+    _lib.check(lib.dg_testing_mgrouped_store({"auto": 0, "thread0": 1, "warp": 2}[which]))

@@ -9,7 +9,7 @@ from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_BAD_INDEX, 
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
-                         sentinel_value, set_mgrouped_kernel, sync, to_f64)
+                         sentinel_value, set_mgrouped_kernel, set_mgrouped_store, sync, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -104,6 +104,26 @@ def test_pair_tiles_odd_runs_and_column_tail():
     a = wl.randn_bf16((mi.size, 256), 95)
     b = wl.randn_bf16((5, 640, 256), 96, 0.05)
     contiguous_case(a, b, mi)
+
+
+@pytest.mark.parametrize("N", [512, 1024])
+def test_store_paths_bitwise_equal(mgrouped_kernel, N):
+    """Both store paths on ragged m_indices segments (store extent from the row ballots)."""
+    if mgrouped_kernel == "pair":
+        pytest.skip("the store paths belong to the single-CTA kernel")
+    counts = [130, 0, 1, 128, 257, 9]
+    mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
+    a = wl.randn_bf16((mi.size, 384), 61, 1.5)
+    b = wl.randn_bf16((len(counts), N, 384), 62, 0.02)
+    outs = []
+    try:
+        for which in ("thread0", "warp"):
+            set_mgrouped_store(which)
+            d, _ = contiguous_case(a, b, mi, calls=2)
+            outs.append(out_bits(d))
+    finally:
+        set_mgrouped_store("auto")
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_segments_out_of_expert_order():

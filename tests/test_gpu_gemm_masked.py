@@ -9,7 +9,7 @@ from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_COUNT_GT_CA
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
-                         sentinel_value, set_mgrouped_kernel, sync, to_f64)
+                         sentinel_value, set_mgrouped_kernel, set_mgrouped_store, sync, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -144,6 +144,27 @@ def test_single_and_pair_kernels_bitwise_equal(mgrouped_kernel, fmt):
         set_mgrouped_kernel(which)
         d, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
         outs.append(out_bits(d))
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("N,out", [(512, torch.bfloat16), (1024, torch.bfloat16), (384, torch.float32)])
+def test_store_paths_bitwise_equal(mgrouped_kernel, N, out):
+    """Tile stores issued by thread 0 of the promotion warps or by a separate store warp: each
+    passes the oracle check (valid rows, untouched padding rows) and both give the same bits,
+    on 128- and 256-column tiles, with partial tiles that need owner-thread tails."""
+    if mgrouped_kernel == "pair":
+        pytest.skip("the store paths belong to the single-CTA kernel")
+    G, cap, K = 3, 300, 512
+    a = wl.randn_bf16((G, cap, K), 17, 1.5)
+    b = wl.randn_bf16((G, N, K), 18, 0.02)
+    outs = []
+    try:
+        for which in ("thread0", "warp"):
+            set_mgrouped_store(which)
+            d, _ = masked_case(a, b, [300, 77, 133], out=out, calls=2)
+            outs.append(out_bits(d))
+    finally:
+        set_mgrouped_store("auto")
     assert np.array_equal(outs[0], outs[1])
 
 
