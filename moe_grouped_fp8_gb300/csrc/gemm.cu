@@ -567,8 +567,14 @@ constexpr int MG_STAGES_WIDE = 3;    // 48 KB stages
 // through shared memory; measured 0.408 -> 0.329 ms on the prefill shape, 0.478 -> 0.419 ms on
 // decode), else 128 (narrow N: twice the tiles for the same weights, measured faster at N = 512).
 // Both tile widths give bitwise the same results.
+std::atomic<int> g_force_bn{0};  // testing: 0 automatic, else the tile width (128, or 256 when allowed)
+
 int single_bn(int out, int64_t N) {
-    return (out == DG_OUT_BF16 && N % MG_BN_WIDE == 0 && N >= 4 * MG_BN_WIDE) ? MG_BN_WIDE : MG_BN;
+    const bool wide_ok = out == DG_OUT_BF16 && N % MG_BN_WIDE == 0;
+    const int f = g_force_bn.load(std::memory_order_relaxed);
+    if (f == MG_BN) return MG_BN;
+    if (f == MG_BN_WIDE && wide_ok) return MG_BN_WIDE;
+    return (wide_ok && N >= 4 * MG_BN_WIDE) ? MG_BN_WIDE : MG_BN;
 }
 
 CUtensorMapDataType out_tmap_type(int out) {
@@ -775,6 +781,12 @@ extern "C" int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sf
 // ------------------------------------------------------------------------- test hook
 // Selects the m-grouped kernel of later bf16-output calls in this process: 0 automatic,
 // 1 single-CTA 128 x 128 tiles, 2 CTA pairs.  Lets the tests hold both kernels to the oracle.
+extern "C" int dg_testing_mgrouped_bn(int bn) {
+    DG_CHECK_ARG(bn == 0 || bn == MG_BN || bn == MG_BN_WIDE, "bn must be 0, %d or %d", MG_BN, MG_BN_WIDE);
+    g_force_bn.store(bn, std::memory_order_relaxed);
+    return DG_OK;
+}
+
 extern "C" int dg_testing_mgrouped_store(int which) {
     DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0 (automatic), 1 (thread 0) or 2 (store warp)");
     g_force_store.store(which, std::memory_order_relaxed);

@@ -124,3 +124,9 @@ def set_mgrouped_store(which: str) -> None:
     of the promotion warps, or a separate "warp")."""
     lib = _lib.load()
     _lib.check(lib.dg_testing_mgrouped_store({"auto": 0, "thread0": 1, "warp": 2}[which]))
+
+
+def set_mgrouped_bn(bn: int) -> None:
+    """Test hook: the single-CTA tile width (0 automatic, 128, or 256 where N allows)."""
+    lib = _lib.load()
+    _lib.check(lib.dg_testing_mgrouped_bn(int(bn)))

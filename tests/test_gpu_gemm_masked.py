@@ -9,7 +9,8 @@ from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_COUNT_GT_CA
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
-                         sentinel_value, set_mgrouped_kernel, set_mgrouped_store, sync, to_f64)
+                         sentinel_value, set_mgrouped_bn, set_mgrouped_kernel, set_mgrouped_store, sync,
+                         to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -112,6 +113,25 @@ def test_wide_tiles(fmt):
     d2, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
     set_mgrouped_kernel("auto")
     assert np.array_equal(out_bits(d), out_bits(d2))
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+def test_tile_widths_bitwise_equal(mgrouped_kernel, fmt):
+    """The same call on 128- and 256-column tiles: both pass the oracle check, same bits."""
+    if mgrouped_kernel == "pair":
+        pytest.skip("tile widths belong to the single-CTA kernel")
+    G, cap, N, K = 3, 260, 512, 640
+    a = wl.randn_bf16((G, cap, K), 19, 2.0)
+    b = wl.randn_bf16((G, N, K), 20, 0.02)
+    outs = []
+    try:
+        for bn in (128, 256):
+            set_mgrouped_bn(bn)
+            d, _ = masked_case(a, b, [260, 9, 131], fmt=fmt)
+            outs.append(out_bits(d))
+    finally:
+        set_mgrouped_bn(0)
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_single_expert_and_all_empty():
