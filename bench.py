@@ -617,11 +617,86 @@ class BF16GroupedWorkload:
 
 # ----------------------------------------------------------------------------- arms
 
+class DenseWorkload:
+    """Plain FP8 GEMM (one expert owning every row): a step = the activation 1x128 cast + GEMM.
+    dense_prefill: M=8192 tokens, N=4096, K=7168 (one expert of the prefill shape, dense)."""
+    kernel_name = "k_grouped_gemm"
+    launches_per_step = 2
+    SHAPES = {"dense_prefill": (8192, 4096, 7168)}
+
+    def __init__(self, kind, device, ours=True):
+        from moe_grouped_fp8_gb300 import workloads as wl
+        if kind not in self.SHAPES:
+            raise SystemExit(f"unknown workload {kind}")
+        self.M, self.N, self.K = self.SHAPES[kind]
+        M, N, K = self.M, self.N, self.K
+        self.name = f"{kind}_M{M}_N{N}_K{K}"
+        self.R = 1
+        a = wl.randn_bf16((M, K), 2001, 1.0, device)
+        b = wl.randn_bf16((1, N, K), 2002, 0.02, device)
+        self.a_rows = a[:4].cpu()
+        self.b_block = b[0, :128].cpu()
+        if not ours:
+            return
+        from moe_grouped_fp8_gb300 import api
+        self.api = api
+        self.a = a
+        self.qa = torch.empty(M, K, dtype=torch.uint8, device=device)
+        self.sfa = api.empty_sfa(M, K, 0, device)
+        self.qb = torch.empty(1, N, K, dtype=torch.uint8, device=device)
+        self.sfb = torch.empty(1, N // 128, K // 128, dtype=torch.float32, device=device)
+        api.dg_quant_block_128x128(b, self.qb, self.sfb, 0)
+        del b
+        self.d = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+
+    @property
+    def flops(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def casts(self, r):
+        self.api.dg_quant_per_token_1x128(self.a, self.qa, self.sfa, 0)
+
+    def gemm_only(self, r):
+        self.api.dg_fp8_gemm_nt(self.qa, self.sfa, self.qb.view(self.N, self.K),
+                                self.sfb.view(self.N // 128, self.K // 128), self.d)
+
+    wgrad = gemm_only
+
+    def step(self, r):
+        self.casts(r)
+        self.gemm_only(r)
+
+    def gemm_bytes(self):
+        M, N, K = self.M, self.N, self.K
+        return N * K + M * K + M * (K // 128) * 4 + (N // 128) * (K // 128) * 4 + M * N * 2
+
+    def cast_bytes(self):
+        return self.M * self.K * 3 + self.M * (self.K // 128) * 4
+
+    def e2e(self, steps, stream):
+        return None
+
+    def oracle_step(self, channels=None):
+        """Oracle on a bounded sample: 4 rows x the first 128 output columns."""
+        import oracle
+        t0 = time.perf_counter()
+        qa, sa, _ = oracle.quant_per_token_1x128(self.a_rows)
+        qb, sb, _ = oracle.quant_block_128x128(self.b_block.unsqueeze(0))
+        oracle.gemm_batched(qa[None], sa[None], qb, sb)
+        return time.perf_counter() - t0, 2.0 * 4 * 128 * self.K
+
+    def config(self):
+        return {"workload": self.name, "M": self.M, "N": self.N, "K": self.K, "scales": "fp32",
+                "l2": "weights 29 MB, activations 59 MB: the A and D streams exceed L2"}
+
+
 def make_workload(kind, device, ours=True):
     if kind == "kgrouped_wgrad":
         return KGroupedWorkload(device, sets=None if ours else 1, ours=ours)
     if kind.endswith("_bf16"):
         return BF16GroupedWorkload(kind, device, ours=ours)
+    if kind.startswith("dense_"):
+        return DenseWorkload(kind, device, ours=ours)
     return MGroupedWorkload(kind, device, ours=ours)
 
 
@@ -780,7 +855,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="kgrouped_wgrad",
                     help="kgrouped_wgrad | masked_decode | masked_repro | contiguous_prefill | "
-                         "many_expert_{w13,w2}_E{1,32,113} | masked_decode_g8 | contiguous_prefill_g8 "
+                         "many_expert_{w13,w2}_E{1,32,113} | masked_decode_g8 | contiguous_prefill_g8 | dense_prefill "
                          "(the last two: 8-expert cases for profiler captures) | "
                          "{masked_repro,masked_decode,contiguous_prefill}_bf16 (BF16 grouped GEMM)")
     ap.add_argument("--steps-per-graph", type=int, default=8,

@@ -190,6 +190,32 @@ int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const uint8_t* b,
                             size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * Plain FP8 GEMM with the same scaling ([P2] validation: the adjacent-path checks of ordinary
+ * GEMM layouts, output dtypes and accumulation, and batched GEMM):
+ *   D[m, n] = C[m, n] + sum_k A[m, k] sfa[k/128, m] * B[n, k] sfb[n/128, k/128]
+ * for m < M (C omitted when c is NULL).
+ *   a: e4m3 [M, K] row-major.  sfa: [K/128][Mp] per-token scales ("Scale-factor layouts").
+ *   b: e4m3 [N, K] row-major.  sfb: [N/128][K/128] (the [G][N/128][K/128] layout with G = 1).
+ *   c: optional fp32 [M, N]; needs out_dtype DG_OUT_FP32; may equal d (in-place accumulate).
+ *   d: [M, N] bf16 or fp32 (out_dtype).  M >= 0 (0: nothing enqueued), M <= 524288.
+ * Runs the contiguous m-grouped kernel with one expert owning every row; no routing tensor.
+ */
+int dg_fp8_gemm_nt(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
+                   const float* c, void* d, int out_dtype, int64_t M, int64_t N, int64_t K,
+                   int sf_format, int32_t* status, void* stream);
+
+/*
+ * Batched FP8 GEMM ([P2] validation, batched GEMM; also the masked layout with every count
+ * equal to the capacity):  D[i] = C[i] + A[i] . B[i]^T for i < batch.
+ *   a: e4m3 [batch, M, K].  sfa: [K/128][Mp] over the batch*M rows.  b: e4m3 [batch, N, K].
+ *   sfb: [batch][N/128][K/128].  c: optional fp32 [batch, M, N] (fp32 output only; may equal d).
+ *   d: [batch, M, N] bf16 or fp32.  1 <= batch <= DG_MAX_GROUPS.
+ */
+int dg_fp8_gemm_nt_batched(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
+                           const float* c, void* d, int out_dtype, int batch, int64_t M,
+                           int64_t N, int64_t K, int sf_format, int32_t* status, void* stream);
+
+/*
  * m-grouped masked BF16 GEMM ([P2] m_grouped_bf16_gemm_nt_masked(a, b, d, masked_m, expected_m),
  * the GEMM of the pages' reproduction, checked there against bmm(a.double(), b.double().mT)
  * rounded to bf16):

@@ -34,6 +34,8 @@ SIGNATURES = {
     "dg_quant_block_128x128": (I32, [P, I32, I64, I64, P, P, I32, F32, P]),
     "dg_m_grouped_fp8_contiguous": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, I32, P, SZ, P, P]),
     "dg_m_grouped_fp8_masked": (I32, [P, P, P, P, P, I32, P, I32, I64, I64, I64, I32, I32, P, SZ, P, P]),
+    "dg_fp8_gemm_nt": (I32, [P, P, P, P, P, P, I32, I64, I64, I64, I32, P, P]),
+    "dg_fp8_gemm_nt_batched": (I32, [P, P, P, P, P, P, I32, I32, I64, I64, I64, I32, P, P]),
     "dg_m_grouped_fp8_contiguous_psum": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, I32, P, SZ, P, P]),
     "dg_k_grouped_fp8_wgrad_psum": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
     "dg_quant_per_channel_128_psum": (I32, [P, I64, I64, P, I32, P, P, F32, P, P]),

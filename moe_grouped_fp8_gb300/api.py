@@ -16,7 +16,8 @@ from ._lib import DG_OP_K_GROUPED_WGRAD, DG_OUT_BF16, DG_OUT_FP32, DG_SF_FP32, D
 __all__ = [
     "dg_quant_per_token_1x128", "dg_quant_per_token_1x128_routed", "dg_quant_per_channel_128", "dg_quant_per_channel_128_pair",
     "dg_quant_block_128x128",
-    "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad",
+    "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad", "dg_fp8_gemm_nt",
+    "dg_fp8_gemm_nt_batched",
     "dg_k_grouped_fp8_wgrad_noalloc",
     "dg_workspace_size", "dg_last_error", "sfa_padded_rows", "empty_sfa", "kgrouped_workspace", "DGError",
 ]
@@ -180,6 +181,39 @@ def dg_m_grouped_fp8_contiguous_psum(a, sfa, b, sfb, d, psum, sf_format=DG_SF_FP
     """dg_m_grouped_fp8_contiguous routed by psum int32 [G]: expert e owns rows
     [round_up(psum[e-1], 128), psum[e])."""
     dg_m_grouped_fp8_contiguous(a, sfa, b, sfb, d, psum, sf_format, status, workspace, stream, _psum=True)
+
+
+def dg_fp8_gemm_nt(a, sfa, b, sfb, d, c=None, sf_format=DG_SF_FP32, status=None, stream=None):
+    """Plain FP8 GEMM: d [M, N] = c + a [M, K] . b [N, K]^T (c optional fp32, may be d)."""
+    _dev(a, sfa, b, sfb, d, c, status)
+    _need(a.dim() == 2 and b.dim() == 2 and a.shape[1] == b.shape[1], "a [M, K], b [N, K]")
+    M, K = a.shape
+    N = b.shape[0]
+    _need(tuple(d.shape) == (M, N) and a.is_contiguous() and b.is_contiguous() and d.is_contiguous(), "d [M, N]")
+    _need(sfa.dtype == _sf_dtype(sf_format) and sfb.dtype == _sf_dtype(sf_format), "scale dtype")
+    _need(sfa.numel() >= (K // 128) * sfa_padded_rows(M, sf_format), "sfa size")
+    _need(sfb.numel() >= (N // 128) * (K // 128), "sfb size")
+    if c is not None:
+        _need(c.dtype == torch.float32 and tuple(c.shape) == (M, N) and c.is_contiguous(), "c fp32 [M, N]")
+    check(load().dg_fp8_gemm_nt(_p(a), _p(sfa), _p(b), _p(sfb), _p(c), _p(d), _out_code(d), M, N, K, sf_format,
+                                _p(status), _s(stream)))
+
+
+def dg_fp8_gemm_nt_batched(a, sfa, b, sfb, d, c=None, sf_format=DG_SF_FP32, status=None, stream=None):
+    """Batched FP8 GEMM: d [B, M, N] = c + a [B, M, K] . b [B, N, K]^T per batch entry."""
+    _dev(a, sfa, b, sfb, d, c, status)
+    _need(a.dim() == 3 and b.dim() == 3 and a.shape[0] == b.shape[0] and a.shape[2] == b.shape[2], "shapes")
+    Bt, M, K = a.shape
+    N = b.shape[1]
+    _need(tuple(d.shape) == (Bt, M, N) and a.is_contiguous() and b.is_contiguous() and d.is_contiguous(),
+          "d [B, M, N]")
+    _need(sfa.dtype == _sf_dtype(sf_format) and sfb.dtype == _sf_dtype(sf_format), "scale dtype")
+    _need(sfa.numel() >= (K // 128) * sfa_padded_rows(Bt * M, sf_format), "sfa size")
+    _need(sfb.numel() >= Bt * (N // 128) * (K // 128), "sfb size")
+    if c is not None:
+        _need(c.dtype == torch.float32 and tuple(c.shape) == (Bt, M, N) and c.is_contiguous(), "c fp32 [B, M, N]")
+    check(load().dg_fp8_gemm_nt_batched(_p(a), _p(sfa), _p(b), _p(sfb), _p(c), _p(d), _out_code(d), Bt, M, N, K,
+                                        sf_format, _p(status), _s(stream)))
 
 
 def dg_m_grouped_fp8_masked(a, sfa, b, sfb, d, counts, expected_m=0, sf_format=DG_SF_FP32, status=None,

@@ -445,6 +445,22 @@ __global__ void __launch_bounds__(num_threads<SEP_STORE>(), 1)
                 load_group(kb0 / P::SFG + 2, sa_n, sb_n);
             }
 
+            // ---- accumulate: D = C + result (fp32 output; C may alias D: each element is read by
+            // the thread that later writes it, before any store of this tile)
+            if constexpr (OUT_FP32) {
+                if (a.c != nullptr && row_ok && !failed) {
+                    const float* crow = a.c + grow * a.ldd + static_cast<int64_t>(ti.nb) * BN + h2 * P::CPT;
+#pragma unroll
+                    for (int i = 0; i < P::CPT; i += 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(crow + i);
+                        acc[i] += v.x;
+                        acc[i + 1] += v.y;
+                        acc[i + 2] += v.z;
+                        acc[i + 3] += v.w;
+                    }
+                }
+            }
+
             // ---- stage the tile in shared memory once the previous tile's stores have read it
             if (tid == 0 && tix > 0) {
                 if constexpr (SEP_STORE) {
@@ -613,15 +629,19 @@ int dispatch_mgrouped(bool pair, int out, int fmt, const CUtensorMap& tA, const 
     return launch_gemm<L, MG_BN, MG_STAGES_BF16, false, false>(tA, tB, tD, tD8, args, s);
 }
 
-int check_common_mg(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d, int out,
-                    int G, int64_t N, int64_t K, int fmt) {
+// Shapes and codes; then (for a non-empty call) the pointers.
+int check_shape_mg(int out, int G, int64_t N, int64_t K, int fmt) {
     DG_CHECK_ARG(G >= 1 && G <= DG_MAX_GROUPS, "G must be in [1, %d] (%d)", DG_MAX_GROUPS, G);
     DG_CHECK_ARG(N > 0 && K > 0 && N % 128 == 0 && K % 128 == 0, "N and K must be positive multiples of 128");
     DG_CHECK_ARG(out == DG_OUT_BF16 || out == DG_OUT_FP32, "bad out_dtype %d", out);
     DG_CHECK_ARG(fmt == DG_SF_FP32 || fmt == DG_SF_UE8M0, "bad sf_format %d", fmt);
+    DG_CHECK_SUPPORTED(K <= (1 << 30) && N <= (1 << 24), "N or K too large");
+    return DG_OK;
+}
+
+int check_ptrs_mg(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d) {
     DG_CHECK_ARG(a && sfa && b && sfb && d, "null pointer argument");
     DG_CHECK_ARG(aligned16(a) && aligned16(b) && aligned16(d), "a, b and d must be 16-byte aligned");
-    DG_CHECK_SUPPORTED(K <= (1 << 30) && N <= (1 << 24), "N or K too large");
     return DG_OK;
 }
 
@@ -630,16 +650,27 @@ int check_common_mg(const uint8_t* a, const void* sfa, const uint8_t* b, const v
 
 using namespace dg;
 
-extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d,
-                                       int out_dtype, const int32_t* counts, int G, int64_t cap, int64_t N, int64_t K,
-                                       int expected_m, int sf_format, void* workspace, size_t workspace_bytes,
-                                       int32_t* status, void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
+namespace dg {
+namespace {
+
+int check_accumulator(const float* c, int out_dtype) {
+    if (c == nullptr) return DG_OK;
+    DG_CHECK_ARG(out_dtype == DG_OUT_FP32, "accumulation (c != NULL) needs fp32 output");
+    DG_CHECK_ARG(aligned16(c), "c must be 16-byte aligned");
+    return DG_OK;
+}
+
+// The masked layout [G, cap, K]; dense: every group has cap rows (a batched GEMM), no counts.
+int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, const float* c, void* d,
+                     int out_dtype, const int32_t* counts, bool dense, int G, int64_t cap, int64_t N, int64_t K,
+                     int expected_m, int sf_format, int32_t* status, void* stream) {
     DG_CHECK_ARG(cap >= 0, "cap must be >= 0");
-    if (int rc = check_common_mg(a, sfa, b, sfb, d, out_dtype, G, N, K, sf_format)) return rc;
-    DG_CHECK_ARG(counts != nullptr, "counts is null");
+    if (int rc = check_shape_mg(out_dtype, G, N, K, sf_format)) return rc;
+    DG_CHECK_ARG(c == nullptr || out_dtype == DG_OUT_FP32, "accumulation (c != NULL) needs fp32 output");
     if (cap == 0) return DG_OK;
+    if (int rc = check_ptrs_mg(a, sfa, b, sfb, d)) return rc;
+    if (int rc = check_accumulator(c, out_dtype)) return rc;
+    DG_CHECK_ARG(dense || counts != nullptr, "counts is null");
     DG_CHECK_SUPPORTED(cap <= (1 << 24) && static_cast<int64_t>(G) * cap < (1ll << 31), "cap too large");
     const int esize = out_dtype == DG_OUT_FP32 ? 4 : 2;
     const int64_t M = static_cast<int64_t>(G) * cap;
@@ -675,6 +706,8 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
     }
     GemmArgs args{};
     args.routing = counts;
+    args.dense = dense ? 1 : 0;
+    args.c = c;
     args.sfa = sfa;
     args.sfb = sfb;
     args.d = d;
@@ -692,17 +725,18 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
                                              static_cast<cudaStream_t>(stream));
 }
 
-namespace dg {
-namespace {
-
-// The contiguous layout, routed by m_indices [M] or (psum) by per-expert end rows [G].
-int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d,
-                         int out_dtype, const int32_t* routing, bool psum, int64_t M, int G, int64_t N, int64_t K,
-                         int sf_format, int32_t* status, void* stream) {
+// The contiguous layout, routed by m_indices [M] or (psum) by per-expert end rows [G]; dense:
+// one expert owning all M rows (a plain GEMM), no routing tensor.
+int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, const float* c,
+                         void* d, int out_dtype, const int32_t* routing, bool psum, bool dense, int64_t M, int G,
+                         int64_t N, int64_t K, int sf_format, int32_t* status, void* stream) {
     DG_CHECK_ARG(M >= 0, "M must be >= 0");
-    if (int rc = check_common_mg(a, sfa, b, sfb, d, out_dtype, G, N, K, sf_format)) return rc;
-    DG_CHECK_ARG(routing != nullptr, psum ? "psum is null" : "m_indices is null");
+    if (int rc = check_shape_mg(out_dtype, G, N, K, sf_format)) return rc;
+    DG_CHECK_ARG(c == nullptr || out_dtype == DG_OUT_FP32, "accumulation (c != NULL) needs fp32 output");
     if (M == 0) return DG_OK;
+    if (int rc = check_ptrs_mg(a, sfa, b, sfb, d)) return rc;
+    if (int rc = check_accumulator(c, out_dtype)) return rc;
+    DG_CHECK_ARG(dense || routing != nullptr, psum ? "psum is null" : "m_indices is null");
     DG_CHECK_SUPPORTED((M + BM - 1) / BM <= DG_MAX_M_BLOCKS, "M too large (at most %d rows)", DG_MAX_M_BLOCKS * BM);
     const int esize = out_dtype == DG_OUT_FP32 ? 4 : 2;
     const int64_t Mp = sf_format == DG_SF_FP32 ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
@@ -738,6 +772,8 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     GemmArgs args{};
     args.routing = routing;
     args.psum = psum ? 1 : 0;
+    args.dense = dense ? 1 : 0;
+    args.c = c;
     args.sfa = sfa;
     args.sfb = sfb;
     args.d = d;
@@ -764,8 +800,32 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
                                            size_t workspace_bytes, int32_t* status, void* stream) {
     (void)workspace;
     (void)workspace_bytes;
-    return m_grouped_contiguous(a, sfa, b, sfb, d, out_dtype, m_indices, false, M, G, N, K, sf_format, status,
+    return m_grouped_contiguous(a, sfa, b, sfb, nullptr, d, out_dtype, m_indices, false, false, M, G, N, K,
+                                sf_format, status, stream);
+}
+
+extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, void* d,
+                                       int out_dtype, const int32_t* counts, int G, int64_t cap, int64_t N, int64_t K,
+                                       int expected_m, int sf_format, void* workspace, size_t workspace_bytes,
+                                       int32_t* status, void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return m_grouped_masked(a, sfa, b, sfb, nullptr, d, out_dtype, counts, false, G, cap, N, K, expected_m,
+                            sf_format, status, stream);
+}
+
+extern "C" int dg_fp8_gemm_nt(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, const float* c,
+                              void* d, int out_dtype, int64_t M, int64_t N, int64_t K, int sf_format,
+                              int32_t* status, void* stream) {
+    return m_grouped_contiguous(a, sfa, b, sfb, c, d, out_dtype, nullptr, true, true, M, 1, N, K, sf_format, status,
                                 stream);
+}
+
+extern "C" int dg_fp8_gemm_nt_batched(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
+                                      const float* c, void* d, int out_dtype, int batch, int64_t M, int64_t N,
+                                      int64_t K, int sf_format, int32_t* status, void* stream) {
+    return m_grouped_masked(a, sfa, b, sfb, c, d, out_dtype, nullptr, true, batch, M, N, K, static_cast<int>(M),
+                            sf_format, status, stream);
 }
 
 extern "C" int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sfa, const uint8_t* b,
@@ -775,24 +835,28 @@ extern "C" int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sf
                                                 void* stream) {
     (void)workspace;
     (void)workspace_bytes;
-    return m_grouped_contiguous(a, sfa, b, sfb, d, out_dtype, psum, true, M, G, N, K, sf_format, status, stream);
+    return m_grouped_contiguous(a, sfa, b, sfb, nullptr, d, out_dtype, psum, true, false, M, G, N, K, sf_format,
+                                status, stream);
 }
 
-// ------------------------------------------------------------------------- test hook
-// Selects the m-grouped kernel of later bf16-output calls in this process: 0 automatic,
-// 1 single-CTA 128 x 128 tiles, 2 CTA pairs.  Lets the tests hold both kernels to the oracle.
+// ------------------------------------------------------------------------- test hooks
+// Each selects, for later calls in this process, one choice the library otherwise makes
+// itself, so that the tests hold every variant to the oracle and to each other.
+// The single-CTA tile width: 0 automatic, 128, or 256 (where N allows).
 extern "C" int dg_testing_mgrouped_bn(int bn) {
     DG_CHECK_ARG(bn == 0 || bn == MG_BN || bn == MG_BN_WIDE, "bn must be 0, %d or %d", MG_BN, MG_BN_WIDE);
     g_force_bn.store(bn, std::memory_order_relaxed);
     return DG_OK;
 }
 
+// Who issues the tile stores: 0 automatic, 1 thread 0 of the promotion warps, 2 the store warp.
 extern "C" int dg_testing_mgrouped_store(int which) {
     DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0 (automatic), 1 (thread 0) or 2 (store warp)");
     g_force_store.store(which, std::memory_order_relaxed);
     return DG_OK;
 }
 
+// The m-grouped kernel of bf16-output calls: 0 automatic, 1 single-CTA tiles, 2 CTA pairs.
 extern "C" int dg_testing_mgrouped_kernel(int which) {
     DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0, 1 or 2");
     g_force_kernel.store(which, std::memory_order_relaxed);

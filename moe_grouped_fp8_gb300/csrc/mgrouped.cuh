@@ -37,6 +37,8 @@ struct GemmArgs {
     int num_nb;      // output column tiles of the launched kernel
     int n128;        // N / 128 (sfb row count)
     int psum;        // Contiguous: routing holds per-expert end rows (prefix sums), not m_indices
+    int dense;       // no routing tensor: Masked counts all equal cap; Contiguous (psum) one expert ending at M
+    const float* c;  // fp32 accumulator added to the result (fp32 output only), row stride ldd; may alias d
 };
 
 // Shared-memory bytes of the run table used by build_runs / tile_prefix: int32 prefix and x,
@@ -70,6 +72,11 @@ struct RunTable {
 // rt.x holds the end row; an expert whose end is below its predecessor's, past M, or inside the
 // rounding gap is flagged DG_STATUS_BAD_INDEX and it and every later expert are skipped.
 // `scratch` holds one int16 per m-block.
+// End row of expert e of a prefix-sum routed call (the dense form has one expert ending at M).
+__device__ __forceinline__ int64_t route_end(const GemmArgs& a, int e) {
+    return a.dense ? a.M : static_cast<int64_t>(a.routing[e]);
+}
+
 template <Layout L, int NT>
 __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, void* scratch) {
     const int tid = threadIdx.x;
@@ -78,7 +85,7 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
         R = a.G;
         int bad = 0;
         for (int g = tid; g < a.G; g += NT) {
-            int c = a.routing[g];
+            int c = a.dense ? static_cast<int>(a.M) : a.routing[g];
             if (c < 0) { bad |= DG_STATUS_COUNT_GT_CAP; c = 0; }
             if (c > a.M) { bad |= DG_STATUS_COUNT_GT_CAP; c = static_cast<int>(a.M); }
             rt.first[g] = static_cast<int16_t>(g);
@@ -93,8 +100,8 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
         if (tid == 0) *s_first_bad = a.G;
         __syncthreads();
         for (int e = tid; e < a.G; e += NT) {
-            const int64_t prev = e > 0 ? a.routing[e - 1] : 0;
-            const int64_t end = a.routing[e];
+            const int64_t prev = e > 0 ? route_end(a, e - 1) : 0;
+            const int64_t end = route_end(a, e);
             const int64_t start = (prev + BM - 1) / BM * BM;
             const bool bad = prev < 0 || end < prev || end > a.M || (end > prev && end < start);
             if (bad) atomicMin(s_first_bad, e);
@@ -103,8 +110,8 @@ __device__ int build_runs(const GemmArgs& a, const RunTable& rt, int* s_scan, vo
         const int first_bad = *s_first_bad;
         if (first_bad < a.G && blockIdx.x == 0 && tid == 0) status_or(a.status, DG_STATUS_BAD_INDEX);
         for (int e = tid; e < a.G; e += NT) {
-            const int64_t prev = e > 0 ? a.routing[e - 1] : 0;
-            const int64_t end = a.routing[e];
+            const int64_t prev = e > 0 ? route_end(a, e - 1) : 0;
+            const int64_t end = route_end(a, e);
             const int64_t start = (prev + BM - 1) / BM * BM;
             const bool live = e < first_bad && end > start;
             rt.first[e] = static_cast<int16_t>(live ? start / BM : 0);

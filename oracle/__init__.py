@@ -61,6 +61,7 @@ def _load():
             lib.oracle_gemm_contiguous.argtypes = [P, P, P, P, P, i64, i32, i64, i64, P]
             lib.oracle_dot_rows.argtypes = [P, P, P, P, i64, i64, P]
             lib.oracle_gemm_masked.argtypes = [P, P, P, P, P, i32, i64, i64, i64, P]
+            lib.oracle_gemm_batched.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P]
             lib.oracle_gemm_kgrouped.argtypes = [P, P, P, P, P, P, i32, i64, i64, i64, P]
             lib.oracle_gemm_masked_bf16.argtypes = [P, P, P, i32, i64, i64, i64, P]
             lib.oracle_sizes_from_psum.argtypes = [P, i32, P]
@@ -207,6 +208,18 @@ def gemm_masked(qa, sfa, qb, sfb, counts) -> np.ndarray:
     N = qb.shape[1]
     d = np.full((G, cap, N), np.nan, np.float64)
     _load().oracle_gemm_masked(_p(qa), _p(sfa), _p(qb), _p(sfb), _p(cnt), G, cap, N, K, _p(d))
+    return d
+
+
+def gemm_batched(qa, sfa, qb, sfb, c=None) -> np.ndarray:
+    """fp64 D [B, M, N] = c + per-entry products (plain GEMM: B = 1); qa [B, M, K],
+    sfa [B, M, K/128] fp32 values, qb [B, N, K], sfb [B, N/128, K/128], c [B, M, N] or None."""
+    qa, sfa, qb, sfb = _c(qa, np.uint8), _c(sfa, np.float32), _c(qb, np.uint8), _c(sfb, np.float32)
+    B, M, K = qa.shape
+    N = qb.shape[1]
+    cc = None if c is None else _c(c, np.float64)
+    d = np.empty((B, M, N), np.float64)
+    _load().oracle_gemm_batched(_p(qa), _p(sfa), _p(qb), _p(sfb), _p(cc), B, M, N, K, _p(d))
     return d
 
 

@@ -330,6 +330,35 @@ void oracle_gemm_masked(const uint8_t* qa, const float* sfa, const uint8_t* qb, 
 }
 
 /* ----------------------------------------------------------------------------------------
+ * Plain and batched FP8 GEMM with accumulation (#469 validation: the adjacent-path checks of
+ * ordinary GEMM layouts, output dtypes and accumulation, and batched GEMM): for every batch
+ * entry b < B, row m < M and column n < N,
+ *   D[b][m][n] = C[b][m][n] + sum_k decode(qa[b][m][k]) sfa[b][m][k/128]
+ *                                  * decode(qb[b][n][k]) sfb[b][n/128][k/128]
+ * with C taken as 0 when c is NULL.  A plain GEMM is B = 1.
+ * qa [B][M][K], sfa [B][M][K/128], qb [B][N][K], sfb [B][N/128][K/128], c and d [B][M][N].
+ * --------------------------------------------------------------------------------------*/
+void oracle_gemm_batched(const uint8_t* qa, const float* sfa, const uint8_t* qb, const float* sfb,
+                         const double* c, int64_t B, int64_t M, int64_t N, int64_t K, double* d) {
+    int64_t KB = K / 128, NB = N / 128;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t m = 0; m < M; ++m) {
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double xa = g_dec[qa[(b * M + m) * K + k]] * (double)sfa[(b * M + m) * KB + k / 128];
+                    double xb = g_dec[qb[(b * N + n) * K + k]] *
+                                (double)sfb[(b * NB + n / 128) * KB + k / 128];
+                    acc += xa * xb;
+                }
+                d[(b * M + m) * N + n] = (c != NULL ? c[(b * M + m) * N + n] : 0.0) + acc;
+            }
+        }
+    }
+}
+
+/* ----------------------------------------------------------------------------------------
  * k-grouped wgrad GEMM (#365 repro): for each expert e with span [o_e, o_e + K_e) along K,
  *   D_e[n][h] = C_e[n][h] + sum_{t < K_e} decode(a_e[n][t]) sfa[(o_e+t)/128][n]
  *                                      * decode(b_e[h][t]) sfb[(o_e+t)/128][h]

@@ -577,3 +577,45 @@ def test_m_indices_from_psum_stops_at_the_first_bad_entry():
         first_row_of_e = {1: 256, 2: 384}[e]
         np.testing.assert_array_equal(mi[:first_row_of_e], good[:first_row_of_e])
         assert np.all(mi[first_row_of_e:] == -1)
+
+
+# ------------------------------------------------------------------------------ plain / batched GEMM
+
+def _random_codes(rng, shape):
+    q = rng.integers(0, 256, shape, dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0          # no NaN codes
+    return q
+
+
+def test_batched_gemm_matches_numpy_einsum_and_adds_c():
+    """The plain/batched oracle GEMM equals numpy's einsum over torch-decoded operands with the
+    block scales expanded (an independent route), C is added as given, and B = 1 is a plain GEMM."""
+    rng = np.random.default_rng(7)
+    Bt, M, N, K = 3, 5, 256, 384
+    qa, qb = _random_codes(rng, (Bt, M, K)), _random_codes(rng, (Bt, N, K))
+    sfa = rng.uniform(0.5, 2.0, (Bt, M, K // 128)).astype(np.float32)
+    sfb = rng.uniform(0.5, 2.0, (Bt, N // 128, K // 128)).astype(np.float32)
+    c = rng.standard_normal((Bt, M, N))
+    dec = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    A = dec[qa] * np.repeat(sfa.astype(np.float64), 128, axis=2)
+    B = dec[qb] * np.repeat(np.repeat(sfb.astype(np.float64), 128, axis=1), 128, axis=2)
+    prod = np.einsum("bmk,bnk->bmn", A, B)
+    got = oracle.gemm_batched(qa, sfa, qb, sfb, c)
+    np.testing.assert_allclose(got, c + prod, rtol=0, atol=1e-9 * np.abs(prod).max())
+    np.testing.assert_allclose(oracle.gemm_batched(qa, sfa, qb, sfb), prod, rtol=0, atol=1e-9 * np.abs(prod).max())
+    one = oracle.gemm_batched(qa[:1], sfa[:1], qb[:1], sfb[:1])
+    np.testing.assert_array_equal(one[0], oracle.gemm_batched(qa, sfa, qb, sfb)[0])
+
+
+def test_batched_gemm_equals_masked_at_full_counts_and_contiguous_single_expert():
+    """Batched GEMM = masked GEMM with every count = capacity; a plain GEMM = the contiguous
+    GEMM with every row routed to expert 0 (bitwise: same fp64 sums in the same order)."""
+    rng = np.random.default_rng(8)
+    Bt, M, N, K = 2, 7, 128, 256
+    qa, qb = _random_codes(rng, (Bt, M, K)), _random_codes(rng, (Bt, N, K))
+    sfa = rng.uniform(0.5, 2.0, (Bt, M, K // 128)).astype(np.float32)
+    sfb = rng.uniform(0.5, 2.0, (Bt, N // 128, K // 128)).astype(np.float32)
+    got = oracle.gemm_batched(qa, sfa, qb, sfb)
+    np.testing.assert_array_equal(got, oracle.gemm_masked(qa, sfa, qb, sfb, np.full(Bt, M, np.int32)))
+    cont = oracle.gemm_contiguous(qa[0], sfa[0], qb[:1], sfb[:1], np.zeros(M, np.int32))
+    np.testing.assert_array_equal(got[0], cont)
