@@ -445,6 +445,7 @@ __global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant
                                                            int64_t N, int64_t H, CUtensorMap* ws) {
     __shared__ __align__(128) CUtensorMap s_maps[8][2];
     __shared__ long long s_warp[8];
+    __shared__ long long s_o[256], s_k[256];  // this round's expert spans (k = 0: nothing to publish)
     __shared__ long long s_carry;
     __shared__ int s_first_bad;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
@@ -475,13 +476,17 @@ __global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant
         if (bad) atomicMin(&s_first_bad, e);
         __syncthreads();
         const bool live = e < G && e < s_first_bad && kk > 0;
-        unsigned live_mask = __ballot_sync(0xffffffffu, live);
-        while (live_mask) {
-            const int src = __ffs(live_mask) - 1;
-            live_mask &= live_mask - 1;
-            const long long o_src = __shfl_sync(0xffffffffu, o_e, src);
-            const long long k_src = __shfl_sync(0xffffffffu, kk, src);
-            const int e_src = base + wid * 32 + src;
+        s_o[t] = o_e;
+        s_k[t] = live ? kk : 0;
+        __syncthreads();
+        // the experts of this round are spread over the warps (expert j -> warp j % 8), so that
+        // their descriptor edits and release fences run side by side
+        const int n_round = G - base < static_cast<int>(blockDim.x) ? G - base : static_cast<int>(blockDim.x);
+        for (int j = wid; j < n_round; j += 8) {
+            const long long k_src = s_k[j];
+            if (k_src == 0) continue;  // warp-uniform
+            const long long o_src = s_o[j];
+            const int e_src = base + j;
             if (lane == 0) {
                 s_maps[wid][0] = (k_src * N >= TMAP_LARGE_BYTES) ? tmpl.a_large : tmpl.a_small;
                 s_maps[wid][1] = (k_src * H >= TMAP_LARGE_BYTES) ? tmpl.b_large : tmpl.b_small;
