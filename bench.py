@@ -7,9 +7,9 @@ grad_y [768, 2048] = randn * 1e-7 with channel 0 zeroed in each 128-token expert
 act [768, 2048] = randn * 0.4, D_e [2048, 2048] fp32 = C_e + grad_y_e^T act_e with C passed as D.
 
 One step = one pass of the k-grouped path over one batch: the per-channel FP8 casts of grad_y
-and act (with the per-expert K-major pack; both operands in one launch), the descriptor prologue
-and the k-grouped GEMM.
-Steps are captured once per input set as CUDA graphs and replayed; input sets rotate so the
+and act (with the per-expert K-major pack) and the per-expert descriptors in one launch, then
+the k-grouped GEMM.
+Steps are captured as CUDA graphs of several consecutive steps and replayed; input sets rotate so the
 working set of consecutive steps exceeds L2.  The metric is TFLOP/s on valid rows
 (2 * sum(K_e) * N * H per step).  Other workloads (--workload) are the m-grouped configs of
 the same pages; for those a step is the activation cast plus the GEMM (weights cast ahead).
@@ -295,8 +295,10 @@ class KGroupedWorkload:
         self.api.dg_k_grouped_fp8_wgrad(s["ap"], s["sfa"], s["bp"], s["sfb"], s["d"], s["d"], self.ks, self.T, s["ws"])
 
     def step(self, r):
-        self.casts(r)
-        self.wgrad(r)
+        """Both per-channel casts with the descriptors in one launch, then the GEMM."""
+        s = self.sets[r]
+        self.api.dg_k_grouped_fp8_wgrad_from_bf16(s["gy"], s["act"], self.ks, s["ap"], s["sfa"], s["bp"], s["sfb"],
+                                                  s["d"], s["d"], s["ws"])
 
     def gemm_only(self, r):
         import ctypes
@@ -307,11 +309,11 @@ class KGroupedWorkload:
             self.N, self.H, p(s["ws"]), s["ws"].numel(), None,
             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
 
-    launches_per_step = 3  # both per-channel casts (one launch), descriptor prologue, GEMM
+    launches_per_step = 2  # both per-channel casts + descriptors (one launch), GEMM
 
     def e2e(self, steps, stream):
         """Same step through the C ABI from pinned host buffers: H2D of grad_y, act, ks and C,
-        casts + prologue + GEMM, D2H of D, every step.  Double-buffered as a training loop that
+        casts + descriptors (one launch) + GEMM, D2H of D, every step.  Double-buffered as a training loop that
         offloads would run it: the device buffers alternate between two sets, copies in and out
         run on their own streams, so step i's D2H overlaps step i + 1's H2D (and compute); events
         order each buffer's reuse.  Returns ms per step and the bytes copied each way per step."""
@@ -340,9 +342,8 @@ class KGroupedWorkload:
                 x["d"].copy_(c_h, non_blocking=True)
                 ev["in"][b].record(s_in)
             stream.wait_event(ev["in"][b])
-            api.dg_quant_per_channel_128_pair(x["gy"], x["act"], x["ks"], s0["ap"], s0["sfa"], s0["bp"], s0["sfb"])
-            api.dg_k_grouped_fp8_wgrad(s0["ap"], s0["sfa"], s0["bp"], s0["sfb"], x["d"], x["d"], x["ks"], self.T,
-                                       s0["ws"])
+            api.dg_k_grouped_fp8_wgrad_from_bf16(x["gy"], x["act"], x["ks"], s0["ap"], s0["sfa"], s0["bp"],
+                                                 s0["sfb"], x["d"], x["d"], s0["ws"])
             ev["comp"][b].record(stream)
             s_out.wait_event(ev["comp"][b])
             with torch.cuda.stream(s_out):

@@ -262,6 +262,29 @@ int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa, const uint
                            size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * The whole wgrad of [P1]'s listing from bf16 inputs in two launches: the per-channel casts
+ * with the per-expert K-major packs of grad_y [K_cap, N] (A) and act [K_cap, H] (B), exactly as
+ * dg_quant_per_channel_128_pair fills a_packed/sfa and b_packed/sfb, and in the same launch the
+ * per-expert descriptors; then the GEMM of dg_k_grouped_fp8_wgrad.  The casts and the
+ * descriptors are independent and run side by side, which saves the separate descriptor launch.
+ *   grad_y, act: bf16, row-major, 16-byte aligned.  sf_zero as for the per-channel cast.
+ *   a_packed, sfa, b_packed, sfb: caller buffers of dg_k_grouped_fp8_wgrad's layouts (written).
+ *   ks, G, K_cap, N, H, c, d, workspace, status: as for dg_k_grouped_fp8_wgrad.
+ * The _psum form takes the expert spans as inclusive prefix sums (see dg_k_grouped_fp8_wgrad_psum).
+ */
+int dg_k_grouped_fp8_wgrad_from_bf16(const void* grad_y, const void* act, const int32_t* ks, int G,
+                                     int64_t K_cap, int64_t N, int64_t H, uint8_t* a_packed,
+                                     float* sfa, uint8_t* b_packed, float* sfb, const float* c,
+                                     float* d, float sf_zero, void* workspace,
+                                     size_t workspace_bytes, int32_t* status, void* stream);
+int dg_k_grouped_fp8_wgrad_from_bf16_psum(const void* grad_y, const void* act, const int32_t* psum,
+                                          int G, int64_t K_cap, int64_t N, int64_t H,
+                                          uint8_t* a_packed, float* sfa, uint8_t* b_packed,
+                                          float* sfb, const float* c, float* d, float sf_zero,
+                                          void* workspace, size_t workspace_bytes, int32_t* status,
+                                          void* stream);
+
+/*
  * dg_k_grouped_fp8_wgrad, dg_quant_per_channel_128 and dg_quant_per_channel_128_pair with the
  * expert spans given as inclusive prefix sums ([P1] k_grouped_fp8_gemm_nt_contiguous(...,
  * use_psum_layout=True)): psum[e] = K_0 + ... + K_e, so K_e = psum[e] - psum[e-1] (psum[-1] = 0).

@@ -43,6 +43,8 @@ SIGNATURES = {
     "dg_m_grouped_bf16_masked": (I32, [P, P, P, I32, P, I32, I64, I64, I64, I32, P, P]),
     "dg_m_grouped_bf16_contiguous": (I32, [P, P, P, I32, P, I64, I32, I64, I64, P, P]),
     "dg_k_grouped_fp8_wgrad": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
+    "dg_k_grouped_fp8_wgrad_from_bf16": (I32, [P, P, P, I32, I64, I64, I64, P, P, P, P, P, P, F32, P, SZ, P, P]),
+    "dg_k_grouped_fp8_wgrad_from_bf16_psum": (I32, [P, P, P, I32, I64, I64, I64, P, P, P, P, P, P, F32, P, SZ, P, P]),
     "dg_k_grouped_fp8_wgrad_noalloc": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, P]),
 }
 # test hooks exported by the library (not part of include/dg.h)

@@ -18,7 +18,7 @@ __all__ = [
     "dg_quant_block_128x128",
     "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad", "dg_fp8_gemm_nt",
     "dg_fp8_gemm_nt_batched",
-    "dg_k_grouped_fp8_wgrad_noalloc",
+    "dg_k_grouped_fp8_wgrad_noalloc", "dg_k_grouped_fp8_wgrad_from_bf16", "dg_k_grouped_fp8_wgrad_from_bf16_psum",
     "dg_workspace_size", "dg_last_error", "sfa_padded_rows", "empty_sfa", "kgrouped_workspace", "DGError",
 ]
 
@@ -275,6 +275,36 @@ def dg_k_grouped_fp8_wgrad(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap, worksp
     ws_bytes = workspace.numel() * workspace.element_size()
     check(getattr(load(), _fn)(_p(a_packed), _p(sfa), _p(b_packed), _p(sfb), _p(c), _p(d), _p(ks), G, K_cap, N, H,
                                _p(workspace), ws_bytes, _p(status), _s(stream)))
+
+
+def dg_k_grouped_fp8_wgrad_from_bf16(grad_y, act, ks, a_packed, sfa, b_packed, sfb, c, d, workspace, sf_zero=1e-30,
+                                     status=None, stream=None, _fn="dg_k_grouped_fp8_wgrad_from_bf16"):
+    """The whole wgrad from bf16: per-channel casts and packs of grad_y [K_cap, N] and act
+    [K_cap, H] into a_packed/sfa and b_packed/sfb (caller buffers, as dg_quant_per_channel_128_pair
+    fills them), then D_e = C_e + A_e^T B_e (c may be None or d) -- two launches."""
+    _dev(grad_y, act, ks, a_packed, sfa, b_packed, sfb, c, d, workspace, status)
+    G, N, H = d.shape
+    _need(grad_y.dim() == 2 and act.dim() == 2 and grad_y.shape[0] == act.shape[0], "grad_y [K_cap, N], act [K_cap, H]")
+    K_cap = grad_y.shape[0]
+    _need(grad_y.shape[1] == N and act.shape[1] == H, "grad_y / act columns must match d's N and H")
+    _need(grad_y.dtype == torch.bfloat16 and act.dtype == torch.bfloat16 and grad_y.is_contiguous()
+          and act.is_contiguous(), "grad_y and act must be contiguous bf16")
+    _need(d.dtype == torch.float32 and d.is_contiguous(), "d must be contiguous fp32 [G, N, H]")
+    _need(c is None or (tuple(c.shape) == tuple(d.shape) and c.dtype == torch.float32 and c.is_contiguous()), "c")
+    _need(ks.dtype == torch.int32 and ks.numel() == G, "ks must be int32 [G]")
+    _need(sfa.dtype == torch.float32 and sfa.numel() >= (K_cap // 128) * N, "sfa")
+    _need(sfb.dtype == torch.float32 and sfb.numel() >= (K_cap // 128) * H, "sfb")
+    _need(a_packed.numel() >= K_cap * N and b_packed.numel() >= K_cap * H, "packed operand size")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(getattr(load(), _fn)(_p(grad_y), _p(act), _p(ks), G, K_cap, N, H, _p(a_packed), _p(sfa), _p(b_packed),
+                               _p(sfb), _p(c), _p(d), sf_zero, _p(workspace), ws_bytes, _p(status), _s(stream)))
+
+
+def dg_k_grouped_fp8_wgrad_from_bf16_psum(grad_y, act, psum, a_packed, sfa, b_packed, sfb, c, d, workspace,
+                                          sf_zero=1e-30, status=None, stream=None):
+    """dg_k_grouped_fp8_wgrad_from_bf16 with expert spans as inclusive prefix sums psum int32 [G]."""
+    dg_k_grouped_fp8_wgrad_from_bf16(grad_y, act, psum, a_packed, sfa, b_packed, sfb, c, d, workspace, sf_zero,
+                                     status, stream, _fn="dg_k_grouped_fp8_wgrad_from_bf16_psum")
 
 
 def dg_k_grouped_fp8_wgrad_psum(a_packed, sfa, b_packed, sfb, c, d, psum, K_cap, workspace, status=None, stream=None):

@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "host_common.hpp"
+#include "cast_common.cuh"
 #include "kernel_common.cuh"
 #include "ptx.cuh"
 
@@ -439,18 +440,16 @@ struct Templates {
     CUtensorMap a_small, a_large, b_small, b_large;
 };
 
-__global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant__ Templates tmpl,
-                                                           const uint8_t* a_packed, const uint8_t* b_packed,
-                                                           const int32_t* ks, int psum, int G, int64_t K_cap,
-                                                           int64_t N, int64_t H, CUtensorMap* ws) {
+// The descriptor work of one 256-thread CTA (after the caller's programmatic-launch wait).
+__device__ __forceinline__ void prologue_cta(const Templates& tmpl, const uint8_t* a_packed, const uint8_t* b_packed,
+                                             const int32_t* ks, int psum, int G, int64_t K_cap, int64_t N, int64_t H,
+                                             CUtensorMap* ws) {
     __shared__ __align__(128) CUtensorMap s_maps[8][2];
     __shared__ long long s_warp[8];
     __shared__ long long s_o[256], s_k[256];  // this round's expert spans (k = 0: nothing to publish)
     __shared__ long long s_carry;
     __shared__ int s_first_bad;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    pdl_trigger();
-    pdl_wait();
     if (t == 0) {
         s_carry = 0;
         s_first_bad = 0x7fffffff;
@@ -536,6 +535,36 @@ __global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant
         __syncthreads();
         if (s_first_bad != 0x7fffffff) break;
     }
+}
+
+__global__ void __launch_bounds__(256) k_kgrouped_prologue(const __grid_constant__ Templates tmpl,
+                                                           const uint8_t* a_packed, const uint8_t* b_packed,
+                                                           const int32_t* ks, int psum, int G, int64_t K_cap,
+                                                           int64_t N, int64_t H, CUtensorMap* ws) {
+    pdl_trigger();
+    pdl_wait();
+    prologue_cta(tmpl, a_packed, b_packed, ks, psum, G, K_cap, N, H, ws);
+}
+
+// Both per-channel casts and the descriptors in one launch: CTA (x, y) with x < nblk casts
+// column block x of token block y; CTA (nblk, 0) builds the descriptors (the rest of that
+// column returns at once).  The two jobs are independent; both wait for the previous kernel of
+// the stream (whose operands, scales and descriptors they overwrite) and then run side by side.
+__global__ void __launch_bounds__(256) k_kgrouped_cast_prologue(const ChannelOperand op0, const ChannelOperand op1,
+                                                                int nblk0, int nblk, float sf_zero, int32_t* status,
+                                                                const __grid_constant__ Templates tmpl,
+                                                                const uint8_t* a_packed, const uint8_t* b_packed,
+                                                                const int32_t* ks, int psum, int G, int64_t K_cap,
+                                                                int64_t N, int64_t H, CUtensorMap* ws) {
+    if (static_cast<int>(blockIdx.x) == nblk) {
+        if (blockIdx.y != 0) return;
+        pdl_trigger();
+        pdl_wait();
+        prologue_cta(tmpl, a_packed, b_packed, ks, psum, G, K_cap, N, H, ws);
+        return;
+    }
+    channel_cast_cta(op0, op1, nblk0, K_cap, ks, psum, G, sf_zero, status, static_cast<int>(blockIdx.x),
+                     static_cast<int>(blockIdx.y));
 }
 
 // ---------------------------------------------------------------------------- host side
@@ -624,6 +653,32 @@ int launch(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, c
     return launch_pdl(k_kgrouped_gemm<1>, dim3(sms), dim3(NT), SMEM_TOTAL, s, tC, tD, args);
 }
 
+// Both per-channel casts and the descriptors (one launch), then the GEMM.
+int launch_from_bf16(const void* a_bf16, const void* b_bf16, const int32_t* ks, int psum, int G, int64_t K_cap,
+                     int64_t N, int64_t H, uint8_t* a_packed, float* sfa, uint8_t* b_packed, float* sfb,
+                     const float* c, float* d, float sf_zero, void* workspace, size_t workspace_bytes,
+                     int32_t* status, cudaStream_t s) {
+    if (int rc = check_args(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes))
+        return rc;
+    DG_CHECK_ARG(a_bf16 && b_bf16, "null pointer argument");
+    DG_CHECK_ARG(aligned16(a_bf16) && aligned16(b_bf16), "bf16 inputs must be 16-byte aligned");
+    DG_CHECK_SUPPORTED(K_cap / 128 < 65536, "K_cap too large");
+    if (K_cap == 0) return launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes,
+                                  status, s, true, psum);
+    Templates tmpl;
+    if (int rc = make_templates(a_packed, b_packed, N, H, &tmpl)) return rc;
+    const ChannelOperand op0{static_cast<const uint16_t*>(a_bf16), N, a_packed, sfa};
+    const ChannelOperand op1{static_cast<const uint16_t*>(b_bf16), H, b_packed, sfb};
+    const int nblk0 = static_cast<int>(N / CH_COLS);
+    const int nblk = nblk0 + static_cast<int>(H / CH_COLS);
+    const dim3 grid(static_cast<unsigned>(nblk + 1), static_cast<unsigned>(K_cap / 128));
+    if (int rc = launch_pdl(k_kgrouped_cast_prologue, grid, dim3(256), 0, s, op0, op1, nblk0, nblk, sf_zero, status,
+                            tmpl, a_packed, b_packed, ks, psum, G, K_cap, N, H, static_cast<CUtensorMap*>(workspace)))
+        return rc;
+    return launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes, status, s,
+                  false, psum);
+}
+
 }  // namespace kg
 }  // namespace dg
 
@@ -635,6 +690,24 @@ extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa,
                                       int32_t* status, void* stream) {
     return kg::launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes, status,
                       static_cast<cudaStream_t>(stream), true);
+}
+
+extern "C" int dg_k_grouped_fp8_wgrad_from_bf16(const void* grad_y, const void* act, const int32_t* ks, int G,
+                                                int64_t K_cap, int64_t N, int64_t H, uint8_t* a_packed, float* sfa,
+                                                uint8_t* b_packed, float* sfb, const float* c, float* d,
+                                                float sf_zero, void* workspace, size_t workspace_bytes,
+                                                int32_t* status, void* stream) {
+    return kg::launch_from_bf16(grad_y, act, ks, 0, G, K_cap, N, H, a_packed, sfa, b_packed, sfb, c, d, sf_zero,
+                                workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dg_k_grouped_fp8_wgrad_from_bf16_psum(const void* grad_y, const void* act, const int32_t* psum,
+                                                     int G, int64_t K_cap, int64_t N, int64_t H, uint8_t* a_packed,
+                                                     float* sfa, uint8_t* b_packed, float* sfb, const float* c,
+                                                     float* d, float sf_zero, void* workspace,
+                                                     size_t workspace_bytes, int32_t* status, void* stream) {
+    return kg::launch_from_bf16(grad_y, act, psum, 1, G, K_cap, N, H, a_packed, sfa, b_packed, sfb, c, d, sf_zero,
+                                workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int dg_k_grouped_fp8_wgrad_psum(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,

@@ -235,3 +235,56 @@ def test_determinism_10000_calls():
             bad += (out.view(torch.int32) != first.view(torch.int32)).any().to(torch.int64)
         sync()
         assert bad.item() == 0, f"sf_val={sz}: {bad.item()} calls differ"
+
+
+def _fused_vs_two_calls(ks_or_psum, K_cap, N, H, c_mode, psum=False, seed=21, gy_scale=1.0, act_scale=1.0):
+    """The fused call and the pair cast + wgrad sequence on the same inputs: packed codes,
+    scales, output and status bitwise equal."""
+    G = len(ks_or_psum)
+    gy = wl.randn_bf16((K_cap, N), seed, gy_scale).cuda()
+    act = wl.randn_bf16((K_cap, H), seed + 1, act_scale).cuda()
+    spans = torch.tensor(ks_or_psum, dtype=torch.int32, device="cuda")
+    c_sep = (torch.from_numpy(np.random.default_rng(seed).normal(0, 1e-3, (G, N, H)).astype(np.float32)).cuda()
+             if c_mode == "separate" else None)
+    outs = []
+    for fused in (False, True):
+        ap = torch.zeros(K_cap * N, dtype=torch.uint8, device="cuda")
+        bp = torch.zeros(K_cap * H, dtype=torch.uint8, device="cuda")
+        sfa = torch.zeros(K_cap // 128, N, dtype=torch.float32, device="cuda")
+        sfb = torch.zeros(K_cap // 128, H, dtype=torch.float32, device="cuda")
+        d = torch.zeros(G, N, H, dtype=torch.float32, device="cuda")
+        c = None if c_mode == "none" else (d if c_mode == "alias" else c_sep)
+        ws = api.kgrouped_workspace(G, "cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            fn = api.dg_k_grouped_fp8_wgrad_from_bf16_psum if psum else api.dg_k_grouped_fp8_wgrad_from_bf16
+            fn(gy, act, spans, ap, sfa, bp, sfb, c, d, ws, status=status)
+        else:
+            cast = api.dg_quant_per_channel_128_pair_psum if psum else api.dg_quant_per_channel_128_pair
+            cast(gy, act, spans, ap, sfa, bp, sfb, status=status)
+            gemm = api.dg_k_grouped_fp8_wgrad_psum if psum else api.dg_k_grouped_fp8_wgrad
+            gemm(ap, sfa, bp, sfb, c, d, spans, K_cap, ws, status)
+        sync()
+        outs.append([t.cpu().numpy().view(np.uint8) for t in (ap, bp, sfa, sfb, d)] + [status.item()])
+    for i, what in enumerate(["a_packed", "b_packed", "sfa", "sfb", "d"]):
+        np.testing.assert_array_equal(outs[0][i], outs[1][i], err_msg=what)
+    assert outs[0][5] == outs[1][5]
+    return outs[1][5]
+
+
+@pytest.mark.parametrize("ks,K_cap,N,H,c_mode", [([256, 0, 128, 384], 768, 256, 384, "alias"),
+                                                 ([128, 256], 1024, 128, 256, "separate"),
+                                                 ([256, 128, 128, 256], 768, 2048, 2048, "alias"),
+                                                 ([384, 128], 512, 256, 128, "none")])
+def test_from_bf16_bitwise_equals_cast_then_wgrad(ks, K_cap, N, H, c_mode):
+    """Casts + descriptors in one launch, then the GEMM: the same bits as the two public calls
+    (which the tests above hold to the oracle)."""
+    assert _fused_vs_two_calls(ks, K_cap, N, H, c_mode, gy_scale=1e-3, act_scale=0.4) == 0
+
+
+def test_from_bf16_psum_and_bad_spans():
+    assert _fused_vs_two_calls([256, 256, 384, 768], 768, 256, 256, "alias", psum=True) == 0
+    st = _fused_vs_two_calls([128, 100, 128], 512, 128, 128, "alias")        # K_e not a multiple of 128
+    assert st & DG_STATUS_K_NOT_ALIGNED
+    st = _fused_vs_two_calls([256, 512, 128], 512, 128, 256, "alias")        # spans past K_cap
+    assert st & DG_STATUS_K_OVERFLOW
