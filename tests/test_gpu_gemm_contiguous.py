@@ -210,7 +210,8 @@ def test_psum_bad_entry_flagged_and_walk_stops():
 
 def replay_case(G, N, K, E, replays, check_every, seed, mode="m_indices"):
     """Capture cast + GEMM once; replay with routing re-drawn in place (same buffers), routed by
-    m_indices or by psum (the modes of the pages' graph-mutation test)."""
+    m_indices or by psum (the modes of the pages' graph-mutation test); "routed" also casts only
+    the rows whose m_indices entry is >= 0 (the routed cast reads the same re-drawn tensor)."""
     T = G * E
     m_max = wl.contiguous_capacity(T, G)
     a = wl.randn_bf16((m_max, K), seed, 1.0, device="cuda")
@@ -220,6 +221,7 @@ def replay_case(G, N, K, E, replays, check_every, seed, mode="m_indices"):
     sfa = api.empty_sfa(m_max, K, fmt, "cuda")
     qb, sfb = gpu_quant_blocks(b, fmt)
     psum_mode = mode == "psum"
+    routed_cast = mode == "routed"
     mi_dev = torch.full((G if psum_mode else m_max,), -1, dtype=torch.int32, device="cuda")
     d = torch.empty(m_max, N, dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -228,7 +230,10 @@ def replay_case(G, N, K, E, replays, check_every, seed, mode="m_indices"):
         return wl.contiguous_psum(counts) if psum_mode else wl.contiguous_m_indices(counts, m_max)
 
     def step():
-        api.dg_quant_per_token_1x128(a, qa, sfa, fmt)
+        if routed_cast:
+            api.dg_quant_per_token_1x128_routed(a, qa, sfa, mi_dev, fmt)
+        else:
+            api.dg_quant_per_token_1x128(a, qa, sfa, fmt)
         if psum_mode:
             api.dg_m_grouped_fp8_contiguous_psum(qa, sfa, qb, sfb, d, mi_dev, fmt, status)
         else:
@@ -282,7 +287,7 @@ def replay_case(G, N, K, E, replays, check_every, seed, mode="m_indices"):
     assert checked >= replays // check_every
 
 
-@pytest.mark.parametrize("mode", ["m_indices", "psum"])
+@pytest.mark.parametrize("mode", ["m_indices", "psum", "routed"])
 def test_graph_replay_with_changed_routing_small(mode):
     replay_case(G=16, N=256, K=256, E=20, replays=30, check_every=3, seed=7, mode=mode)
 

@@ -288,3 +288,56 @@ def test_from_bf16_psum_and_bad_spans():
     assert st & DG_STATUS_K_NOT_ALIGNED
     st = _fused_vs_two_calls([256, 512, 128], 512, 128, 256, "alias")        # spans past K_cap
     assert st & DG_STATUS_K_OVERFLOW
+
+
+def test_fused_graph_replay_with_changed_ks():
+    """dg_k_grouped_fp8_wgrad_from_bf16 captured once; 12 replays with the expert spans re-drawn in
+    place (including empty experts), each checked against the oracle (C = D = 0 before a replay)."""
+    G, N, H, K_cap = 5, 256, 128, 1280
+    gy = wl.randn_bf16((K_cap, N), 91, 1e-3)
+    act = wl.randn_bf16((K_cap, H), 92, 0.4)
+    gyd, actd = gy.cuda(), act.cuda()
+    ks_dev = torch.tensor([256, 256, 256, 256, 256], dtype=torch.int32, device="cuda")
+    ap = torch.empty(K_cap * N, dtype=torch.uint8, device="cuda")
+    bp = torch.empty(K_cap * H, dtype=torch.uint8, device="cuda")
+    sfa = torch.empty(K_cap // 128, N, dtype=torch.float32, device="cuda")
+    sfb = torch.empty(K_cap // 128, H, dtype=torch.float32, device="cuda")
+    d = torch.zeros(G, N, H, dtype=torch.float32, device="cuda")
+    ws = api.kgrouped_workspace(G, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        api.dg_k_grouped_fp8_wgrad_from_bf16(gyd, actd, ks_dev, ap, sfa, bp, sfb, d, d, ws, status=status)
+
+    step()
+    sync()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    sync()
+    rng = np.random.default_rng(93)
+    for it in range(12):
+        blocks = rng.multinomial(K_cap // 128 - rng.integers(0, 3), np.full(G, 1.0 / G))
+        if it == 4:
+            blocks[1] = 0
+            blocks[3] = 0
+        ks = (blocks * 128).astype(np.int32)
+        ks_dev.copy_(torch.from_numpy(ks))
+        d.zero_()
+        g.replay()
+        sync()
+        assert status.item() == 0
+        T = int(ks.sum())
+        oqa, osfa = oracle.quant_per_channel_128(gy[:T])
+        oqb, osfb = oracle.quant_per_channel_128(act[:T])
+        ref = oracle.gemm_kgrouped(oracle.pack_kmajor(oqa, ks), osfa, oracle.pack_kmajor(oqb, ks), osfb, list(ks), N, H)
+        got = d.double().cpu().numpy()
+        for e in range(G):
+            if ks[e] == 0:
+                assert np.all(got[e] == 0), f"replay {it}: empty expert {e} written"
+            else:
+                assert_close(got[e], ref[e].astype(np.float32), True, f"replay {it} expert {e}")

@@ -243,3 +243,61 @@ def test_decode_shape_full_size_sampled():
     rows = torch.arange(cap, device="cuda")[None, :]
     pad = rows >= cnt[:, None]
     assert bool((d.view(torch.int16)[pad] == -1).all()), "padding rows written"
+
+
+def test_graph_replay_with_changed_counts():
+    """Cast (row counts) + GEMM captured once; 24 replays with the counts re-drawn in place
+    (including all-zero, full and over-capacity values): valid rows match the oracle on samples,
+    rows at or past each count keep their sentinel."""
+    G, cap, N, K = 12, 320, 512, 384
+    a = wl.randn_bf16((G, cap, K), 81, 1.0, device="cuda")
+    b = wl.randn_bf16((G, N, K), 82, 0.02, device="cuda")
+    qa = torch.empty(G * cap, K, dtype=torch.uint8, device="cuda")
+    sfa = api.empty_sfa(G * cap, K, DG_SF_FP32, "cuda")
+    qb, sfb = gpu_quant_blocks(b, DG_SF_FP32)
+    cnt = torch.zeros(G, dtype=torch.int32, device="cuda")
+    d = sentinel_like((G, cap, N), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        api.dg_quant_per_token_1x128(a.view(G * cap, K), qa, sfa, DG_SF_FP32, row_counts=cnt)
+        api.dg_m_grouped_fp8_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, 96, DG_SF_FP32, status)
+
+    cnt.copy_(torch.full((G,), 100, dtype=torch.int32))
+    step()
+    sync()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    sync()
+    oqb, osfb, _ = oracle.quant_block_128x128(b.cpu())
+    rng = np.random.default_rng(83)
+    for it in range(24):
+        counts = rng.poisson(96, G).astype(np.int32)
+        if it == 5:
+            counts[:] = 0
+        if it == 9:
+            counts[:] = cap
+        if it == 13:
+            counts[::3] = cap + 50                        # clamped to cap and flagged
+        cnt.copy_(torch.from_numpy(counts))
+        d.view(torch.int16).fill_(-1)
+        status.zero_()
+        g.replay()
+        sync()
+        v = np.clip(counts, 0, cap)
+        valid = np.arange(cap)[None, :] < v[:, None]
+        assert np.all(out_bits(d)[~valid] == sentinel_value(torch.bfloat16)), f"replay {it}: padding row written"
+        assert bool(status.item()) == bool(np.any(counts > cap)), f"replay {it}: status {status.item()}"
+        for e in rng.choice(G, 3, replace=False):
+            if v[e] == 0:
+                continue
+            rows = np.unique(rng.integers(0, v[e], 4))
+            oqa, osfa, _ = oracle.quant_per_token_1x128(a[int(e), torch.from_numpy(rows).cuda()].cpu())
+            ref = oracle.gemm_masked(oqa[None], osfa[None], oqb[int(e):int(e) + 1], osfb[int(e):int(e) + 1], [len(rows)])
+            assert_close(to_f64(d[int(e), torch.from_numpy(rows).cuda()]), ref_out(ref[0], False), False,
+                         f"replay {it} expert {e}")
