@@ -329,3 +329,30 @@ def test_prefill_shape_full_size_sampled():
     assert_close(np.concatenate(gpu_vals), np.concatenate(ref_vals), False, "prefill sampled")
     pad = torch.from_numpy(mi < 0).cuda()
     assert bool((d.view(torch.int16)[pad] == -1).all()), "padding rows written"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["m_indices", "psum"])
+def test_determinism_10000_calls(mgrouped_kernel, mode):
+    """Ragged segments routed by m_indices or psum: 10,000 calls, each bitwise equal to the first."""
+    if mgrouped_kernel == "pair":
+        pytest.skip("the default kernel")
+    counts = [130, 0, 1, 128, 257, 9]
+    G, N, K = len(counts), 1024, 512
+    m_max = wl.contiguous_capacity(sum(counts), G)
+    a = wl.randn_bf16((m_max, K), 47, 1.0, device="cuda")
+    b = wl.randn_bf16((G, N, K), 48, 0.02, device="cuda")
+    qa, sfa = gpu_quant_tokens(a, DG_SF_UE8M0)
+    qb, sfb = gpu_quant_blocks(b, DG_SF_UE8M0)
+    route = wl.contiguous_psum(counts) if mode == "psum" else wl.contiguous_m_indices(counts, m_max)
+    r = torch.tensor(route, dtype=torch.int32, device="cuda")
+    fn = api.dg_m_grouped_fp8_contiguous_psum if mode == "psum" else api.dg_m_grouped_fp8_contiguous
+    d = torch.zeros(m_max, N, dtype=torch.bfloat16, device="cuda")
+    fn(qa, sfa, qb, sfb, d, r, DG_SF_UE8M0)
+    first = d.clone()
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(10000):
+        fn(qa, sfa, qb, sfb, d, r, DG_SF_UE8M0)
+        bad += (d.view(torch.int16) != first.view(torch.int16)).any().to(torch.int64)
+    sync()
+    assert bad.item() == 0, f"{bad.item()} of 10000 calls differ"

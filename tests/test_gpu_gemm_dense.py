@@ -111,3 +111,23 @@ def test_batched_gemm(Bt, M, N, K, fmt, out, accumulate):
                               None if c_host is None else c_host.double().numpy())
     fp32 = out == torch.float32
     assert_close(to_f64(d), ref_out(ref, fp32), fp32, "batched GEMM")
+
+
+@pytest.mark.slow
+def test_plain_gemm_determinism_10000_calls():
+    """10,000 in-place accumulating calls from the same C: each bitwise equal to the first."""
+    M, N, K = 300, 512, 384
+    a = wl.randn_bf16((M, K), 730, 1.5)
+    b = wl.randn_bf16((1, N, K), 731, 0.02)
+    qa, sfa, qb, sfb, *_ = quantized(a, b, DG_SF_FP32)
+    c0 = torch.randn(M, N, dtype=torch.float32, device="cuda")
+    d = c0.clone()
+    api.dg_fp8_gemm_nt(qa, sfa, qb.view(N, K), sfb.view(N // 128, K // 128), d, c=d)
+    first = d.clone()
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(10000):
+        d.copy_(c0)
+        api.dg_fp8_gemm_nt(qa, sfa, qb.view(N, K), sfb.view(N // 128, K // 128), d, c=d)
+        bad += (d.view(torch.int32) != first.view(torch.int32)).any().to(torch.int64)
+    sync()
+    assert bad.item() == 0, f"{bad.item()} of 10000 calls differ"

@@ -301,3 +301,27 @@ def test_graph_replay_with_changed_counts():
             ref = oracle.gemm_masked(oqa[None], osfa[None], oqb[int(e):int(e) + 1], osfb[int(e):int(e) + 1], [len(rows)])
             assert_close(to_f64(d[int(e), torch.from_numpy(rows).cuda()]), ref_out(ref[0], False), False,
                          f"replay {it} expert {e}")
+
+
+@pytest.mark.slow
+def test_determinism_10000_calls(mgrouped_kernel):
+    """The pages' reproduction shape (G=8, cap=32, N=K=256, its counts): 10,000 calls, each
+    bitwise equal to the first; and 2,000 on a 128 x 256-tile shape with partial blocks."""
+    if mgrouped_kernel == "pair":
+        pytest.skip("the default kernel")
+    for (G, cap, N, K, counts, iters) in [(8, 32, 256, 256, [0, 1, 16, 31, 32, 1, 32, 32], 10000),
+                                          (4, 300, 1024, 768, [300, 7, 129, 0], 2000)]:
+        a = wl.randn_bf16((G, cap, K), 37, 1.0, device="cuda")
+        b = wl.randn_bf16((G, N, K), 38, 0.02, device="cuda")
+        qa, sfa = gpu_quant_tokens(a.view(G * cap, K), DG_SF_FP32)
+        qb, sfb = gpu_quant_blocks(b, DG_SF_FP32)
+        cnt = torch.tensor(counts, dtype=torch.int32, device="cuda")
+        d = torch.zeros(G, cap, N, dtype=torch.bfloat16, device="cuda")
+        api.dg_m_grouped_fp8_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, 0, DG_SF_FP32)
+        first = d.clone()
+        bad = torch.zeros((), dtype=torch.int64, device="cuda")
+        for _ in range(iters):
+            api.dg_m_grouped_fp8_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, 0, DG_SF_FP32)
+            bad += (d.view(torch.int16) != first.view(torch.int16)).any().to(torch.int64)
+        sync()
+        assert bad.item() == 0, f"{bad.item()} of {iters} calls differ"
