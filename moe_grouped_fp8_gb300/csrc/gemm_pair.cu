@@ -9,9 +9,9 @@
 // flight to keep the tensor core busy.  (N = 192 rather than 256 keeps each promotion thread at
 // 64 accumulators within the 128 registers that 14 warps per SM leave.)
 //
-// Roles (448 threads per CTA): warps 0-11 promote and store (lane quarter = warp % 4, 64-column
+// Roles (480 threads per CTA): warps 0-11 promote and store (lane quarter = warp % 4, 64-column
 // group = warp / 4), warp 12 loads A and B with TMA, warp 13 owns tensor memory; in the even
-// CTA its lane 0 issues the MMAs of the pair.  Per 128-K block the partial P goes to one of two
+// CTA lane 0 of warps 13 and 14 issue the MMAs of the pair, on alternate 128-K blocks.  Per 128-K block the partial P goes to one of two
 // TMEM buffers; the promotion warps read it and accumulate
 // acc += sfa * sfb * P in fp32 registers - the per-128-K-block promotion of the 1x128 / 128x128
 // scaling ("FP8 GEMM with fine-grained scaling": per-token activation scales, per-block weight
@@ -40,8 +40,9 @@ namespace {
 
 constexpr int P_EPI_WARPS = 12;
 constexpr int P_PRODUCER_WARP = 12;
-constexpr int P_MMA_WARP = 13;
-constexpr int P_THREADS = 448;
+constexpr int P_MMA_WARP = 13;         // and P_MMA_WARP + 1: two issuers taking alternate 128-K blocks
+constexpr int P_MMA_WARPS = 2;
+constexpr int P_THREADS = 480;
 constexpr int P_EPI_BAR = 1;             // named barrier of the 384 promotion/store threads
 constexpr int P_BN = PAIR_BN;            // output columns of a pair tile
 constexpr int P_BHALF = PAIR_B_ROWS;     // B rows held by each CTA
@@ -67,7 +68,7 @@ struct PairPlan {
     static constexpr int MISC_BYTES = 256;
     static constexpr int TOTAL = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(P_EPI_WARPS * 32 + 64 == P_THREADS, "roles");
+    static_assert(P_EPI_WARPS * 32 + 32 + 32 * P_MMA_WARPS == P_THREADS, "roles");
     static_assert(P_CPT * (P_EPI_WARPS / 4) == P_BN && P_CPT % 32 == 0, "column groups");
     static_assert(P_CPT * 2 == 128, "a promotion thread's bf16 columns fill one 128-byte chunk row");
     static_assert(STG_OFF % 1024 == 0 && SCHED_OFF % 1024 == 0, "TMA / swizzle buffers are 1024-byte aligned");
@@ -222,16 +223,28 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == P_MMA_WARP) {
+    } else if (warp >= P_MMA_WARP && warp < P_MMA_WARP + P_MMA_WARPS) {
+        // Two issuers in the even CTA take alternate 128-K blocks (block number n of the pair), as
+        // in the single-CTA kernel: while one is blocked issuing, the other has passed its waits.
+        // Each waits for its TMEM buffer before its stage: with an odd stage count a stage's uses
+        // alternate between the issuers, and the buffer wait (after the in-order promotion of block
+        // n - TBUFS) orders the stage's previous use first.
+        static_assert(P_STAGES % P_MMA_WARPS == 0 || P_TBUFS <= P_STAGES - 1, "stage phase order");
+        static_assert(P_TBUFS % P_MMA_WARPS == 0, "one issuer per TMEM buffer");
+        const uint32_t me = static_cast<uint32_t>(warp - P_MMA_WARP);
         if (leader && lane == 0 && num_tiles > 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int tb = 0;
-            uint32_t tphase = 0;
             bool ok = true, any = false;
+            int last_tb = 0;
+            uint32_t last_tphase = 0;
+            uint32_t n = 0;
             constexpr uint32_t IDESC = idesc_e4m3_f32(2 * BM, P_BN);
             for (int t = cid; t < num_tiles && ok; t += ncl) {
-                for (int kb = 0; kb < a.KB; ++kb) {
+                for (int kb = 0; kb < a.KB; ++kb, ++n) {
+                    if (n % P_MMA_WARPS != me) continue;
+                    const int stage = static_cast<int>(n % P_STAGES);
+                    const uint32_t phase = (n / P_STAGES) & 1u;
+                    const int tb = static_cast<int>(n % P_TBUFS);
+                    const uint32_t tphase = (n / P_TBUFS) & 1u;
                     if (!mbar_wait_cl(&tempty[tb], tphase ^ 1u, wc)) { ok = false; break; }
                     if (!mbar_wait_cl(&full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
@@ -245,17 +258,14 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                     umma_commit_pair(&empty[stage], 3);
                     umma_commit_pair(&tfull[tb], 3);
                     any = true;
-                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
-                    if (++tb == P_TBUFS) { tb = 0; tphase ^= 1u; }
+                    last_tb = tb;
+                    last_tphase = tphase;
                 }
             }
             if (any) {
-                // the last commit: every MMA issued has completed
-                int lt = tb - 1;
-                uint32_t lp = tphase;
-                if (lt < 0) { lt = P_TBUFS - 1; lp ^= 1u; }
+                // this issuer's last commit: every MMA it issued has completed
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait_cl(&tfull[lt], lp)) {
+                while (!mbar_try_wait_cl(&tfull[last_tb], last_tphase)) {
                     if (globaltimer_ns() - t0 > a.wait_limit_ns) break;
                 }
             }
