@@ -707,6 +707,11 @@ def run_ours(args, ws, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     wk = make_workload(args.workload, device)
+    if args.mgrouped_kernel != "auto":
+        from moe_grouped_fp8_gb300 import _lib
+        _lib.check(_lib.load().dg_testing_mgrouped_kernel({"single": 1, "pair": 2}[args.mgrouped_kernel]))
+        if wk.kernel_name == "k_grouped_gemm" and args.mgrouped_kernel == "pair":
+            wk.kernel_name = "k_grouped_gemm_pair"
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
 
@@ -864,6 +869,9 @@ def main():
                          "--steps steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--mgrouped-kernel", choices=["auto", "single", "pair"], default="auto",
+                    help="m-grouped FP8 GEMM kernel of bf16-output workloads: the library's choice, or one "
+                         "forced through its test hook for a comparison (outputs are bitwise equal)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_env()

@@ -48,7 +48,8 @@ def test_prologue_descriptors_match_host_encoding():
 
 def kgrouped_case(ks, N, H, c_mode="alias", sf_zero=1e-30, seed=0, gy_scale=1.0, act_scale=1.0, zero_ch=False,
                   calls=1, K_cap=None):
-    """c_mode: 'none' (c = NULL), 'separate' (random C), 'alias' (c = d, zero-initialised)."""
+    """c_mode: 'none' (c = NULL), 'separate' (random C), 'alias' (c = d, zero-initialised),
+    'alias_random' (c = d, initialised with the random C of 'separate')."""
     G = len(ks)
     T = sum(ks)
     K_cap = T if K_cap is None else K_cap
@@ -66,12 +67,16 @@ def kgrouped_case(ks, N, H, c_mode="alias", sf_zero=1e-30, seed=0, gy_scale=1.0,
     ws = api.kgrouped_workspace(G, "cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     c_host = None
-    if c_mode == "separate":
+    if c_mode in ("separate", "alias_random"):
         c_host = torch.from_numpy(np.random.default_rng(seed).normal(0, 1e-3, (G, N, H)).astype(np.float32))
     first = None
     for i in range(calls):
-        d = torch.zeros(G, N, H, dtype=torch.float32, device="cuda")
-        c = None if c_mode == "none" else (d if c_mode == "alias" else c_host.cuda())
+        if c_mode == "alias_random":
+            d = c_host.cuda()
+            c = d
+        else:
+            d = torch.zeros(G, N, H, dtype=torch.float32, device="cuda")
+            c = None if c_mode == "none" else (d if c_mode == "alias" else c_host.cuda())
         api.dg_k_grouped_fp8_wgrad(ap, sfa, bp, sfb, c, d, ks_dev, K_cap, ws, status)
         if calls > 1:
             if first is None:
@@ -93,9 +98,17 @@ def kgrouped_case(ks, N, H, c_mode="alias", sf_zero=1e-30, seed=0, gy_scale=1.0,
     return d, status
 
 
-@pytest.mark.parametrize("c_mode", ["alias", "none", "separate"])
+@pytest.mark.parametrize("c_mode", ["alias", "alias_random", "none", "separate"])
 def test_small_with_empty_expert(c_mode):
     kgrouped_case([256, 0, 128, 384], 256, 384, c_mode=c_mode, seed=3)
+
+
+def test_aliased_and_separate_accumulator_bitwise_equal():
+    """D = C + result with C aliasing D (the tile is added into D where it lies) and with C in its
+    own buffer (C loaded and added before the store): the same fp32 bits, for every expert."""
+    d_alias, _ = kgrouped_case([256, 128, 0, 384], 384, 512, c_mode="alias_random", seed=5)
+    d_sep, _ = kgrouped_case([256, 128, 0, 384], 384, 512, c_mode="separate", seed=5)
+    assert torch.equal(d_alias.view(torch.int32), d_sep.view(torch.int32))
 
 
 def test_pages_wgrad_repro_full():
