@@ -40,14 +40,18 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;     // and MMA_WARP + 1: the two MMA issuers
 constexpr int NUM_MMA_WARPS = 2;
-constexpr int STORE_WARP = 11;  // with SEP_STORE: issues the TMA stores of staged tiles
+constexpr int STORE_WARP = 11;  // with ST_WARP: issues the TMA stores of staged tiles
+// How a tile reaches the output: staged in shared memory and stored with TMA by thread 0 of the
+// promotion warps (ST_THREAD0) or by a separate store warp (ST_WARP); or written from registers
+// by each row's owner thread (ST_DIRECT: no staging buffer).
+constexpr int ST_THREAD0 = 0, ST_WARP = 1, ST_DIRECT = 2;
 // Threads of a CTA: 8 promotion warps, the producer, two MMA issuers (+ the store warp).
-template <bool SEP_STORE>
-__host__ __device__ constexpr int num_threads() { return SEP_STORE ? 384 : 352; }
+template <int SM>
+__host__ __device__ constexpr int num_threads() { return SM == ST_WARP ? 384 : 352; }
 constexpr int EPI_BAR = 1;  // named barrier of the 256 promotion/store threads
 
 
-template <Layout L, int BN, int STAGES, bool OUT_FP32>
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool STAGED>
 struct Plan {
     // TMEM partial buffers (the tensor core runs up to TB - 1 blocks ahead of the promotion) and
     // the 128-K blocks whose scales a promotion thread prefetches together; a 256-column tile
@@ -61,7 +65,7 @@ struct Plan {
     static constexpr int CPT = BN / 2;                 // output columns per promotion thread
     static constexpr int CHUNKS = BN * ESIZE / 128;    // 128-byte column chunks of a tile row
     static constexpr int CHUNK_BYTES = BM * 128;
-    static constexpr int STG_BYTES = CHUNKS * CHUNK_BYTES;
+    static constexpr int STG_BYTES = STAGED ? CHUNKS * CHUNK_BYTES : 0;
     static constexpr int RING_OFF = 0;
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
@@ -133,13 +137,15 @@ __device__ __forceinline__ int stored_rows(const TileInfo& ti, const GemmArgs& a
 
 // ------------------------------------------------------------------------- the kernel
 
-template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, bool SEP_STORE>
-__global__ void __launch_bounds__(num_threads<SEP_STORE>(), 1)
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, int SM>
+__global__ void __launch_bounds__(num_threads<SM>(), 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD8,
                    const GemmArgs a) {
-    using P = Plan<L, BN, STAGES, OUT_FP32>;
-    constexpr int NUM_THREADS = num_threads<SEP_STORE>();
+    constexpr bool SEP_STORE = SM == ST_WARP;
+    constexpr bool DIRECT = SM == ST_DIRECT;
+    using P = Plan<L, BN, STAGES, OUT_FP32, !DIRECT>;
+    constexpr int NUM_THREADS = num_threads<SM>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -195,7 +201,8 @@ __global__ void __launch_bounds__(num_threads<SEP_STORE>(), 1)
     __syncthreads();
 
     // ---------------------------------------------------------------- tile schedule
-    const int R = build_runs<L, NUM_THREADS>(a, rt, s_scan, stg);  // staging is free during set-up
+    // scratch: the staging buffer (or, without one, the ring) is free during set-up
+    const int R = build_runs<L, NUM_THREADS>(a, rt, s_scan, DIRECT ? ring : stg);
     const int num_tiles = tile_prefix<NUM_THREADS, 1>(R, a.num_nb, rt, s_scan, s_ntiles);
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
@@ -461,24 +468,15 @@ __global__ void __launch_bounds__(num_threads<SEP_STORE>(), 1)
                 }
             }
 
-            // ---- stage the tile in shared memory once the previous tile's stores have read it
-            if (tid == 0 && tix > 0) {
-                if constexpr (SEP_STORE) {
-                    if (!mbar_wait(stg_free, static_cast<uint32_t>((tix - 1) & 1), wc)) failed = true;
-                } else {
-                    bulk_wait_read_all();
-                }
-            }
-            named_bar_sync(EPI_BAR, NUM_EPI_WARPS * 32);
-            if (!failed) {
+            // this thread's row of the tile (CPT columns), written from registers
+            auto store_own_row = [&]() {
+                uint8_t* dst = static_cast<uint8_t*>(a.d) +
+                               ((grow * a.ldd) + ti.nb * BN + h2 * P::CPT) * static_cast<int64_t>(P::ESIZE);
                 constexpr int PIECES = P::CPT * P::ESIZE / 16;
 #pragma unroll
                 for (int p = 0; p < PIECES; ++p) {
-                    const int off = h2 * P::CPT * P::ESIZE + 16 * p;  // byte offset in the tile row
-                    const int chunk = off >> 7, j = (off & 127) >> 4;
-                    uint8_t* dst = stg + chunk * P::CHUNK_BYTES + row * 128 + ((j ^ (row & 7)) << 4);
                     if constexpr (OUT_FP32) {
-                        *reinterpret_cast<float4*>(dst) =
+                        *reinterpret_cast<float4*>(dst + 16 * p) =
                             make_float4(acc[4 * p], acc[4 * p + 1], acc[4 * p + 2], acc[4 * p + 3]);
                     } else {
                         uint32_t w[4];
@@ -487,49 +485,67 @@ __global__ void __launch_bounds__(num_threads<SEP_STORE>(), 1)
                             const __nv_bfloat162 h = __floats2bfloat162_rn(acc[8 * p + 2 * i], acc[8 * p + 2 * i + 1]);
                             w[i] = *reinterpret_cast<const uint32_t*>(&h);
                         }
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(dst + 16 * p) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
-            }
-            fence_async_smem();
-            if (bar_or(EPI_BAR, NUM_EPI_WARPS * 32, failed || *s_abort != 0)) break;
+            };
 
-            // ---- stores: TMA for the leading 8-row-aligned valid rows (by the store warp, or here
-            // by thread 0), owner threads for the rest
-            const int v8 = stored_rows<L>(ti, a, s_ballot + parity_slot * 4) & ~7;
-            if (tid == 0) {
-                if constexpr (SEP_STORE) {
-                    mbar_arrive(staged);
-                } else if (v8 > 0) {
-                    issue_stores(ti, v8);
-                    have_store = true;
+            if constexpr (DIRECT) {
+                // ---- every valid row by its owner thread; no barrier: a failed wait ends this
+                // warp's loop, and the abort flag ends the others' waits
+                if (failed || *s_abort != 0) break;
+                if (row_ok) store_own_row();
+            } else {
+                // ---- stage the tile in shared memory once the previous tile's stores have read it
+                if (tid == 0 && tix > 0) {
+                    if constexpr (SEP_STORE) {
+                        if (!mbar_wait(stg_free, static_cast<uint32_t>((tix - 1) & 1), wc)) failed = true;
+                    } else {
+                        bulk_wait_read_all();
+                    }
                 }
-            }
-            if (row_ok && row >= v8) {
-                    uint8_t* dst = static_cast<uint8_t*>(a.d) +
-                                   ((grow * a.ldd) + ti.nb * BN + h2 * P::CPT) * static_cast<int64_t>(P::ESIZE);
+                named_bar_sync(EPI_BAR, NUM_EPI_WARPS * 32);
+                if (!failed) {
                     constexpr int PIECES = P::CPT * P::ESIZE / 16;
 #pragma unroll
                     for (int p = 0; p < PIECES; ++p) {
+                        const int off = h2 * P::CPT * P::ESIZE + 16 * p;  // byte offset in the tile row
+                        const int chunk = off >> 7, j = (off & 127) >> 4;
+                        uint8_t* dst = stg + chunk * P::CHUNK_BYTES + row * 128 + ((j ^ (row & 7)) << 4);
                         if constexpr (OUT_FP32) {
-                            *reinterpret_cast<float4*>(dst + 16 * p) =
+                            *reinterpret_cast<float4*>(dst) =
                                 make_float4(acc[4 * p], acc[4 * p + 1], acc[4 * p + 2], acc[4 * p + 3]);
                         } else {
                             uint32_t w[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const __nv_bfloat162 h =
-                                    __floats2bfloat162_rn(acc[8 * p + 2 * i], acc[8 * p + 2 * i + 1]);
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(acc[8 * p + 2 * i], acc[8 * p + 2 * i + 1]);
                                 w[i] = *reinterpret_cast<const uint32_t*>(&h);
                             }
-                            *reinterpret_cast<uint4*>(dst + 16 * p) = make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
+                }
+                fence_async_smem();
+                if (bar_or(EPI_BAR, NUM_EPI_WARPS * 32, failed || *s_abort != 0)) break;
+
+                // ---- stores: TMA for the leading 8-row-aligned valid rows (by the store warp, or here
+                // by thread 0), owner threads for the rest
+                const int v8 = stored_rows<L>(ti, a, s_ballot + parity_slot * 4) & ~7;
+                if (tid == 0) {
+                    if constexpr (SEP_STORE) {
+                        mbar_arrive(staged);
+                    } else if (v8 > 0) {
+                        issue_stores(ti, v8);
+                        have_store = true;
+                    }
+                }
+                if (row_ok && row >= v8) store_own_row();
             }
             parity_slot ^= 1;
             ++tix;
         }
-        if (!SEP_STORE && tid == 0 && have_store) bulk_wait_all();
+        if (SM == ST_THREAD0 && tid == 0 && have_store) bulk_wait_all();
         __syncwarp();
     }
 
@@ -544,32 +560,47 @@ __global__ void __launch_bounds__(num_threads<SEP_STORE>(), 1)
 
 namespace {
 
-// Tile stores.  With few 128-K blocks per tile the tile transitions dominate, and a separate
-// store warp lets the promotion warps stage a tile and move straight on (w2 of the many-expert
-// shape, K = 256: 0.160 -> 0.136 ms); with long K thread 0 issuing the stores itself measured
-// ~3% faster (the extra warp costs the promotion loop registers / issue slots).  Both paths store
-// the same staged bytes.
-constexpr int SEP_STORE_MAX_KB = 32;
-std::atomic<int> g_force_store{0};  // 0 automatic, 1 thread 0 of the promotion warps, 2 store warp
+// Tile stores.  With few 128-K blocks per tile the tile transitions dominate: staging the tile and
+// the TMA store's shared-memory reads sit between one tile's last partial and the next tile's
+// first.  Up to 32 blocks each row's owner thread writes it from registers (no staging, no wait
+// on a store): the many-expert w2 shape (K = 256) 0.140 -> 0.124 ms at 113 tokens per expert,
+// 0.067 -> 0.052 ms at 1, and even at K = 4096.  With long K the TMA stores issued by thread 0
+// measured faster (decode, K = 7168).  A separate store warp (staged TMA stores issued while the
+// promotion warps move on) is the third path, selectable for testing.  All three write the same
+// bits.
+constexpr int DIRECT_MAX_KB = 32;
+// testing: 0 automatic, 1 thread 0 of the promotion warps, 2 store warp, 3 owner-thread stores
+std::atomic<int> g_force_store{0};
 
-bool use_sep_store(int KB) {
-    const int f = g_force_store.load(std::memory_order_relaxed);
-    return f == 0 ? KB <= SEP_STORE_MAX_KB : f == 2;
+int store_mode(int KB) {
+    switch (g_force_store.load(std::memory_order_relaxed)) {
+        case 1: return ST_THREAD0;
+        case 2: return ST_WARP;
+        case 3: return ST_DIRECT;
+        default: return KB <= DIRECT_MAX_KB ? ST_DIRECT : ST_THREAD0;
+    }
+}
+
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, int SM>
+int launch_gemm_sm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
+                   const GemmArgs& args, cudaStream_t stream) {
+    using P = Plan<L, BN, STAGES, OUT_FP32, SM != ST_DIRECT>;
+    auto kern = k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0, SM>;
+    // The attribute is per device: set it on every call (cheap, host-only, capture-safe).
+    DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL));
+    int sms = 0;
+    if (int rc = device_sm_count(&sms)) return rc;
+    return launch_pdl(kern, dim3(sms), dim3(num_threads<SM>()), P::TOTAL, stream, tA, tB, tD, tD8, args);
 }
 
 template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0>
 int launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
                 const GemmArgs& args, cudaStream_t stream) {
-    using P = Plan<L, BN, STAGES, OUT_FP32>;
-    const bool sep = use_sep_store(args.KB);
-    auto kern = sep ? k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0, true>
-                    : k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0, false>;
-    // The attribute is per device: set it on every call (cheap, host-only, capture-safe).
-    DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL));
-    int sms = 0;
-    if (int rc = device_sm_count(&sms)) return rc;
-    return launch_pdl(kern, dim3(sms), dim3(sep ? num_threads<true>() : num_threads<false>()), P::TOTAL, stream,
-                      tA, tB, tD, tD8, args);
+    switch (store_mode(args.KB)) {
+        case ST_WARP: return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_WARP>(tA, tB, tD, tD8, args, stream);
+        case ST_DIRECT: return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_DIRECT>(tA, tB, tD, tD8, args, stream);
+        default: return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_THREAD0>(tA, tB, tD, tD8, args, stream);
+    }
 }
 
 constexpr int MG_BN = 128;
@@ -849,9 +880,10 @@ extern "C" int dg_testing_mgrouped_bn(int bn) {
     return DG_OK;
 }
 
-// Who issues the tile stores: 0 automatic, 1 thread 0 of the promotion warps, 2 the store warp.
+// How the single-CTA kernel stores tiles: 0 automatic, 1 TMA stores issued by thread 0 of the
+// promotion warps, 2 TMA stores issued by the store warp, 3 owner-thread stores from registers.
 extern "C" int dg_testing_mgrouped_store(int which) {
-    DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0 (automatic), 1 (thread 0) or 2 (store warp)");
+    DG_CHECK_ARG(which >= 0 && which <= 3, "which must be 0 (automatic), 1 (thread 0), 2 (store warp) or 3 (owner threads)");
     g_force_store.store(which, std::memory_order_relaxed);
     return DG_OK;
 }

@@ -120,10 +120,10 @@ def set_token_items_per_cta(items: int):
 
 
 def set_mgrouped_store(which: str) -> None:
-    """Test hook: who issues the tile stores of the single-CTA m-grouped kernel ("auto", "thread0"
-    of the promotion warps, or a separate "warp")."""
+    """Test hook: how the single-CTA m-grouped kernel stores tiles ("auto"; TMA stores issued by
+    "thread0" of the promotion warps or by a separate "warp"; "direct" owner-thread stores)."""
     lib = _lib.load()
-    _lib.check(lib.dg_testing_mgrouped_store({"auto": 0, "thread0": 1, "warp": 2}[which]))
+    _lib.check(lib.dg_testing_mgrouped_store({"auto": 0, "thread0": 1, "warp": 2, "direct": 3}[which]))
 
 
 def set_mgrouped_bn(bn: int) -> None:

@@ -108,7 +108,8 @@ def test_pair_tiles_odd_runs_and_column_tail():
 
 @pytest.mark.parametrize("N", [512, 1024])
 def test_store_paths_bitwise_equal(mgrouped_kernel, N):
-    """Both store paths on ragged m_indices segments (store extent from the row ballots)."""
+    """The three store paths (TMA stores from thread 0 or a store warp, owner-thread stores) on
+    ragged m_indices segments (TMA store extent from the row ballots): same bits."""
     if mgrouped_kernel == "pair":
         pytest.skip("the store paths belong to the single-CTA kernel")
     counts = [130, 0, 1, 128, 257, 9]
@@ -117,13 +118,13 @@ def test_store_paths_bitwise_equal(mgrouped_kernel, N):
     b = wl.randn_bf16((len(counts), N, 384), 62, 0.02)
     outs = []
     try:
-        for which in ("thread0", "warp"):
+        for which in ("thread0", "warp", "direct"):
             set_mgrouped_store(which)
             d, _ = contiguous_case(a, b, mi, calls=2)
             outs.append(out_bits(d))
     finally:
         set_mgrouped_store("auto")
-    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
 def test_segments_out_of_expert_order():

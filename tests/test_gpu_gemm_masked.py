@@ -169,9 +169,10 @@ def test_single_and_pair_kernels_bitwise_equal(mgrouped_kernel, fmt):
 
 @pytest.mark.parametrize("N,out", [(512, torch.bfloat16), (1024, torch.bfloat16), (384, torch.float32)])
 def test_store_paths_bitwise_equal(mgrouped_kernel, N, out):
-    """Tile stores issued by thread 0 of the promotion warps or by a separate store warp: each
-    passes the oracle check (valid rows, untouched padding rows) and both give the same bits,
-    on 128- and 256-column tiles, with partial tiles that need owner-thread tails."""
+    """Tile stores by TMA (issued by thread 0 of the promotion warps or by a separate store warp)
+    or from registers by each row's owner thread: each passes the oracle check (valid rows,
+    untouched padding rows) and all give the same bits, on 128- and 256-column tiles, with
+    partial tiles that need owner-thread tails."""
     if mgrouped_kernel == "pair":
         pytest.skip("the store paths belong to the single-CTA kernel")
     G, cap, K = 3, 300, 512
@@ -179,13 +180,13 @@ def test_store_paths_bitwise_equal(mgrouped_kernel, N, out):
     b = wl.randn_bf16((G, N, K), 18, 0.02)
     outs = []
     try:
-        for which in ("thread0", "warp"):
+        for which in ("thread0", "warp", "direct"):
             set_mgrouped_store(which)
             d, _ = masked_case(a, b, [300, 77, 133], out=out, calls=2)
             outs.append(out_bits(d))
     finally:
         set_mgrouped_store("auto")
-    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
 def test_counts_out_of_range_are_clamped_and_flagged():
