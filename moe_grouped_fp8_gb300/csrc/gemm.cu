@@ -8,11 +8,12 @@
 //                output overwrites in SM90 masked GEMM", #469).
 // (The k-grouped weight-gradient GEMM lives in kgrouped.cu.)
 //
-// Roles (320 threads): warps 0-7 promote and store (TMEM lane quarter = warp % 4, column half
-// = warp / 4), warp 8 issues TMA loads, warp 9 owns tensor memory and issues tcgen05.mma.
-// Per 128-K block the MMA writes a fresh fp32 partial P into one of two TMEM buffers; the
+// Roles (352 threads, 384 with the store warp): warps 0-7 promote and store (TMEM lane quarter
+// = warp % 4, column half = warp / 4), warp 8 issues TMA loads, warps 9 and 10 issue tcgen05.mma
+// on alternate 128-K blocks (warp 9 owns tensor memory), warp 11 (optional) issues TMA stores.
+// Per 128-K block the MMA writes a fresh fp32 partial P into one of the TMEM buffers; the
 // promotion warps read it (tcgen05.ld) and accumulate acc += sfa * sfb * P in fp32 registers
-// while the tensor core fills the other buffer.  The K order is fixed, there is no split-K
+// while the tensor core fills the next buffer.  The K order is fixed, there is no split-K
 // and no atomic on outputs, so every call is bitwise reproducible.
 //
 // The tile schedule is rebuilt in shared memory by every CTA from the device-side routing
@@ -20,11 +21,12 @@
 // kernel parameters, so a CUDA graph replayed after the routing tensor changed in place never
 // uses stale schedule or descriptor state.
 //
-// Outputs: the epilogue stages the tile in shared memory (128-byte swizzle) and stores rows
-// [0, 8*floor(v/8)) of the tile's v valid leading rows with TMA boxes of 128 or 8 rows through a
-// descriptor that keeps the expert dimension (3-D [G, cap, N] for the masked layout), so a store
-// can never cross into the next expert; the remaining valid rows are written by their owner
-// threads.  Rows that are not valid are never written.
+// Outputs: with long K the epilogue stages the tile in shared memory (128-byte swizzle) and
+// stores rows [0, 8*floor(v/8)) of the tile's v valid leading rows with TMA boxes of 128 or 8
+// rows through a descriptor that keeps the expert dimension (3-D [G, cap, N] for the masked
+// layout), so a store can never cross into the next expert; the remaining valid rows are written
+// by their owner threads.  With short K every valid row is written by its owner thread from
+// registers.  Rows that are not valid are never written.
 #include <cuda_bf16.h>
 
 #include <atomic>

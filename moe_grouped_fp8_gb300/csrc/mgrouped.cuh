@@ -1,5 +1,5 @@
 // mgrouped.cuh - pieces shared by the two m-grouped FP8 GEMM kernels (gemm.cu: one CTA per
-// 128 x 128 tile; gemm_pair.cu: a CTA pair per 256 x 192 tile): the layouts, the kernel
+// 128 x 128 or 128 x 256 tile; gemm_pair.cu: a CTA pair per 256 x 192 tile): the layouts, the kernel
 // arguments, and the on-device tile schedule that every CTA rebuilds at the start of a launch
 // from the routing tensor ("SM120 m_grouped_fp8 contiguous kernel: illegal memory access at
 // CUDA graph replay", #444 - nothing derived from routing is cached across launches).
