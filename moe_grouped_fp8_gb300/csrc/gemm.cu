@@ -346,8 +346,15 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const TileInfo ti = decode_tile<L>(t, rt, R, a);
             bool failed = false;
-            bool row_ok = false;
+            // With m_indices routing and short K (owner-thread stores) a row's scales are loaded
+            // whether or not the row is valid (an invalid row's result is never stored), so that
+            // they do not wait for the row's routing entry: tiles of a few valid rows spend most
+            // of their time in such hand-offs (many-expert w2 at 1 token per expert: -11%).  With
+            // long K the waiting is hidden and the extra live registers cost more (+1-4%).
+            constexpr bool EARLY_SCALES = L == Layout::Contiguous && DIRECT;
+            bool row_ok = false, row_in = false;
             int64_t grow = 0;
+            int mi = -1;
             if constexpr (L == Layout::Masked) {
                 row_ok = row < ti.valid;
                 grow = static_cast<int64_t>(ti.e) * a.M + ti.row0 + row;
@@ -356,12 +363,17 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                 row_ok = row < ti.valid;
             } else {
                 grow = static_cast<int64_t>(ti.row0) + row;
-                const int mi = grow < a.M ? a.routing[grow] : -1;
-                row_ok = (mi == ti.e);
-                if (mi >= 0 && mi != ti.e) status_or(a.status, DG_STATUS_BAD_INDEX);
-                const uint32_t bal = __ballot_sync(0xffffffffu, row_ok);
-                if (h2 == 0 && lane == 0) s_ballot[parity_slot * 4 + q] = bal;
+                row_in = grow < a.M;
+                mi = row_in ? a.routing[grow] : -1;
+                if constexpr (!EARLY_SCALES) {
+                    row_ok = (mi == ti.e);
+                    if (mi >= 0 && mi != ti.e) status_or(a.status, DG_STATUS_BAD_INDEX);
+                    const uint32_t bal = __ballot_sync(0xffffffffu, row_ok);
+                    if (h2 == 0 && lane == 0) s_ballot[parity_slot * 4 + q] = bal;
+                }
             }
+            // the rows whose scales are loaded
+            const bool row_sc = (EARLY_SCALES && !a.psum) ? row_in : row_ok;
 
             float acc[P::CPT];
 #pragma unroll
@@ -378,7 +390,7 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                     const int kbi = g * P::SFG + u;
                     sa[u] = 0u;
                     sb[u] = 0u;
-                    if (row_ok && kbi < ti.kbt) {
+                    if (row_sc && kbi < ti.kbt) {
                         const int64_t idx = static_cast<int64_t>(kbi) * a.sfa_ld + grow;
                         if constexpr (SF_UE8M0) {
                             sa[u] = __ldg(static_cast<const uint8_t*>(a.sfa) + idx);
@@ -399,6 +411,14 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
             uint32_t sa_c[P::SFG], sb_c[P::SFG], sa_n[P::SFG], sb_n[P::SFG];
             load_group(0, sa_c, sb_c);
             load_group(1, sa_n, sb_n);
+            if constexpr (EARLY_SCALES) {
+                if (!a.psum) {
+                    row_ok = (mi == ti.e);
+                    if (mi >= 0 && mi != ti.e) status_or(a.status, DG_STATUS_BAD_INDEX);
+                    const uint32_t bal = __ballot_sync(0xffffffffu, row_ok);
+                    if (h2 == 0 && lane == 0) s_ballot[parity_slot * 4 + q] = bal;
+                }
+            }
             for (int kb0 = 0; kb0 < ti.kbt && !failed; kb0 += P::SFG) {
 #pragma unroll
                 for (int u = 0; u < P::SFG; ++u) {
