@@ -132,6 +132,11 @@ __device__ __forceinline__ void tma_store_3d(const void* tm, const void* src, in
                  : "memory");
 }
 
+// A 128-byte line into L2 (a hint: no completion, no value returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // Tile prefetches into L2 (no shared memory, no completion): a later load of the same box hits L2.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tm, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
