@@ -46,6 +46,15 @@ def dist_env():
     return ws, rank, local
 
 
+def l2_label(weight_bytes: int, act_bytes: int) -> str:
+    """How a shape's operands relate to the 129 MB L2 (inputs rotate over sets larger than L2)."""
+    if weight_bytes > 2 * L2_BYTES:
+        return "weights exceed L2"
+    if weight_bytes + act_bytes > L2_BYTES:
+        return "operands exceed L2"
+    return "L2-resident (launch-latency-bound shape)"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -409,6 +418,10 @@ class MGroupedWorkload:
             self.w = wl.masked_decode_g8()
         elif kind == "contiguous_prefill_g8":
             self.w = wl.contiguous_prefill_g8()
+        elif kind == "contiguous_balanced":
+            self.w = wl.contiguous_balanced()
+        elif kind == "masked_balanced":
+            self.w = wl.masked_balanced()
         elif kind.startswith("many_expert_"):
             _, _, which, e = kind.split("_")
             self.w = wl.many_expert(int(e[1:]), which)
@@ -512,8 +525,7 @@ class MGroupedWorkload:
     def config(self):
         w = self.w
         c = {"workload": self.name, "experts": w.G, "N": w.N, "K": w.K, "valid_rows": w.valid_rows,
-             "scales": "ue8m0" if self.fmt else "fp32", "l2": "weights exceed L2" if w.G * w.N * w.K > 2 * L2_BYTES
-             else "L2-resident (launch-latency-bound shape)"}
+             "scales": "ue8m0" if self.fmt else "fp32", "l2": l2_label(w.G * w.N * w.K, self.M * w.K)}
         if self.masked:
             c["capacity"] = w.cap
             c["expected_m"] = w.expected_m
@@ -606,8 +618,7 @@ class BF16GroupedWorkload:
     def config(self):
         w = self.w
         c = {"workload": self.name, "experts": w.G, "N": w.N, "K": w.K, "valid_rows": w.valid_rows,
-             "operands": "bf16", "l2": "weights exceed L2" if 2 * w.G * w.N * w.K > 2 * L2_BYTES
-             else "L2-resident (launch-latency-bound shape)"}
+             "operands": "bf16", "l2": l2_label(2 * w.G * w.N * w.K, 2 * self.M * w.K)}
         if self.masked:
             c["capacity"] = w.cap
             c["expected_m"] = w.expected_m
@@ -766,6 +777,12 @@ def run_ours(args, ws, rank, local):
         achieved = wk.flops / (ms_gemm * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp8_peak, 4)}
+        # The kernel-only timing runs n_kernel launches back to back; when that lasts seconds the
+        # GPU is under its power cap, the condition of the measured sustained rate (cuBLAS bf16
+        # back to back for 4 s), reported beside the burst-based fraction.
+        sus = peaks["bf16_tflops_sustained"] * (1.0 if hasattr(wk, "peak_tflops") else 2.0)
+        roof.update({"peak_sustained": round(sus, 1), "frac_sustained": round(achieved / sus, 4),
+                     "timed_s": round(n_kernel * ms_gemm * 1e-3, 2)})
     traffic, traffic_note = profiled_traffic(f"{args.workload}_gemm", wk.kernel_name, gemm_bytes)
     roof.update({"traffic": traffic, "traffic_source": traffic_note, "kernel": wk.kernel_name,
                  "algorithmic_bytes": gemm_bytes,
@@ -863,6 +880,8 @@ def main():
                     help="kgrouped_wgrad | masked_decode | masked_repro | contiguous_prefill | "
                          "many_expert_{w13,w2}_E{1,32,113} | masked_decode_g8 | contiguous_prefill_g8 | dense_prefill "
                          "(the last two: 8-expert cases for profiler captures) | "
+                         "contiguous_balanced | masked_balanced (8 experts x 4096 tokens, N=4096, K=7168: "
+                         "compute-bound) | "
                          "{masked_repro,masked_decode,contiguous_prefill}_bf16 (BF16 grouped GEMM)")
     ap.add_argument("--steps-per-graph", type=int, default=8,
                     help="consecutive steps captured in one CUDA graph (the timed region still runs exactly "

@@ -233,6 +233,20 @@ def masked_decode_g8() -> Masked:
                   seed=1004, b_scale=0.02, expected_m=192, name="masked_decode_g8")
 
 
+# Compute-bound shapes for the tensor-peak measurement: every expert holds the prefill's full
+# 4096-token batch (no padding rows, no empty experts), N=4096, K=7168, 8 experts.
+def contiguous_balanced() -> Contiguous:
+    G, per = 8, 4096
+    return Contiguous(G=G, N=4096, K=7168, counts=np.full(G, per, np.int32), m_max=G * per, seed=1006,
+                      b_scale=0.02, name="contiguous_balanced")
+
+
+def masked_balanced() -> Masked:
+    G, cap = 8, 4096
+    return Masked(G=G, cap=cap, N=4096, K=7168, counts=np.full(G, cap, np.int32), seed=1007, b_scale=0.02,
+                  expected_m=cap, name="masked_balanced")
+
+
 def many_expert(E: int, which: str = "w13", seed: int = 1005) -> Contiguous:
     G = 288
     N, K = (512, 4096) if which == "w13" else (4096, 256)
