@@ -379,8 +379,9 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
 #pragma unroll
             for (int i = 0; i < P::CPT; ++i) acc[i] = 0.0f;
 
-            // Scales travel in registers, four 128-K blocks at a time: while the blocks of group g
-            // are promoted, the loads of group g + 1 are in flight (issued one group earlier).
+            // Scales travel in registers, P::SFG 128-K blocks at a time (2 for 256-column tiles, 4
+            // for 128): while the blocks of group g are promoted, the loads of group g + 1 are in
+            // flight (issued one group earlier).
             const int sbi0 = (ti.e * a.n128 + (ti.nb * BN + h2 * P::CPT) / 128) * a.KB;
             // raw scale bits (fp32, or the UE8M0 byte): converted where used, so that no
             // instruction waits on the loads until the group's first block is promoted
