@@ -59,7 +59,6 @@ def _load():
             lib.oracle_quant_per_channel_128.argtypes = [P, i64, i64, f32, P, P]
             lib.oracle_pack_kmajor.argtypes = [P, P, i32, i64, P]
             lib.oracle_gemm_contiguous.argtypes = [P, P, P, P, P, i64, i32, i64, i64, P]
-            lib.oracle_dot_rows.argtypes = [P, P, P, P, i64, i64, P]
             lib.oracle_gemm_masked.argtypes = [P, P, P, P, P, i32, i64, i64, i64, P]
             lib.oracle_gemm_batched.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P]
             lib.oracle_gemm_kgrouped.argtypes = [P, P, P, P, P, P, i32, i64, i64, i64, P]
@@ -190,16 +189,6 @@ def gemm_contiguous(qa, sfa, qb, sfb, m_indices) -> np.ndarray:
     return d
 
 
-def dot_rows(qa_rows, sfa_rows, qb_rows, sfb_rows) -> np.ndarray:
-    """out[i] = sum_k decode(qa_rows[i,k]) sfa_rows[i,k/128] decode(qb_rows[i,k]) sfb_rows[i,k/128]."""
-    qa, sfa = _c(qa_rows, np.uint8), _c(sfa_rows, np.float32)
-    qb, sfb = _c(qb_rows, np.uint8), _c(sfb_rows, np.float32)
-    P, K = qa.shape
-    out = np.empty(P, np.float64)
-    _load().oracle_dot_rows(_p(qa), _p(sfa), _p(qb), _p(sfb), P, K, _p(out))
-    return out
-
-
 def gemm_masked(qa, sfa, qb, sfb, counts) -> np.ndarray:
     """fp64 D [G, cap, N]; rows at or past min(count, cap) are NaN."""
     qa, sfa, qb, sfb = _c(qa, np.uint8), _c(sfa, np.float32), _c(qb, np.uint8), _c(sfb, np.float32)
@@ -221,14 +210,6 @@ def gemm_batched(qa, sfa, qb, sfb, c=None) -> np.ndarray:
     d = np.empty((B, M, N), np.float64)
     _load().oracle_gemm_batched(_p(qa), _p(sfa), _p(qb), _p(sfb), _p(cc), B, M, N, K, _p(d))
     return d
-
-
-def _bf16_bits(x) -> np.ndarray:
-    """uint16 bit patterns of a bf16 torch tensor (or of a uint16 array)."""
-    if hasattr(x, "view") and not isinstance(x, np.ndarray):
-        import torch
-        x = x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    return np.ascontiguousarray(x, np.uint16)
 
 
 def gemm_masked_bf16(a, b, counts) -> np.ndarray:

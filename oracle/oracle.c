@@ -278,25 +278,6 @@ void oracle_gemm_contiguous(const uint8_t* qa, const float* sfa, const uint8_t* 
     }
 }
 
-/* Same contraction for an explicit list of (row, column) pairs of the contiguous layout;
- * used to check sampled outputs of large problems one by one.  out[i] = D[rows[i]][cols[i]]
- * or NAN when the row is not routed.  qb_rows: the codes of the needed weight rows,
- * qb_rows[i] = qb[e][cols[i]][:] with scales sfb_rows[i][K/128]. */
-void oracle_dot_rows(const uint8_t* qa_rows, const float* sfa_rows, const uint8_t* qb_rows,
-                     const float* sfb_rows, int64_t P, int64_t K, double* out) {
-    int64_t KB = K / 128;
-#pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < P; ++i) {
-        double acc = 0.0;
-        for (int64_t k = 0; k < K; ++k) {
-            double xa = g_dec[qa_rows[i * K + k]] * (double)sfa_rows[i * KB + k / 128];
-            double xb = g_dec[qb_rows[i * K + k]] * (double)sfb_rows[i * KB + k / 128];
-            acc += xa * xb;
-        }
-        out[i] = acc;
-    }
-}
-
 /* ----------------------------------------------------------------------------------------
  * m-grouped masked GEMM (#469 reproduction): for r < min(max(counts[g], 0), cap):
  *   D[g][r][n] = sum_k decode(qa[g][r][k]) sfa[g][r][k/128] * decode(qb[g][n][k]) sfb[g][n/128][k/128]

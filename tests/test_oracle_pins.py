@@ -619,3 +619,18 @@ def test_batched_gemm_equals_masked_at_full_counts_and_contiguous_single_expert(
     np.testing.assert_array_equal(got, oracle.gemm_masked(qa, sfa, qb, sfb, np.full(Bt, M, np.int32)))
     cont = oracle.gemm_contiguous(qa[0], sfa[0], qb[:1], sfb[:1], np.zeros(M, np.int32))
     np.testing.assert_array_equal(got[0], cont)
+
+
+# Plumbing that computes nothing the path does (compilation, thread count).
+_NOT_ARITHMETIC = {"build", "num_threads"}
+
+
+def test_every_exported_oracle_function_has_a_pin():
+    """Each public function of the oracle is called by at least one test in this file, so none
+    is left unpinned (a function that nothing pins must be pinned or removed)."""
+    import inspect
+    src = open(__file__).read()
+    public = [n for n, f in vars(oracle).items()
+              if inspect.isfunction(f) and not n.startswith("_") and f.__module__ == oracle.__name__]
+    missing = [n for n in public if n not in _NOT_ARITHMETIC and f"oracle.{n}(" not in src]
+    assert not missing, f"oracle functions without a pin: {missing}"
