@@ -1,18 +1,19 @@
 #!/usr/bin/env python3
 """Benchmark of the blockwise-scaled FP8 grouped-GEMM hot path on GB300.
 
-Default workload (the k-grouped wgrad of "Non-deterministic numerical problem of
-k_grouped_fp8_gemm_nt_contiguous", repro listing): Ks = [256, 128, 128, 256] (768 tokens),
-grad_y [768, 2048] = randn * 1e-7 with channel 0 zeroed in each 128-token expert,
-act [768, 2048] = randn * 0.4, D_e [2048, 2048] fp32 = C_e + grad_y_e^T act_e with C passed as D.
+Default workload: the masked decode shape of "Fix cross-expert output overwrites in SM90 masked
+GEMM" (#469), performance table, last row - G=32 experts, capacity 4096, N=6144, K=7168, per-expert
+token counts ~ Poisson(192) clipped to [0, 4096], fp32 scales, bf16 output; the largest of the
+configured workloads (541 GFLOP and 1.53 GB of weights per step).
 
-One step = one pass of the k-grouped path over one batch: the per-channel FP8 casts of grad_y
-and act (with the per-expert K-major pack) and the per-expert descriptors in one launch, then
-the k-grouped GEMM.
-Steps are captured as CUDA graphs of several consecutive steps and replayed; input sets rotate so the
-working set of consecutive steps exceeds L2.  The metric is TFLOP/s on valid rows
-(2 * sum(K_e) * N * H per step).  Other workloads (--workload) are the m-grouped configs of
-the same pages; for those a step is the activation cast plus the GEMM (weights cast ahead).
+One step = one pass of the hot path over one batch: the 1x128 per-token FP8 cast of the rows
+under each expert's count, then the masked grouped GEMM (the weights are cast once, ahead, as a
+model's are).  Steps are captured as CUDA graphs of several consecutive steps and replayed; the
+weights (1.41 GB) exceed L2, so every step streams them from HBM.  The metric is TFLOP/s on valid
+rows (2 * sum(counts) * N * K per step).  Other workloads (--workload): the k-grouped wgrad of
+"Non-deterministic numerical problem of k_grouped_fp8_gemm_nt_contiguous" (a step = both
+per-channel casts with the descriptors in one launch, then the k-grouped GEMM), the contiguous
+prefill and many-expert shapes, the BF16 GEMM and the profiling cases.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead.
 """
@@ -132,7 +133,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "k_kgrouped_gemm": ["kgrouped.cu", "kernel_common.cuh", "ptx.cuh"],
     "k_grouped_gemm": ["gemm.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
-    "k_grouped_gemm_pair": ["gemm_pair.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
+    "k_grouped_gemm_mx": ["gemm_mx.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
     "k_grouped_gemm_bf16": ["gemm_bf16.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
 }
 
@@ -420,6 +421,8 @@ class MGroupedWorkload:
             self.w = wl.contiguous_prefill_g8()
         elif kind == "contiguous_balanced":
             self.w = wl.contiguous_balanced()
+        elif kind == "contiguous_balanced_ue8m0":
+            self.w = wl.contiguous_balanced_ue8m0()
         elif kind == "masked_balanced":
             self.w = wl.masked_balanced()
         elif kind.startswith("many_expert_"):
@@ -439,14 +442,17 @@ class MGroupedWorkload:
         self.M = M
         self.a = a.view(M, K)
         # host copies of the bf16 slices the oracle sample needs (the oracle quantizes them itself)
+        # the CPU oracle's sample: every row of the expert with the most tokens (its bf16 rows and
+        # weight slab copied to the host once)
+        counts = np.clip(np.asarray(w.counts), 0, getattr(w, "cap", 1 << 30))
+        self.e_sample = int(np.argmax(counts))
+        n_rows = int(counts[self.e_sample])
         if self.masked:
-            self.e_sample = int(np.argmax(w.counts))
-            rows = np.arange(4) + self.e_sample * w.cap
+            rows = np.arange(n_rows) + self.e_sample * w.cap
         else:
-            rows = np.nonzero(w.m_indices >= 0)[0][:4]
-            self.e_sample = int(w.m_indices[rows[0]])
+            rows = np.nonzero(w.m_indices == self.e_sample)[0]
         self.a_rows = self.a[torch.from_numpy(rows).to(self.a.device)].cpu()
-        self.b_block = b[self.e_sample, :128].cpu()
+        self.b_slab = b[self.e_sample].cpu()
         self.R = 1
         self.name = f"{kind}_G{G}_N{N}_K{K}"
         if not ours:
@@ -507,20 +513,106 @@ class MGroupedWorkload:
         rows = int(np.clip(np.asarray(w.counts), 0, getattr(w, "cap", 1 << 30)).sum())  # routed rows only
         return rows * w.K * 3 + rows * (w.K // 128) * (4 if self.fmt == 0 else 1)
 
+    def segments(self):
+        """(first device row, first packed host row, rows) of every expert's token rows: the rows a
+        caller fills in the activation buffer and reads back from the output."""
+        w = self.w
+        segs, h = [], 0
+        counts = np.clip(np.asarray(w.counts), 0, getattr(w, "cap", 1 << 30))
+        if self.masked:
+            starts = [g * w.cap for g in range(w.G)]
+        else:
+            mi = w.m_indices
+            starts = [int(np.argmax(mi == e)) if c > 0 else 0 for e, c in enumerate(counts)]
+        for r0, n in zip(starts, counts):
+            if n > 0:
+                segs.append((int(r0), h, int(n)))
+                h += int(n)
+        return segs, h
+
     def e2e(self, steps, stream):
-        return None
+        """The same step through the C ABI from pinned host buffers: every step copies each expert's
+        token rows (bf16) and the routing tensor (counts or m_indices) host -> device, runs the cast
+        and the GEMM, and copies each expert's output rows device -> host.  Double-buffered as a
+        serving loop runs it: device buffers alternate between two sets, copies in and out run on
+        their own streams, so step i's D2H overlaps step i + 1's H2D and compute; events order each
+        buffer's reuse.  Returns ms per step and the bytes copied each way per step."""
+        w = self.w
+        segs, rows = self.segments()
+        idx = torch.cat([torch.arange(r0, r0 + n) for r0, _, n in segs]).to(self.a.device)
+        a_h = self.a[idx].cpu().pin_memory()
+        route_dev = self.counts if self.masked else self.mi
+        route_h = route_dev.cpu().pin_memory()
+        d_flat = self.d.view(-1, w.N)
+        d_h = [torch.empty(rows, w.N, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        bufs = [dict(a=torch.empty_like(self.a), route=torch.empty_like(route_dev), d=torch.empty_like(d_flat))
+                for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
+        for b in range(2):
+            ev["out"][b].record(stream)
+
+        def one(i):
+            b = i & 1
+            x = bufs[b]
+            s_in.wait_event(ev["out"][b])
+            with torch.cuda.stream(s_in):
+                for r0, h0, n in segs:
+                    x["a"][r0:r0 + n].copy_(a_h[h0:h0 + n], non_blocking=True)
+                x["route"].copy_(route_h, non_blocking=True)
+                ev["in"][b].record(s_in)
+            stream.wait_event(ev["in"][b])
+            with torch.cuda.stream(stream):
+                if self.masked:
+                    self.api.dg_quant_per_token_1x128(x["a"], self.qa, self.sfa, self.fmt, row_counts=x["route"])
+                    self.api.dg_m_grouped_fp8_masked(self.qa.view(w.G, w.cap, w.K), self.sfa, self.qb, self.sfb,
+                                                     x["d"].view(w.G, w.cap, w.N), x["route"], w.expected_m, self.fmt)
+                else:
+                    self.api.dg_quant_per_token_1x128_routed(x["a"], self.qa, self.sfa, x["route"], self.fmt)
+                    self.api.dg_m_grouped_fp8_contiguous(self.qa, self.sfa, self.qb, self.sfb, x["d"], x["route"],
+                                                         self.fmt)
+            ev["comp"][b].record(stream)
+            s_out.wait_event(ev["comp"][b])
+            with torch.cuda.stream(s_out):
+                for r0, h0, n in segs:
+                    d_h[b][h0:h0 + n].copy_(x["d"][r0:r0 + n], non_blocking=True)
+                ev["out"][b].record(s_out)
+
+        for i in range(4):
+            one(i)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        s_in.wait_stream(stream)
+        for i in range(steps):
+            one(i)
+        stream.wait_stream(s_out)
+        ev1.record(stream)
+        ev1.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        h2d = rows * w.K * 2 + route_h.numel() * 4
+        d2h = rows * w.N * 2
+        return ms, h2d, d2h
 
     def oracle_step(self, channels=None):
-        """Oracle on a bounded sample: 4 routed rows x the expert's first 128 output columns."""
+        """The oracle (casts of the rows and the weight slab, fp64 GEMM) on a bounded sample: every
+        row of the expert with the most tokens x its first `channels` output columns (all N by
+        default; a multiple of 128)."""
         import oracle
         w = self.w
         ue = bool(self.fmt)
+        n = w.N if channels is None else channels
+        rows = self.a_rows.shape[0]
         t0 = time.perf_counter()
         qa, sa, _ = oracle.quant_per_token_1x128(self.a_rows, ue8m0=ue)
-        qb, sb, _ = oracle.quant_block_128x128(self.b_block.unsqueeze(0), ue8m0=ue)
-        oracle.gemm_contiguous(qa, sa, qb, sb, np.zeros(4, np.int32))
+        qb, sb, _ = oracle.quant_block_128x128(self.b_slab[:n].unsqueeze(0), ue8m0=ue)
+        oracle.gemm_contiguous(qa, sa, qb, sb, np.zeros(rows, np.int32))
         dt = time.perf_counter() - t0
-        return dt, 2.0 * 4 * 128 * w.K
+        return dt, 2.0 * rows * n * w.K
+
+    def oracle_sample(self, channels=None):
+        n = self.w.N if channels is None else channels
+        return f"all {self.a_rows.shape[0]} rows of expert {self.e_sample} x {n} of {self.w.N} output columns"
 
     def config(self):
         w = self.w
@@ -718,11 +810,12 @@ def run_ours(args, ws, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     wk = make_workload(args.workload, device)
-    if args.mgrouped_kernel != "auto":
+    if args.promotion_warps or args.ue8m0_kernel != "auto":
         from moe_grouped_fp8_gb300 import _lib
-        _lib.check(_lib.load().dg_testing_mgrouped_kernel({"single": 1, "pair": 2}[args.mgrouped_kernel]))
-        if wk.kernel_name == "k_grouped_gemm" and args.mgrouped_kernel == "pair":
-            wk.kernel_name = "k_grouped_gemm_pair"
+        _lib.check(_lib.load().dg_testing_mgrouped_warps(args.promotion_warps))
+        _lib.check(_lib.load().dg_testing_mgrouped_kernel({"auto": 0, "promotion": 1, "mx": 2}[args.ue8m0_kernel]))
+    if getattr(wk, "fmt", 0) == 1 and wk.kernel_name == "k_grouped_gemm" and args.ue8m0_kernel != "promotion":
+        wk.kernel_name = "k_grouped_gemm_mx"
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
 
@@ -823,12 +916,12 @@ def cpu_baseline(wk, budget_s=12.0):
     dt, fl = wk.oracle_step()
     times.append(dt)
     flops = fl
-    while sum(times) < budget_s and len(times) < 5:
+    while sum(times) < budget_s and len(times) < 20:
         dt, _ = wk.oracle_step()
         times.append(dt)
     t = statistics.median(times)
     sample = ("the full workload (both per-channel casts, packs and the fp64 k-grouped GEMM)"
-              if isinstance(wk, KGroupedWorkload) else "4 routed rows x one 128-column block")
+              if isinstance(wk, KGroupedWorkload) else getattr(wk, "oracle_sample", lambda: "4 rows x 128 columns")())
     return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{sample}, median of {len(times)} runs ({t:.2f} s each)"}
 
@@ -842,11 +935,14 @@ def run_reference(args, ws, rank, local):
     # first `n` grad_y channels (all tokens, all experts, every act channel), n sized so that the
     # whole warm-up + timed run stays within about two minutes
     n = None
+    budget = 120.0 / max(1, args.steps + args.warmup)
     if isinstance(wk, KGroupedWorkload):
         dt64, _ = wk.oracle_step(64)
         per_ch = dt64 / 64
-        budget = 120.0 / max(1, args.steps + args.warmup)
         n = int(max(1, min(wk.N, budget / per_ch)))
+    elif hasattr(wk, "oracle_sample"):
+        dt128, _ = wk.oracle_step(128)            # output columns in blocks of 128 (the weight-cast unit)
+        n = int(max(1, min(wk.w.N // 128, budget / dt128))) * 128
     for _ in range(args.warmup):
         wk.oracle_step(n)
     t0 = time.perf_counter()
@@ -856,8 +952,12 @@ def run_reference(args, ws, rank, local):
         flops += fl
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
-    sample = (f"{n} of {wk.N} grad_y channels x all {wk.T} tokens x {wk.H} act channels per step"
-              if n is not None else "4 routed rows x one 128-column block per step")
+    if isinstance(wk, KGroupedWorkload):
+        sample = f"{n} of {wk.N} grad_y channels x all {wk.T} tokens x {wk.H} act channels per step"
+    elif hasattr(wk, "oracle_sample"):
+        sample = wk.oracle_sample(n) + " per step"
+    else:
+        sample = "4 routed rows x one 128-column block per step"
     line = {"impl": "reference", "metric": getattr(wk, "metric", "grouped FP8 GEMM TFLOP/s on valid rows; % of GB300 FP8 tensor/HBM roofline"),
             "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / max(1, args.steps) * 1e3, 3), "higher_is_better": True, "scaling": "weak",
@@ -876,8 +976,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="kgrouped_wgrad",
-                    help="kgrouped_wgrad | masked_decode | masked_repro | contiguous_prefill | "
+    ap.add_argument("--workload", default="masked_decode",
+                    help="masked_decode (the default: G=32, cap=4096, N=6144, K=7168, the largest configuration) | "
+                         "kgrouped_wgrad | masked_repro | contiguous_prefill | "
                          "many_expert_{w13,w2}_E{1,32,113} | masked_decode_g8 | contiguous_prefill_g8 | dense_prefill "
                          "(the last two: 8-expert cases for profiler captures) | "
                          "contiguous_balanced | masked_balanced (8 experts x 4096 tokens, N=4096, K=7168: "
@@ -888,9 +989,12 @@ def main():
                          "--steps steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--mgrouped-kernel", choices=["auto", "single", "pair"], default="auto",
-                    help="m-grouped FP8 GEMM kernel of bf16-output workloads: the library's choice, or one "
-                         "forced through its test hook for a comparison (outputs are bitwise equal)")
+    ap.add_argument("--ue8m0-kernel", choices=["auto", "promotion", "mx"], default="auto",
+                    help="m-grouped kernel of UE8M0-scale workloads: the library's choice (the block-scaled MMA "
+                         "kernel), or one forced through its test hook for a comparison")
+    ap.add_argument("--promotion-warps", type=int, choices=[0, 8, 16], default=0,
+                    help="promotion warps of the m-grouped FP8 GEMM's 128 x 256 tiles: 0 the library's choice, "
+                         "else forced through its test hook for a comparison (outputs are bitwise equal)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_env()

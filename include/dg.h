@@ -315,8 +315,10 @@ int dg_quant_per_channel_128_pair_psum(const void* x_a, int64_t C_a, uint8_t* q_
  *   The per-expert descriptors go to a 64 KiB array compiled into the library
  *   (2 * DG_NOALLOC_MAX_GROUPS descriptors of 128 bytes), held by every device that loads the
  *   library until the process exits.  G > DG_NOALLOC_MAX_GROUPS returns DG_ERR_UNSUPPORTED.
- *   The first call on each device looks up the array's device address (once per device, with
- *   that device current); make that first call before any stream capture.
+ *   The first call in each CUDA context (normally once per device: its primary context, with
+ *   that device current) looks up the array's device address and caches it for that context;
+ *   a context created later (after cudaDeviceReset, or a caller's own driver context) gets its
+ *   own lookup on its first call.  Make the first call in a context before any stream capture.
  *   All calls share the one array: calls that may overlap on the GPU (other streams, other
  *   host threads) race on it and must be serialised by the caller.  Every descriptor a call
  *   reads is rewritten by that same call, so nothing is carried over from the previous call.

@@ -53,6 +53,8 @@ TESTING_SIGNATURES = {
     "dg_testing_kgrouped_host_maps": (I32, [P, P, P, I32, I64, I64, P]),
     "dg_testing_kgrouped_gemm_only": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, SZ, P, P]),
     "dg_testing_mgrouped_kernel": (I32, [I32]),
+    "dg_testing_mgrouped_warps": (I32, [I32]),
+    "dg_testing_wait_limit_ns": (I32, [ctypes.c_uint64]),
     "dg_testing_mgrouped_store": (I32, [I32]),
     "dg_testing_mgrouped_bn": (I32, [I32]),
     "dg_testing_token_items_per_cta": (I32, [I32]),

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdg.so")
-SOURCES = ["host_common.cu", "quant.cu", "gemm.cu", "gemm_pair.cu", "gemm_bf16.cu", "kgrouped.cu"]
+SOURCES = ["host_common.cu", "quant.cu", "gemm.cu", "gemm_mx.cu", "gemm_bf16.cu", "kgrouped.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}"]
 
@@ -42,11 +42,21 @@ def is_stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
+def _remove_orphan_objects() -> None:
+    """Delete objects in the build folder whose source is no longer compiled, so that nothing
+    stale lies beside the library."""
+    keep = {os.path.splitext(s)[0] + ".o" for s in SOURCES}
+    for f in os.listdir(BUILD_DIR):
+        if f.endswith(".o") and f not in keep:
+            os.remove(os.path.join(BUILD_DIR, f))
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile csrc/*.cu for sm_103a and link libdg.so; returns its path."""
     if not force and not is_stale():
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
+    _remove_orphan_objects()
     nvcc = _nvcc()
 
     def compile_one(src):

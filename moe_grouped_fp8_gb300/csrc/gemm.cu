@@ -8,9 +8,10 @@
 //                output overwrites in SM90 masked GEMM", #469).
 // (The k-grouped weight-gradient GEMM lives in kgrouped.cu.)
 //
-// Roles (352 threads, 384 with the store warp): warps 0-7 promote and store (TMEM lane quarter
-// = warp % 4, column half = warp / 4), warp 8 issues TMA loads, warps 9 and 10 issue tcgen05.mma
-// on alternate 128-K blocks (warp 9 owns tensor memory), warp 11 (optional) issues TMA stores.
+// Roles (EW promotion warps + 3): warps 0..EW-1 promote and store (TMEM lane quarter = warp % 4,
+// column group = warp / 4; EW = 8 for 128-column tiles, 16 for 256-column tiles, so that a thread
+// always holds 64 accumulators), warp EW issues TMA loads, warps EW+1 and EW+2 issue tcgen05.mma on
+// alternate 128-K blocks (warp EW+1 owns tensor memory).
 // Per 128-K block the MMA writes a fresh fp32 partial P into one of the TMEM buffers; the
 // promotion warps read it (tcgen05.ld) and accumulate acc += sfa * sfb * P in fp32 registers
 // while the tensor core fills the next buffer.  The K order is fixed, there is no split-K
@@ -38,33 +39,45 @@
 
 namespace dg {
 
-constexpr int NUM_EPI_WARPS = 8;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;     // and MMA_WARP + 1: the two MMA issuers
 constexpr int NUM_MMA_WARPS = 2;
-constexpr int STORE_WARP = 11;  // with ST_WARP: issues the TMA stores of staged tiles
 // How a tile reaches the output: staged in shared memory and stored with TMA by thread 0 of the
-// promotion warps (ST_THREAD0) or by a separate store warp (ST_WARP); or written from registers
-// by each row's owner thread (ST_DIRECT: no staging buffer).
-constexpr int ST_THREAD0 = 0, ST_WARP = 1, ST_DIRECT = 2;
-// Threads of a CTA: 8 promotion warps, the producer, two MMA issuers (+ the store warp).
-template <int SM>
-__host__ __device__ constexpr int num_threads() { return SM == ST_WARP ? 384 : 352; }
-constexpr int EPI_BAR = 1;  // named barrier of the 256 promotion/store threads
+// promotion warps (ST_THREAD0), or written from registers by each row's owner thread (ST_DIRECT:
+// no staging buffer).
+constexpr int ST_THREAD0 = 0, ST_DIRECT = 1;
+// Threads of a CTA: EW promotion warps, the producer and two MMA issuers; with 16 promotion warps
+// one idle warp completes the fifth warpgroup of the register split below.
+template <int EW>
+__host__ __device__ constexpr int num_threads() { return (EW + (EW == 16 ? 4 : 1 + NUM_MMA_WARPS)) * 32; }
+
+// Register split of the 16-warp CTA (640 threads, 96 registers each at launch: an SM sub-partition
+// holds 16384 registers and runs 5 of the 20 warps).  The control warpgroup (producer, MMA issuers,
+// idle warp) gives registers back, the promotion warpgroups take them: per sub-partition
+// 4 x 32 x (RS_PROMO - RS_LAUNCH) <= 32 x (RS_LAUNCH - RS_CONTROL), so every increase is covered by
+// the decreases (an increase that the pool cannot cover would wait forever).  The host checks the
+// compiled register count equals RS_LAUNCH before it launches.
+constexpr int RS_LAUNCH = 96, RS_CONTROL = 40, RS_PROMO = 104;
+static_assert(4 * (RS_PROMO - RS_LAUNCH) <= RS_LAUNCH - RS_CONTROL, "register split exceeds the pool");
+static_assert(RS_LAUNCH * 640 <= 65536 && RS_LAUNCH * 5 * 32 <= 16384, "launch registers");
+constexpr int EPI_BAR = 1;  // named barrier of the promotion/store threads
 
 
-template <Layout L, int BN, int STAGES, bool OUT_FP32, bool STAGED>
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool STAGED, int EW>
 struct Plan {
-    // TMEM partial buffers (the tensor core runs up to TB - 1 blocks ahead of the promotion) and
-    // the 128-K blocks whose scales a promotion thread prefetches together; a 256-column tile
-    // keeps 128 accumulators per thread, which leaves room for fewer of both.
+    // TMEM partial buffers (the tensor core runs up to TB - 1 blocks ahead of the promotion; 512
+    // columns hold two 256-column or four 128-column buffers) and the 128-K blocks whose scales
+    // a promotion thread prefetches together.
     static constexpr int TB = BN == 256 ? 2 : 4;
     static constexpr int SFG = BN == 256 ? 2 : 4;
+    static constexpr int CGROUPS = EW / 4;             // column groups (warps per TMEM lane quarter)
+    // Columns of the partial loaded per tcgen05.ld round: all 64 at once when the registers allow
+    // (8 warps with 64 accumulators: 352 threads, 168 registers each), 16 beside 128 accumulators,
+    // 32 with 16 warps (608 threads, 104 registers each).
+    static constexpr int RC = EW == 16 ? 16 : (BN / CGROUPS == 64 ? 64 : 16);
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int ESIZE = OUT_FP32 ? 4 : 2;
-    static constexpr int CPT = BN / 2;                 // output columns per promotion thread
+    static constexpr int CPT = BN / CGROUPS;           // output columns per promotion thread
     static constexpr int CHUNKS = BN * ESIZE / 128;    // 128-byte column chunks of a tile row
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int STG_BYTES = STAGED ? CHUNKS * CHUNK_BYTES : 0;
@@ -72,7 +85,7 @@ struct Plan {
     static constexpr int STG_OFF = STAGES * STAGE_BYTES;
     static constexpr int SCHED_OFF = STG_OFF + STG_BYTES;
     static constexpr int BAR_OFF = (SCHED_OFF + SCHED_BYTES + 127) / 128 * 128;  // mbarriers: 8-byte aligned
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * TB + 2;  // + staged, staging free
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * TB;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int MISC_BYTES = 256;
     static constexpr int TOTAL = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
@@ -83,71 +96,25 @@ struct Plan {
     static_assert(STG_OFF % 1024 == 0 && SCHED_OFF % 1024 == 0, "TMA / swizzle buffers are 1024-byte aligned");
     static_assert(BAR_OFF % 8 == 0 && MISC_OFF % 8 == 0, "mbarrier objects are 8-byte aligned");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation: power of two <= 512");
-    static_assert(CPT <= 64 || CPT % 16 == 0, "chunked promotion");
+    static_assert(CPT % RC == 0 && (RC == 16 || RC % 32 == 0), "promotion rounds of whole loads");
+    static_assert(EW == 8 || EW == 16, "promotion warps");
     static_assert(BN == 128 || (BN == 256 && !OUT_FP32), "256-column tiles stage bf16 output only");
     static_assert(TOTAL <= 232448, "shared memory");
 };
 
-// ------------------------------------------------------------------------- small helpers
-
-struct TileInfo {
-    int e;        // expert / group
-    int nb;       // output column tile
-    int row0;     // first row of the tile: Contiguous global row, Masked row within the group
-    int valid;    // Masked: valid rows of the tile (<= 128)
-    int kbt;      // 128-K blocks of this tile
-};
-
-template <Layout L>
-__device__ __forceinline__ TileInfo decode_tile(int t, const RunTable& rt, int R, const GemmArgs& a) {
-    const int r = find_run(rt.prefix, R, t);
-    const int local = t - rt.prefix[r];
-    const int Lr = rt.L[r];
-    const int nb = local / Lr, j = local - nb * Lr;  // m-blocks fastest: consecutive tiles share B
-    TileInfo ti;
-    ti.nb = nb;
-    ti.e = rt.e[r];
-    ti.valid = 0;
-    ti.kbt = a.KB;
-    if constexpr (L == Layout::Contiguous) {
-        ti.row0 = (rt.first[r] + j) * BM;
-        if (a.psum) {
-            const int v = rt.x[r] - ti.row0;
-            ti.valid = v < BM ? v : BM;
-        }
-    } else {
-        ti.row0 = j * BM;
-        const int v = rt.x[r] - ti.row0;
-        ti.valid = v < BM ? v : BM;
-    }
-    return ti;
-}
-
-// Valid rows at the start of a tile: the count for masked / psum tiles, else the leading rows
-// whose m_indices entry is the tile's expert (ballots of the four 32-row quarters).
-template <Layout L>
-__device__ __forceinline__ int stored_rows(const TileInfo& ti, const GemmArgs& a, const uint32_t* ballot) {
-    if (L == Layout::Masked || a.psum) return ti.valid;
-    int v = 0;
-    for (int qq = 0; qq < 4; ++qq) {
-        const uint32_t bal = ballot[qq];
-        if (bal == 0xffffffffu) { v += 32; continue; }
-        return v + __ffs(~bal) - 1;
-    }
-    return v;
-}
-
 // ------------------------------------------------------------------------- the kernel
 
-template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, int SM>
-__global__ void __launch_bounds__(num_threads<SM>(), 1)
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, int SM, int EW>
+__global__ void __launch_bounds__(num_threads<EW>(), 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD8,
                    const GemmArgs a) {
-    constexpr bool SEP_STORE = SM == ST_WARP;
     constexpr bool DIRECT = SM == ST_DIRECT;
-    using P = Plan<L, BN, STAGES, OUT_FP32, !DIRECT>;
-    constexpr int NUM_THREADS = num_threads<SM>();
+    using P = Plan<L, BN, STAGES, OUT_FP32, !DIRECT, EW>;
+    constexpr int NUM_THREADS = num_threads<EW>();
+    constexpr int NUM_EPI_WARPS = EW;
+    constexpr int PRODUCER_WARP = EW;
+    constexpr int MMA_WARP = EW + 1;  // and MMA_WARP + 1: the two MMA issuers
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -160,8 +127,6 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + P::TB;
-    uint64_t* staged = tempty + P::TB;    // the promotion warps have written a tile's staging
-    uint64_t* stg_free = staged + 1;      // the store warp's TMA stores have read it
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + P::MISC_OFF);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + P::MISC_OFF + 4);
     int* s_ntiles = reinterpret_cast<int*>(smem + P::MISC_OFF + 12);
@@ -182,8 +147,6 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], NUM_EPI_WARPS);
         }
-        mbar_init(staged, 1);
-        mbar_init(stg_free, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -230,6 +193,9 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
     };
 
     // ---------------------------------------------------------------- roles
+    // (each warpgroup changes its register limit before its roles' code, which it dominates)
+    if (warp >= EW) {
+    if constexpr (EW == 16) setmaxnreg_dec<RS_CONTROL>();
     if (warp == PRODUCER_WARP) {
         if (lane == 0 && R > 0) {
             int stage = 0;
@@ -239,7 +205,7 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile<L>(t, rt, R, a);
                 for (int kb = 0; kb < ti.kbt; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_inl(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     uint8_t* sa = ring + stage * P::STAGE_BYTES;
                     uint8_t* sb = sa + P::A_BYTES;
                     mbar_arrive_expect_tx(&full[stage], P::STAGE_BYTES);
@@ -258,7 +224,7 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                 int s = stage - 1 - i;
                 uint32_t ph = phase;
                 while (s < 0) { s += STAGES; ph ^= 1u; }
-                drain_wait(&full[s], ph, a.wait_limit_ns);
+                drain_wait(&full[s], ph, a.drain_limit_ns);
             }
         }
         __syncwarp();
@@ -291,8 +257,8 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                     // (Each TMEM buffer belongs to one issuer, which consumes its phases in order.)
                     static_assert(STAGES % NUM_MMA_WARPS == 0 || P::TB <= STAGES - 1, "stage phase order");
                     static_assert(P::TB % NUM_MMA_WARPS == 0, "one issuer per TMEM buffer");
-                    if (!mbar_wait(&tempty[tb], tphase ^ 1u, wc)) { ok = false; break; }
-                    if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
+                    if (!mbar_wait_inl(&tempty[tb], tphase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_inl(&full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(ring + stage * P::STAGE_BYTES);
                     const uint32_t sb = sa + P::A_BYTES;
@@ -308,34 +274,15 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                 }
             }
             // this issuer's last commit: the tensor core is done with every MMA it issued
-            if (any) drain_wait(&tfull[last_tb], last_tphase, a.wait_limit_ns);
+            if (any) drain_wait(&tfull[last_tb], last_tphase, a.drain_limit_ns);
         }
         __syncwarp();
-    } else if (SEP_STORE && warp == STORE_WARP) {
-        // ------------------------------------------------------------ tile stores
-        // The promotion warps stage a tile and move on; this thread stores it (TMA for the leading
-        // 8-row-aligned valid rows) and hands the staging back once the stores have read it.
-        if (lane == 0 && R > 0) {
-            bool any = false;
-            int tix = 0;
-            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tix) {
-                const TileInfo ti = decode_tile<L>(t, rt, R, a);
-                if (!mbar_wait(staged, static_cast<uint32_t>(tix & 1), wc)) break;
-                const int v8 = stored_rows<L>(ti, a, s_ballot + (tix & 1) * 4) & ~7;
-                if (v8 > 0) {
-                    issue_stores(ti, v8);
-                    any = true;
-                }
-                bulk_wait_read_all();
-                mbar_arrive(stg_free);
-            }
-            if (any) bulk_wait_all();
-        }
-        __syncwarp();
+    }
     } else {
         // ------------------------------------------------------------ promotion + staging
+        if constexpr (EW == 16) setmaxnreg_inc<RS_PROMO>();
         const int q = warp & 3;       // TMEM lane quarter
-        const int h2 = warp >> 2;     // column half
+        const int h2 = warp >> 2;     // column group
         const int row = q * 32 + lane;
         const uint32_t t_lane = static_cast<uint32_t>(q * 32) << 16;
         int tb = 0;
@@ -425,46 +372,31 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                 for (int u = 0; u < P::SFG; ++u) {
                     if (kb0 + u >= ti.kbt) break;
                     const float s = scale_of(sa_c[u], sb_c[u]);
-                    if (!mbar_wait(&tfull[tb], tphase, wc)) { failed = true; break; }
+                    if (!mbar_wait_inl(&tfull[tb], tphase, wc)) { failed = true; break; }
                     tc_fence_after();
-                    if constexpr (P::CPT <= 64) {
-                        uint32_t v[P::CPT / 32][32];
+                    // P::RC columns per round: the round's loads, one wait, then (after the last
+                    // round) the TMEM buffer goes back to the MMA issuers before the round's FMAs
 #pragma unroll
-                        for (int c2 = 0; c2 < P::CPT / 32; ++c2)
-                            tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32),
-                                        v[c2]);
+                    for (int c0 = 0; c0 < P::CPT; c0 += P::RC) {
+                        constexpr int W = P::RC < 32 ? P::RC : 32;  // columns per tcgen05.ld
+                        uint32_t v[P::RC / W][W];
+                        const uint32_t col = tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c0);
 #pragma unroll
-                        for (int c2 = 0; c2 < P::CPT / 32; ++c2) tmem_wait_ld(v[c2]);
-                        // the partial is in registers: hand the TMEM buffer back before the FMAs
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty[tb]);
-                        if (++tb == P::TB) { tb = 0; tphase ^= 1u; }
+                        for (int c2 = 0; c2 < P::RC / W; ++c2) tmem_ld(col + c2 * W, v[c2]);
 #pragma unroll
-                        for (int c2 = 0; c2 < P::CPT / 32; ++c2)
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2)
-                                ffma2(acc[c2 * 32 + i], acc[c2 * 32 + i + 1], s, __uint_as_float(v[c2][i]),
-                                      __uint_as_float(v[c2][i + 1]));
-                    } else {
-                        // 128 accumulators leave room for 16 loaded columns at a time; the buffer
-                        // is handed back after the last load
-#pragma unroll
-                        for (int c2 = 0; c2 < P::CPT / 16; ++c2) {
-                            uint32_t v[16];
-                            tmem_ld_x16(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 16), v);
-                            tmem_wait_ld(v);
-                            if (c2 == P::CPT / 16 - 1) {
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(&tempty[tb]);
-                                if (++tb == P::TB) { tb = 0; tphase ^= 1u; }
-                            }
-#pragma unroll
-                            for (int i = 0; i < 16; i += 2)
-                                ffma2(acc[c2 * 16 + i], acc[c2 * 16 + i + 1], s, __uint_as_float(v[i]),
-                                      __uint_as_float(v[i + 1]));
+                        for (int c2 = 0; c2 < P::RC / W; ++c2) tmem_wait_ld(v[c2]);
+                        if (c0 + P::RC == P::CPT) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[tb]);
+                            if (++tb == P::TB) { tb = 0; tphase ^= 1u; }
                         }
+#pragma unroll
+                        for (int c2 = 0; c2 < P::RC / W; ++c2)
+#pragma unroll
+                            for (int i = 0; i < W; i += 2)
+                                ffma2(acc[c0 + c2 * W + i], acc[c0 + c2 * W + i + 1], s, __uint_as_float(v[c2][i]),
+                                      __uint_as_float(v[c2][i + 1]));
                     }
                 }
 #pragma unroll
@@ -520,13 +452,7 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                 if (row_ok) store_own_row();
             } else {
                 // ---- stage the tile in shared memory once the previous tile's stores have read it
-                if (tid == 0 && tix > 0) {
-                    if constexpr (SEP_STORE) {
-                        if (!mbar_wait(stg_free, static_cast<uint32_t>((tix - 1) & 1), wc)) failed = true;
-                    } else {
-                        bulk_wait_read_all();
-                    }
-                }
+                if (tid == 0 && tix > 0) bulk_wait_read_all();
                 named_bar_sync(EPI_BAR, NUM_EPI_WARPS * 32);
                 if (!failed) {
                     constexpr int PIECES = P::CPT * P::ESIZE / 16;
@@ -552,16 +478,12 @@ __global__ void __launch_bounds__(num_threads<SM>(), 1)
                 fence_async_smem();
                 if (bar_or(EPI_BAR, NUM_EPI_WARPS * 32, failed || *s_abort != 0)) break;
 
-                // ---- stores: TMA for the leading 8-row-aligned valid rows (by the store warp, or here
-                // by thread 0), owner threads for the rest
+                // ---- stores: TMA for the leading 8-row-aligned valid rows (issued by thread 0), owner
+                // threads for the rest
                 const int v8 = stored_rows<L>(ti, a, s_ballot + parity_slot * 4) & ~7;
-                if (tid == 0) {
-                    if constexpr (SEP_STORE) {
-                        mbar_arrive(staged);
-                    } else if (v8 > 0) {
-                        issue_stores(ti, v8);
-                        have_store = true;
-                    }
+                if (tid == 0 && v8 > 0) {
+                    issue_stores(ti, v8);
+                    have_store = true;
                 }
                 if (row_ok && row >= v8) store_own_row();
             }
@@ -588,42 +510,62 @@ namespace {
 // first.  Up to 32 blocks each row's owner thread writes it from registers (no staging, no wait
 // on a store): the many-expert w2 shape (K = 256) 0.140 -> 0.124 ms at 113 tokens per expert,
 // 0.067 -> 0.052 ms at 1, and even at K = 4096.  With long K the TMA stores issued by thread 0
-// measured faster (decode, K = 7168).  A separate store warp (staged TMA stores issued while the
-// promotion warps move on) is the third path, selectable for testing.  All three write the same
-// bits.
+// measured faster (decode, K = 7168).  Both write the same bits.
 constexpr int DIRECT_MAX_KB = 32;
-// testing: 0 automatic, 1 thread 0 of the promotion warps, 2 store warp, 3 owner-thread stores
+// testing: 0 automatic, 1 TMA stores issued by thread 0 of the promotion warps, 3 owner-thread stores
 std::atomic<int> g_force_store{0};
 
 int store_mode(int KB) {
     switch (g_force_store.load(std::memory_order_relaxed)) {
         case 1: return ST_THREAD0;
-        case 2: return ST_WARP;
         case 3: return ST_DIRECT;
         default: return KB <= DIRECT_MAX_KB ? ST_DIRECT : ST_THREAD0;
     }
 }
 
-template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, int SM>
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, int SM, int EW>
 int launch_gemm_sm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
                    const GemmArgs& args, cudaStream_t stream) {
-    using P = Plan<L, BN, STAGES, OUT_FP32, SM != ST_DIRECT>;
-    auto kern = k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0, SM>;
+    using P = Plan<L, BN, STAGES, OUT_FP32, SM != ST_DIRECT, EW>;
+    auto kern = k_grouped_gemm<L, BN, STAGES, OUT_FP32, SF_UE8M0, SM, EW>;
     // The attribute is per device: set it on every call (cheap, host-only, capture-safe).
     DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL));
+    if constexpr (EW == 16) {
+        // the register split assumes the launch gives every thread RS_LAUNCH registers
+        static int regs = 0;
+        if (regs == 0) {
+            cudaFuncAttributes fa{};
+            DG_CHECK_CUDA(cudaFuncGetAttributes(&fa, kern));
+            regs = fa.numRegs;
+        }
+        DG_CHECK_SUPPORTED(regs == RS_LAUNCH, "m-grouped kernel compiled for %d registers, its register split needs %d",
+                           regs, RS_LAUNCH);
+    }
     int sms = 0;
     if (int rc = device_sm_count(&sms)) return rc;
-    return launch_pdl(kern, dim3(sms), dim3(num_threads<SM>()), P::TOTAL, stream, tA, tB, tD, tD8, args);
+    return launch_pdl(kern, dim3(sms), dim3(num_threads<EW>()), P::TOTAL, stream, tA, tB, tD, tD8, args);
+}
+
+// Promotion warps of a 128 x 256 tile: 16 (64 accumulators per thread, the partial read in two
+// 32-column rounds) or 8 (128 accumulators, eight 16-column rounds).  testing: 0 automatic.
+std::atomic<int> g_force_warps{0};
+
+template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0, int EW>
+int launch_gemm_ew(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
+                   const GemmArgs& args, cudaStream_t stream) {
+    if (store_mode(args.KB) == ST_DIRECT)
+        return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_DIRECT, EW>(tA, tB, tD, tD8, args, stream);
+    return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_THREAD0, EW>(tA, tB, tD, tD8, args, stream);
 }
 
 template <Layout L, int BN, int STAGES, bool OUT_FP32, bool SF_UE8M0>
 int launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
                 const GemmArgs& args, cudaStream_t stream) {
-    switch (store_mode(args.KB)) {
-        case ST_WARP: return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_WARP>(tA, tB, tD, tD8, args, stream);
-        case ST_DIRECT: return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_DIRECT>(tA, tB, tD, tD8, args, stream);
-        default: return launch_gemm_sm<L, BN, STAGES, OUT_FP32, SF_UE8M0, ST_THREAD0>(tA, tB, tD, tD8, args, stream);
+    if constexpr (BN == 256) {
+        if (g_force_warps.load(std::memory_order_relaxed) != 8)
+            return launch_gemm_ew<L, BN, STAGES, OUT_FP32, SF_UE8M0, 16>(tA, tB, tD, tD8, args, stream);
     }
+    return launch_gemm_ew<L, BN, STAGES, OUT_FP32, SF_UE8M0, 8>(tA, tB, tD, tD8, args, stream);
 }
 
 constexpr int MG_BN = 128;
@@ -651,23 +593,22 @@ CUtensorMapDataType out_tmap_type(int out) {
     return out == DG_OUT_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
-// Kernel choice.  The single-CTA kernel (128 x 128 or 128 x 256 tiles) and the CTA-pair kernel
-// (256 x PAIR_BN tiles, gemm_pair.cu, bf16 output only) promote the same fp32 tensor-core
-// partials in the same K order with the same FMAs, so their outputs are bitwise identical.  With
-// 128 x 256 tiles the single-CTA kernel measured faster than the pairs on every configured shape
-// (decode 0.419 vs 0.425 ms, prefill 0.329 vs 0.457 ms), so calls run on single CTAs; the pair
-// kernel is reached through the test hook, which keeps it under the parity tests.
-std::atomic<int> g_force_kernel{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA pairs
+// Kernel choice for UE8M0 scales: the block-scaled MMA kernel (gemm_mx.cu: the tensor core applies
+// the power-of-two scales and accumulates the whole K, no per-block promotion), or the promotion
+// kernel above (fp32 promotion per 128-K block; the only choice for fp32 scales).  The two round
+// differently (the tensor core's accumulation order against fp32 promotion), each within the
+// oracle's tolerance.  testing: 0 automatic, 1 promotion, 2 block-scaled MMA.
+std::atomic<int> g_force_kernel{0};
 
-bool use_pair(int out, bool /*prefer_pair*/) {
-    if (out != DG_OUT_BF16) return false;
-    return g_force_kernel.load(std::memory_order_relaxed) == 2;
+bool use_mx(int fmt) {
+    if (fmt != DG_SF_UE8M0) return false;
+    return g_force_kernel.load(std::memory_order_relaxed) != 1;
 }
 
 template <Layout L>
-int dispatch_mgrouped(bool pair, int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB,
-                      const CUtensorMap& tD, const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
-    if (pair) return launch_mgrouped_pair(L, fmt == DG_SF_UE8M0, tA, tB, tD, tD8, args, s);
+int dispatch_mgrouped(int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD,
+                      const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
+    if (use_mx(fmt)) return launch_mgrouped_mx(L, out == DG_OUT_FP32, tA, tB, args, s);
     const int bn = single_bn(out, args.N);
     args.num_nb = static_cast<int>(args.N / bn);
     // bf16 output stages half as much as fp32, which leaves room for a fifth ring stage
@@ -729,7 +670,7 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     const int esize = out_dtype == DG_OUT_FP32 ? 4 : 2;
     const int64_t M = static_cast<int64_t>(G) * cap;
     const int64_t Mp = sf_format == DG_SF_FP32 ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
-    const bool pair = use_pair(out_dtype, expected_m > BM);
+    (void)expected_m;  // a hint only: the schedule comes from the device-side counts
     CUtensorMap tA, tB, tD, tD8;
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(cap), static_cast<uint64_t>(G)};
@@ -742,7 +683,7 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = pair ? PAIR_B_ROWS : static_cast<uint32_t>(single_bn(out_dtype, N));
+        const uint32_t brows = use_mx(sf_format) ? 128u : static_cast<uint32_t>(single_bn(out_dtype, N));
         uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
@@ -767,6 +708,7 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     args.d = d;
     args.status = status;
     args.wait_limit_ns = wait_limit_ns();
+    args.drain_limit_ns = drain_limit_ns();
     args.M = cap;
     args.sfa_ld = Mp;
     args.ldd = N;
@@ -775,7 +717,7 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     args.KB = static_cast<int>(K / BK);
     args.n128 = static_cast<int>(N / 128);
     args.N = N;
-    return dispatch_mgrouped<Layout::Masked>(pair, out_dtype, sf_format, tA, tB, tD, tD8, args,
+    return dispatch_mgrouped<Layout::Masked>(out_dtype, sf_format, tA, tB, tD, tD8, args,
                                              static_cast<cudaStream_t>(stream));
 }
 
@@ -794,7 +736,6 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     DG_CHECK_SUPPORTED((M + BM - 1) / BM <= DG_MAX_M_BLOCKS, "M too large (at most %d rows)", DG_MAX_M_BLOCKS * BM);
     const int esize = out_dtype == DG_OUT_FP32 ? 4 : 2;
     const int64_t Mp = sf_format == DG_SF_FP32 ? (M + 3) / 4 * 4 : (M + 15) / 16 * 16;
-    const bool pair = use_pair(out_dtype, false);
     CUtensorMap tA, tB, tD, tD8;
     {
         uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
@@ -807,7 +748,7 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = pair ? PAIR_B_ROWS : static_cast<uint32_t>(single_bn(out_dtype, N));
+        const uint32_t brows = use_mx(sf_format) ? 128u : static_cast<uint32_t>(single_bn(out_dtype, N));
         uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
@@ -833,6 +774,7 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     args.d = d;
     args.status = status;
     args.wait_limit_ns = wait_limit_ns();
+    args.drain_limit_ns = drain_limit_ns();
     args.M = M;
     args.sfa_ld = Mp;
     args.ldd = N;
@@ -841,7 +783,7 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     args.KB = static_cast<int>(K / BK);
     args.n128 = static_cast<int>(N / 128);
     args.N = N;
-    return dispatch_mgrouped<Layout::Contiguous>(pair, out_dtype, sf_format, tA, tB, tD, tD8, args,
+    return dispatch_mgrouped<Layout::Contiguous>(out_dtype, sf_format, tA, tB, tD, tD8, args,
                                                  static_cast<cudaStream_t>(stream));
 }
 
@@ -903,17 +845,25 @@ extern "C" int dg_testing_mgrouped_bn(int bn) {
     return DG_OK;
 }
 
-// How the single-CTA kernel stores tiles: 0 automatic, 1 TMA stores issued by thread 0 of the
-// promotion warps, 2 TMA stores issued by the store warp, 3 owner-thread stores from registers.
+// How the kernel stores tiles: 0 automatic, 1 TMA stores issued by thread 0 of the promotion
+// warps, 3 owner-thread stores from registers.
 extern "C" int dg_testing_mgrouped_store(int which) {
-    DG_CHECK_ARG(which >= 0 && which <= 3, "which must be 0 (automatic), 1 (thread 0), 2 (store warp) or 3 (owner threads)");
+    DG_CHECK_ARG(which == 0 || which == 1 || which == 3, "which must be 0 (automatic), 1 (thread 0) or 3 (owner threads)");
     g_force_store.store(which, std::memory_order_relaxed);
     return DG_OK;
 }
 
-// The m-grouped kernel of bf16-output calls: 0 automatic, 1 single-CTA tiles, 2 CTA pairs.
+// The m-grouped kernel of UE8M0-scale calls: 0 automatic, 1 the promotion kernel, 2 the
+// block-scaled MMA kernel.
 extern "C" int dg_testing_mgrouped_kernel(int which) {
-    DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0, 1 or 2");
+    DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0 (automatic), 1 (promotion) or 2 (block-scaled MMA)");
     g_force_kernel.store(which, std::memory_order_relaxed);
+    return DG_OK;
+}
+
+// Promotion warps of 128 x 256 tiles: 0 automatic (16), 8 or 16.
+extern "C" int dg_testing_mgrouped_warps(int warps) {
+    DG_CHECK_ARG(warps == 0 || warps == 8 || warps == 16, "warps must be 0, 8 or 16");
+    g_force_warps.store(warps, std::memory_order_relaxed);
     return DG_OK;
 }

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 int s = stage - 1 - i;
                 uint32_t ph = phase;
                 while (s < 0) { s += STAGES; ph ^= 1u; }
-                drain_wait(&full[s], ph, a.wait_limit_ns);
+                drain_wait(&full[s], ph, a.drain_limit_ns);
             }
         }
         __syncwarp();
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 int lt = tb - 1;
                 uint32_t lp = tphase;
                 if (lt < 0) { lt = H_TBUFS - 1; lp ^= 1u; }
-                drain_wait(&tfull[lt], lp, a.wait_limit_ns);
+                drain_wait(&tfull[lt], lp, a.drain_limit_ns);
             }
         }
         __syncwarp();
@@ -449,6 +449,7 @@ extern "C" int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, i
     args.d = d;
     args.status = status;
     args.wait_limit_ns = wait_limit_ns();
+    args.drain_limit_ns = drain_limit_ns();
     args.M = cap;
     args.ldd = N;
     args.N = N;
@@ -483,6 +484,7 @@ extern "C" int dg_m_grouped_bf16_contiguous(const void* a, const void* b, void* 
     args.d = d;
     args.status = status;
     args.wait_limit_ns = wait_limit_ns();
+    args.drain_limit_ns = drain_limit_ns();
     args.M = M;
     args.ldd = N;
     args.N = N;

@@ -1,4 +1,5 @@
 // host_common.cu - error state, device properties, TMA descriptor encoding, workspace sizes.
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -41,7 +42,7 @@ int device_sm_count(int* out) {
     return DG_OK;
 }
 
-uint64_t wait_limit_ns() {
+uint64_t drain_limit_ns() {
     static uint64_t v = [] {
         const char* s = std::getenv("DG_WAIT_LIMIT_MS");
         long long ms = s ? std::atoll(s) : 2000;
@@ -49,6 +50,15 @@ uint64_t wait_limit_ns() {
         return static_cast<uint64_t>(ms) * 1000000ull;
     }();
     return v;
+}
+
+namespace {
+std::atomic<uint64_t> g_wait_override_ns{0};
+}
+
+uint64_t wait_limit_ns() {
+    const uint64_t o = g_wait_override_ns.load(std::memory_order_relaxed);
+    return o != 0 ? o : drain_limit_ns();
 }
 
 int encode_tmap(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t rank, const void* base,
@@ -83,4 +93,12 @@ extern "C" size_t dg_workspace_size(int op, int G, int64_t M, int64_t N, int64_t
     (void)K;
     if (op == DG_OP_K_GROUPED_WGRAD && G > 0) return static_cast<size_t>(G) * 2 * 128;  // two tensor maps per expert
     return 0;
+}
+
+// Test hook: the limit of the kernels' work waits for later calls in this process (0 restores the
+// default).  Drains on the way out keep the default limit, so that a kernel whose work waits gave
+// up still waits for the copies and MMAs it issued before it frees tensor memory and exits.
+extern "C" int dg_testing_wait_limit_ns(uint64_t ns) {
+    dg::g_wait_override_ns.store(ns, std::memory_order_relaxed);
+    return DG_OK;
 }

@@ -41,9 +41,12 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count(int* out);
 
-// Upper bound, in nanoseconds, of every spin-wait inside the kernels (env DG_WAIT_LIMIT_MS,
-// default 2000 ms).
+// Upper bound, in nanoseconds, of the kernels' work waits (env DG_WAIT_LIMIT_MS, default 2000 ms;
+// a test hook may shorten it).
 uint64_t wait_limit_ns();
+// Upper bound of the waits that drain a kernel's copies and MMAs on its way out (the default limit,
+// never shortened by the test hook).
+uint64_t drain_limit_ns();
 
 // cuTensorMapEncodeTiled through cudaGetDriverEntryPointByVersion; returns DG_OK or an error
 // code with a message.

@@ -84,7 +84,8 @@ struct Args {
     const float* sfb;            // [K_cap/128][H]
     const CUtensorMap* maps;     // per expert: A_e, B_e
     int32_t* status;
-    uint64_t wait_limit_ns;
+    uint64_t wait_limit_ns;      // work waits
+    uint64_t drain_limit_ns;     // drains of issued copies / MMAs on the way out
     int64_t K_cap;
     int G;
     int N;
@@ -280,14 +281,14 @@ __global__ void __launch_bounds__(NT, 1) k_kgrouped_gemm(const __grid_constant__
                 int s = stage - 1 - i;
                 uint32_t ph = phase;
                 while (s < 0) { s += STAGES; ph ^= 1u; }
-                drain_wait(&full[s], ph, a.wait_limit_ns);
+                drain_wait(&full[s], ph, a.drain_limit_ns);
             }
             const int s_drain = issued < SSLOTS ? issued : SSLOTS;
             for (int i = 0; i < s_drain; ++i) {
                 int s = sslot - 1 - i;
                 uint32_t ph = sphase;
                 while (s < 0) { s += SSLOTS; ph ^= 1u; }
-                drain_wait(&sfull[s], ph, a.wait_limit_ns);
+                drain_wait(&sfull[s], ph, a.drain_limit_ns);
             }
         }
         __syncwarp();
@@ -312,7 +313,7 @@ __global__ void __launch_bounds__(NT, 1) k_kgrouped_gemm(const __grid_constant__
             const int c_drain = c_issued < CSLOTS ? c_issued : CSLOTS;
             for (int i = 0; i < c_drain; ++i) {
                 const int j = c_issued - 1 - i;
-                drain_wait(&cfull[j % CSLOTS], (j / CSLOTS) & 1, a.wait_limit_ns);
+                drain_wait(&cfull[j % CSLOTS], (j / CSLOTS) & 1, a.drain_limit_ns);
             }
         }
         __syncwarp();
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(NT, 1) k_kgrouped_gemm(const __grid_constant__
                 int lt = tb - 1;
                 uint32_t lp = tphase;
                 if (lt < 0) { lt = TBUFS - 1; lp ^= 1u; }
-                drain_wait(&tfull[lt], lp, a.wait_limit_ns);
+                drain_wait(&tfull[lt], lp, a.drain_limit_ns);
             }
         }
         __syncwarp();
@@ -661,6 +662,7 @@ int launch(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed, c
     args.maps = ws;
     args.status = status;
     args.wait_limit_ns = wait_limit_ns();
+    args.drain_limit_ns = drain_limit_ns();
     args.K_cap = K_cap;
     args.G = G;
     args.N = static_cast<int>(N);
@@ -743,32 +745,64 @@ extern "C" int dg_k_grouped_fp8_wgrad_psum(const uint8_t* a_packed, const float*
 // dg_k_grouped_fp8_wgrad_noalloc: the same k-grouped call, with its descriptor scratch in a
 // fixed array compiled into the library instead of a caller-provided workspace.  Every device
 // that loads the library holds the array (DG_NOALLOC_MAX_GROUPS experts x two 128-byte
-// descriptors = 64 KiB) until the process exits.
+// descriptors = 64 KiB) until the process exits (or its context is destroyed).
 namespace dg {
 namespace {
 
 static __device__ __align__(256) CUtensorMap g_noalloc_maps[2 * DG_NOALLOC_MAX_GROUPS];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
+// (CUDA context, device address of g_noalloc_maps in it); the address is looked up once per
+// context (normally once per device: its primary context), so a context created later (after a
+// device reset, or a caller's own driver context) gets its own lookup.
+struct ScratchEntry {
+    CUcontext ctx;
+    void* addr;
+};
+ScratchEntry g_noalloc_cache[64] = {};
+int g_noalloc_next = 0;
 
-// Device address of g_noalloc_maps on the current device.  In host code the array's name only
-// stands in for the symbol, so the address is looked up once per device (with that device
-// current) and cached; the first call on each device does this set-up.
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+
+CUcontext current_context() {
+    static PFN_ctxGetCurrent fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<PFN_ctxGetCurrent>(nullptr);
+        return reinterpret_cast<PFN_ctxGetCurrent>(f);
+    }();
+    CUcontext c = nullptr;
+    if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of g_noalloc_maps in the calling thread's current context.  In host code the
+// array's name only stands in for the symbol, so the address is looked up with
+// cudaGetSymbolAddress (which also initialises the device's primary context when no context is
+// current yet) and cached per context.
 int noalloc_scratch(void** out) {
-    int dev = 0;
-    DG_CHECK_CUDA(cudaGetDevice(&dev));
-    DG_CHECK_SUPPORTED(dev >= 0 && dev < 64, "device index %d", dev);
+    CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_maps);
-        if (e != cudaSuccess || p == nullptr)
-            return set_error(DG_ERR_CUDA, "cudaGetSymbolAddress of the built-in descriptor scratch failed: %s",
-                             cudaGetErrorString(e));
-        g_noalloc_addr[dev] = p;
+    if (ctx != nullptr) {
+        for (const ScratchEntry& e : g_noalloc_cache)
+            if (e.ctx == ctx && e.addr != nullptr) {
+                *out = e.addr;
+                return DG_OK;
+            }
     }
-    *out = g_noalloc_addr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_maps);
+    if (e != cudaSuccess || p == nullptr)
+        return set_error(DG_ERR_CUDA, "cudaGetSymbolAddress of the built-in descriptor scratch failed: %s",
+                         cudaGetErrorString(e));
+    if (ctx == nullptr) ctx = current_context();  // the lookup made the primary context current
+    if (ctx != nullptr) {
+        g_noalloc_cache[g_noalloc_next] = ScratchEntry{ctx, p};
+        g_noalloc_next = (g_noalloc_next + 1) % 64;
+    }
+    *out = p;
     return DG_OK;
 }
 

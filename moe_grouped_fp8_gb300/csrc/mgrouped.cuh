@@ -1,11 +1,11 @@
-// mgrouped.cuh - pieces shared by the two m-grouped FP8 GEMM kernels (gemm.cu: one CTA per
-// 128 x 128 or 128 x 256 tile; gemm_pair.cu: a CTA pair per 256 x 192 tile): the layouts, the kernel
-// arguments, and the on-device tile schedule that every CTA rebuilds at the start of a launch
+// mgrouped.cuh - pieces shared by the m-grouped GEMM kernels (gemm.cu, gemm_bf16.cu): the
+// layouts, the kernel arguments, and the on-device tile schedule that every CTA rebuilds at the start of a launch
 // from the routing tensor ("SM120 m_grouped_fp8 contiguous kernel: illegal memory access at
 // CUDA graph replay", #444 - nothing derived from routing is cached across launches).
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 #include <cstdint>
 
@@ -26,7 +26,8 @@ struct GemmArgs {
     const void* sfb;
     void* d;                     // output base (owner-thread stores of tail rows)
     int32_t* status;
-    uint64_t wait_limit_ns;
+    uint64_t wait_limit_ns;      // work waits
+    uint64_t drain_limit_ns;     // drains of issued copies / MMAs on the way out
     int64_t M;       // Contiguous: rows; Masked: cap
     int64_t sfa_ld;  // Mp of the [K/128][Mp] activation scales
     int64_t ldd;     // output row length in elements
@@ -198,12 +199,57 @@ __device__ int tile_prefix(int R, int num_nb, const RunTable& rt, int* s_scan, i
     return *s_ntiles;
 }
 
-// The CTA-pair kernel (bf16 output only), defined in gemm_pair.cu: output tiles of 256 rows x
-// PAIR_BN columns; its B tensor map has boxes of 128 (K) x PAIR_B_ROWS rows.
-constexpr int PAIR_BN = 192;
-constexpr int PAIR_B_ROWS = PAIR_BN / 2;
-// Returns DG_OK or an error.
-int launch_mgrouped_pair(Layout L, bool sf_ue8m0, const CUtensorMap& tA, const CUtensorMap& tB,
-                         const CUtensorMap& tD, const CUtensorMap& tD8, GemmArgs args, void* stream);
+// The block-scaled MMA kernel for UE8M0 scales (gemm_mx.cu): 128 x 128 tiles; its B tensor map has
+// boxes of 128 (K) x 128 rows.  Returns DG_OK or an error.
+int launch_mgrouped_mx(Layout L, bool out_fp32, const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
+                       cudaStream_t stream);
+
+// A tile of the launch's schedule (decoded from its index by every role of a CTA).
+struct TileInfo {
+    int e;        // expert / group
+    int nb;       // output column tile
+    int row0;     // first row of the tile: Contiguous global row, Masked row within the group
+    int valid;    // Masked: valid rows of the tile (<= 128)
+    int kbt;      // 128-K blocks of this tile
+};
+
+template <Layout L>
+__device__ __forceinline__ TileInfo decode_tile(int t, const RunTable& rt, int R, const GemmArgs& a) {
+    const int r = find_run(rt.prefix, R, t);
+    const int local = t - rt.prefix[r];
+    const int Lr = rt.L[r];
+    const int nb = local / Lr, j = local - nb * Lr;  // m-blocks fastest: consecutive tiles share B
+    TileInfo ti;
+    ti.nb = nb;
+    ti.e = rt.e[r];
+    ti.valid = 0;
+    ti.kbt = a.KB;
+    if constexpr (L == Layout::Contiguous) {
+        ti.row0 = (rt.first[r] + j) * BM;
+        if (a.psum) {
+            const int v = rt.x[r] - ti.row0;
+            ti.valid = v < BM ? v : BM;
+        }
+    } else {
+        ti.row0 = j * BM;
+        const int v = rt.x[r] - ti.row0;
+        ti.valid = v < BM ? v : BM;
+    }
+    return ti;
+}
+
+// Valid rows at the start of a tile: the count for masked / psum tiles, else the leading rows
+// whose m_indices entry is the tile's expert (ballots of the four 32-row quarters).
+template <Layout L>
+__device__ __forceinline__ int stored_rows(const TileInfo& ti, const GemmArgs& a, const uint32_t* ballot) {
+    if (L == Layout::Masked || a.psum) return ti.valid;
+    int v = 0;
+    for (int qq = 0; qq < 4; ++qq) {
+        const uint32_t bal = ballot[qq];
+        if (bal == 0xffffffffu) { v += 32; continue; }
+        return v + __ffs(~bal) - 1;
+    }
+    return v;
+}
 
 }  // namespace dg

@@ -90,9 +90,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     return mbar_wait_slow(bar, parity, w);
 }
 
+// The same wait with its slow path inlined: for kernels that change their register limit with
+// setmaxnreg, whose code may not call functions compiled for another limit.
+__device__ __forceinline__ bool mbar_wait_inl(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            status_or(w.status, DG_STATUS_TIMEOUT);
+            *w.abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // Named barrier over `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Per-thread register limit of the executing warpgroup (all four warps execute the same form):
+// `dec` returns registers to the CTA's pool, `inc` waits until the pool can grant them.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------------------- TMA
@@ -223,6 +252,48 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4 (block-scaled) with e4m3 A and B (both
+// K-major), an fp32 accumulator and UE8M0 scale factors: bits 4-5 B scale-factor id, 7-9 A format
+// (0 = e4m3), 10-12 B format (0 = e4m3), 15/16 A/B major (0 = K), 17-22 N >> 3, 23 scale type
+// (1 = UE8M0), 24-28 M >> 4, 29-30 A scale-factor id, 31 K size (0 = dense K 32).  The scale-factor
+// ids pick the byte of each 32-bit tensor-memory word that holds a row's scale; both are 0 here.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3_ue8m0(int M, int N) {
+    return (0u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (0u << 29);
+}
+
+// D[tmem] (+)= (A . 2^sfa)[smem] * (B . 2^sfb)[smem]^T, M x N x 32 (e4m3) with one UE8M0 scale per
+// row of A and of B for the instruction's 32-element K block (scale_vec::1X), read from tensor
+// memory at sfa_tmem / sfb_tmem.  Issued by one thread.
+__device__ __forceinline__ void umma_mxf8_1x(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte matrix stored without swizzle, rows contiguous
+// (8-row core matrices 128 bytes apart: stride byte offset 128, one core matrix along K so the
+// leading byte offset is unused), the source form of tcgen05.cp.32x128b.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;  // layout bits 61-63 = 0: no swizzle
+}
+
+// Copy 32 rows x 128 bits from shared memory into tensor-memory lanes 0-31, columns taddr ..
+// taddr + 3, replicated into each of the four 32-lane quarters.  Issued by one thread; ordered
+// before later tcgen05.mma of the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16 with bf16 A and B (both K-major) and an fp32
 // accumulator: bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 // 15/16 A/B major (0 = K), 17-22 N >> 3, 24-28 M >> 4.  A and B always share the bf16 type.
@@ -273,6 +344,10 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+
+// A warp's 32 TMEM lanes x W consecutive columns (W = 16 or 32), by array size.
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld_x16(taddr, r); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld_x32(taddr, r); }
 
 // tcgen05.wait::ld naming the 16 registers of an earlier tmem_ld_x16 (see the 32-register form).
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {

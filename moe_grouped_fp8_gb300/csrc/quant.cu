@@ -27,17 +27,24 @@ namespace {
 // several 16-byte loads are in flight per thread.  Item indices advance incrementally by the
 // items a pass covers (no division in the loop).  Three launch shapes share the item code:
 //   rows:    one CTA per chunk of rows_per_cta rows of one row group; it returns at once when
-//            the chunk lies past the group's count.  With several groups the group is the grid's
-//            x axis, so the chunks that hold rows (the first ones of every group) are dispatched
-//            first and the empty ones after them;
+//            the chunk lies past the group's count (groups on the grid's x axis: the chunks that
+//            hold rows are dispatched first).  Used without row counts, and for more groups than
+//            the walk below keeps in shared memory;
+//   masked:  a grid of resident CTAs walks one index space of the valid rows only (the rows under
+//            each group's count, numbered group after group): every CTA forms the prefix of the
+//            clamped counts, then takes chunks of rows_per_cta valid rows by a grid stride and
+//            maps each to its group and row.  No CTA is launched for rows past the counts, which
+//            in decode (192 rows of a 4096-row capacity) are 95% of the grid above;
 //   routed:  CTA x owns rows_per_cta rows and compacts those whose m_indices entry is >= 0.
-// rows_per_cta gives each CTA about TOKEN_ITEMS_PER_CTA items.
+// rows_per_cta gives each CTA about TOKEN_ITEMS_PER_CTA items (TOKEN_WALK_ITEMS for the walk).
 // ---------------------------------------------------------------------------------------
 constexpr int TOKEN_ITEMS_PER_HW = 4;
 constexpr int TOKEN_ITEMS_PER_CTA = 512;
 constexpr int TOKEN_MIN_ITEMS_PER_CTA = 128;
 constexpr int TOKEN_CTAS_PER_SM = 4;  // resident 256-thread CTAs at the kernels' register counts
 constexpr int TOKEN_PER_WARP = 2 * TOKEN_ITEMS_PER_HW;
+constexpr int TOKEN_WALK_ITEMS = 256;       // items per chunk of the masked walk
+constexpr int TOKEN_WALK_MAX_GROUPS = 1024; // groups whose prefix the masked walk keeps
 
 __device__ __forceinline__ uint4 token_load(const uint16_t* x, int64_t ldx, bool live, int64_t m, int kb, int sub) {
     return live ? __ldg(reinterpret_cast<const uint4*>(x + m * ldx + static_cast<int64_t>(kb) * 128) + sub)
@@ -128,6 +135,47 @@ __global__ void __launch_bounds__(256) k_quant_token_1x128(const uint16_t* __res
     const int64_t r_end = min(lim, r_begin + rows_per_cta);
     token_rows<UE8M0, false>(x, K, ldx, q, sfa, Mp, sf_zero, g * rpg + r_begin, nullptr,
                              static_cast<int>(r_end - r_begin));
+}
+
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) k_quant_token_masked(const uint16_t* __restrict__ x, int64_t K, int64_t ldx,
+                                                            uint8_t* __restrict__ q, void* sfa, int64_t Mp,
+                                                            float sf_zero, const int32_t* __restrict__ row_counts,
+                                                            int G, int64_t rpg, int rows_per_cta) {
+    __shared__ int s_prefix[TOKEN_WALK_MAX_GROUPS + 1];
+    __shared__ int s_rows[256];
+    __shared__ int s_scan[8];
+    pdl_trigger();
+    pdl_wait();
+    const int t = threadIdx.x;
+    // prefix of the clamped counts: thread t sums a contiguous slice of the groups
+    const int ch = (G + 255) / 256;
+    const int lo = min(G, t * ch), hi = min(G, lo + ch);
+    int sum = 0;
+    for (int g = lo; g < hi; ++g) {
+        const int64_t c = row_counts[g];
+        sum += static_cast<int>(c < 0 ? 0 : (c > rpg ? rpg : c));
+    }
+    int total = 0;
+    int p = cta_excl_scan<256>(sum, s_scan, &total);
+    for (int g = lo; g < hi; ++g) {
+        s_prefix[g] = p;
+        const int64_t c = row_counts[g];
+        p += static_cast<int>(c < 0 ? 0 : (c > rpg ? rpg : c));
+    }
+    if (t == 0) s_prefix[G] = total;
+    __syncthreads();
+    for (int f0 = static_cast<int>(blockIdx.x) * rows_per_cta; f0 < total; f0 += static_cast<int>(gridDim.x) * rows_per_cta) {
+        const int n = min(rows_per_cta, total - f0);
+        if (t < n) {
+            const int f = f0 + t;
+            const int g = find_run(s_prefix, G, f);  // the group whose valid rows hold f
+            s_rows[t] = static_cast<int>(g * rpg) + (f - s_prefix[g]);
+        }
+        __syncthreads();
+        token_rows<UE8M0, true>(x, K, ldx, q, sfa, Mp, sf_zero, 0, s_rows, n);
+        __syncthreads();
+    }
 }
 
 template <bool UE8M0>
@@ -283,6 +331,20 @@ extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int
         rpg = M / G;
     }
     const int64_t groups = row_counts != nullptr ? G : 1;
+    const bool ue = sf_format == DG_SF_UE8M0;
+    if (row_counts != nullptr && G <= TOKEN_WALK_MAX_GROUPS && M < (1ll << 31)) {
+        // the walk over valid rows: resident CTAs (two per resident slot), chunks of about
+        // TOKEN_WALK_ITEMS items (or the test hook's count)
+        const int64_t KB = K / 128;
+        const int64_t want = g_token_items.load(std::memory_order_relaxed) > 0 ? g_token_items.load() : TOKEN_WALK_ITEMS;
+        const int rpc = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(256, want / KB)));
+        int sms = 0;
+        if (int rc = device_sm_count(&sms)) return rc;
+        const int64_t grid = std::min<int64_t>((M + rpc - 1) / rpc, 2ll * TOKEN_CTAS_PER_SM * sms);
+        return launch_pdl(ue ? k_quant_token_masked<true> : k_quant_token_masked<false>, dim3(static_cast<unsigned>(grid)),
+                          dim3(256), 0, static_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(x), K, ldx, q,
+                          sfa, token_mp(M, sf_format), sf_zero, row_counts, G, rpg, rpc);
+    }
     const int64_t rows_per_cta = token_rows_per_cta(K / 128, M, row_counts != nullptr, 1ll << 30);
     const int64_t chunks = (rpg + rows_per_cta - 1) / rows_per_cta;
     // groups on x (fastest dispatch) when there are several and the chunks fit the y axis
@@ -290,7 +352,6 @@ extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int
     DG_CHECK_SUPPORTED(group_in_x || (chunks < (1ll << 31) && groups < 65536), "too many rows or groups");
     const dim3 grid = group_in_x ? dim3(static_cast<unsigned>(groups), static_cast<unsigned>(chunks))
                                  : dim3(static_cast<unsigned>(chunks), static_cast<unsigned>(groups));
-    const bool ue = sf_format == DG_SF_UE8M0;
     return launch_pdl(ue ? k_quant_token_1x128<true> : k_quant_token_1x128<false>, grid, dim3(256), 0,
                       static_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(x), K, ldx, q, sfa,
                       token_mp(M, sf_format), sf_zero, row_counts, rpg, rows_per_cta, group_in_x);

@@ -241,6 +241,14 @@ def contiguous_balanced() -> Contiguous:
                       b_scale=0.02, name="contiguous_balanced")
 
 
+def contiguous_balanced_ue8m0() -> Contiguous:
+    """contiguous_balanced with UE8M0 scales on both operands (the scale format of the many-expert
+    shapes on a compute-bound shape)."""
+    G, per = 8, 4096
+    return Contiguous(G=G, N=4096, K=7168, counts=np.full(G, per, np.int32), m_max=G * per, seed=1006,
+                      b_scale=0.02, ue8m0=True, name="contiguous_balanced_ue8m0")
+
+
 def masked_balanced() -> Masked:
     G, cap = 8, 4096
     return Masked(G=G, cap=cap, N=4096, K=7168, counts=np.full(G, cap, np.int32), seed=1007, b_scale=0.02,

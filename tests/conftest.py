@@ -11,6 +11,7 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: takes more than a few seconds on the CPU")
+    config.addinivalue_line("markers", "ue8m0: a GPU case with UE8M0 scales that runs on both m-grouped kernels")
 
 
 @pytest.fixture(scope="session")

@@ -107,10 +107,16 @@ def ref_out(d64: np.ndarray, fp32_out: bool) -> np.ndarray:
 
 
 def set_mgrouped_kernel(which: str) -> None:
-    """Test hook: the m-grouped kernel of later bf16-output calls ("auto", "single" 128 x 128
-    CTA tiles, "pair" 256 x 192 CTA-pair tiles)."""
+    """Test hook: the m-grouped kernel of later UE8M0-scale calls ("auto", "promotion" per-128-K fp32
+    promotion, "mx" the block-scaled MMA kernel)."""
     lib = _lib.load()
-    _lib.check(lib.dg_testing_mgrouped_kernel({"auto": 0, "single": 1, "pair": 2}[which]))
+    _lib.check(lib.dg_testing_mgrouped_kernel({"auto": 0, "promotion": 1, "mx": 2}[which]))
+
+
+def set_mgrouped_warps(warps: int) -> None:
+    """Test hook: promotion warps of 128 x 256 tiles (0 automatic, 8 or 16)."""
+    lib = _lib.load()
+    _lib.check(lib.dg_testing_mgrouped_warps(int(warps)))
 
 
 def set_token_items_per_cta(items: int):
@@ -120,10 +126,10 @@ def set_token_items_per_cta(items: int):
 
 
 def set_mgrouped_store(which: str) -> None:
-    """Test hook: how the single-CTA m-grouped kernel stores tiles ("auto"; TMA stores issued by
-    "thread0" of the promotion warps or by a separate "warp"; "direct" owner-thread stores)."""
+    """Test hook: how the m-grouped kernel stores tiles ("auto"; TMA stores issued by "thread0" of
+    the promotion warps; "direct" owner-thread stores)."""
     lib = _lib.load()
-    _lib.check(lib.dg_testing_mgrouped_store({"auto": 0, "thread0": 1, "warp": 2, "direct": 3}[which]))
+    _lib.check(lib.dg_testing_mgrouped_store({"auto": 0, "thread0": 1, "direct": 3}[which]))
 
 
 def set_mgrouped_bn(bn: int) -> None:

@@ -9,17 +9,20 @@ from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_BAD_INDEX, 
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
-                         sentinel_value, set_mgrouped_kernel, set_mgrouped_store, sync, to_f64)
+                         sentinel_value, set_mgrouped_kernel, set_mgrouped_store, set_mgrouped_warps, sync, to_f64)
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["auto", "pair"], autouse=True)
-def mgrouped_kernel(request):
-    """Every case runs on the kernel the library picks ("auto": single-CTA tiles, 128 x 256 when
-    N % 256 == 0 and N >= 1024); small cases also run on the CTA-pair kernel."""
-    if request.param == "pair" and request.node.get_closest_marker("slow"):
-        pytest.skip("full-size cases run on the default kernel")
+@pytest.fixture(params=["auto", "promotion"], autouse=True)
+def ue8m0_kernel(request):
+    """Calls with UE8M0 scales run on the kernel the library picks (the block-scaled MMA kernel) and
+    again on the promotion kernel; fp32-scale cases and full-size cases run once."""
+    if request.param == "promotion":
+        cs = getattr(request.node, "callspec", None)
+        fmt = cs.params.get("fmt") if cs is not None else None
+        if request.node.get_closest_marker("slow") or (fmt != DG_SF_UE8M0 and not request.node.get_closest_marker("ue8m0")):
+            pytest.skip("one kernel for this case")
     set_mgrouped_kernel(request.param)
     yield request.param
     set_mgrouped_kernel("auto")
@@ -96,9 +99,8 @@ def test_all_padding_and_ragged_last_block():
     contiguous_case(a, b, mi2)
 
 
-def test_pair_tiles_odd_runs_and_column_tail():
-    """Runs of 5, 1, 3 and 1 m-blocks (a CTA pair's odd block is computed, never stored) and
-    N = 640 (three 192-column tiles and a 64-column tail)."""
+def test_odd_runs_and_narrow_tiles():
+    """Runs of 5, 1, 3 and 1 m-blocks and N = 640 (five 128-column tiles)."""
     counts = [640, 1, 0, 300, 128]
     mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
     a = wl.randn_bf16((mi.size, 256), 95)
@@ -107,24 +109,43 @@ def test_pair_tiles_odd_runs_and_column_tail():
 
 
 @pytest.mark.parametrize("N", [512, 1024])
-def test_store_paths_bitwise_equal(mgrouped_kernel, N):
-    """The three store paths (TMA stores from thread 0 or a store warp, owner-thread stores) on
-    ragged m_indices segments (TMA store extent from the row ballots): same bits."""
-    if mgrouped_kernel == "pair":
-        pytest.skip("the store paths belong to the single-CTA kernel")
+def test_store_paths_bitwise_equal(N):
+    """The two store paths (TMA stores issued by thread 0, owner-thread stores) on ragged m_indices
+    segments (TMA store extent from the row ballots): same bits."""
     counts = [130, 0, 1, 128, 257, 9]
     mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
     a = wl.randn_bf16((mi.size, 384), 61, 1.5)
     b = wl.randn_bf16((len(counts), N, 384), 62, 0.02)
     outs = []
     try:
-        for which in ("thread0", "warp", "direct"):
+        for which in ("thread0", "direct"):
             set_mgrouped_store(which)
             d, _ = contiguous_case(a, b, mi, calls=2)
             outs.append(out_bits(d))
     finally:
         set_mgrouped_store("auto")
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+def test_promotion_warps_bitwise_equal(fmt):
+    """128 x 256 tiles promoted by 16 warps (64 accumulators each) or by 8 (128 each): each passes
+    the oracle check and both give the same bits, with both store paths."""
+    counts = [130, 0, 1, 128, 257, 9]
+    mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
+    for K in (384, 4224):                               # owner-thread stores / staged TMA stores
+        a = wl.randn_bf16((mi.size, K), 63, 1.5)
+        b = wl.randn_bf16((len(counts), 1024, K), 64, 0.02)
+        outs = []
+        try:
+            for warps in (16, 8):
+                set_mgrouped_warps(warps)
+                d, _ = contiguous_case(a, b, mi, fmt=fmt)
+                outs.append(out_bits(d))
+        finally:
+            set_mgrouped_warps(0)
+        assert np.array_equal(outs[0], outs[1]), f"K={K}"
+
 
 
 def test_segments_out_of_expert_order():
@@ -288,13 +309,14 @@ def replay_case(G, N, K, E, replays, check_every, seed, mode="m_indices"):
     assert checked >= replays // check_every
 
 
+@pytest.mark.ue8m0
 @pytest.mark.parametrize("mode", ["m_indices", "psum", "routed"])
 def test_graph_replay_with_changed_routing_small(mode):
     replay_case(G=16, N=256, K=256, E=20, replays=30, check_every=3, seed=7, mode=mode)
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("which,E", [("w13", 1), ("w13", 32), ("w2", 113)])
+@pytest.mark.parametrize("which,E", [("w13", 1), ("w13", 32), ("w13", 113), ("w2", 1), ("w2", 32), ("w2", 113)])
 def test_many_expert_ue8m0_graph_replay(which, E):
     """G=288 many-expert shapes, UE8M0 scales, 100 replays with re-drawn routing (every 10th
     replay checked against the oracle on sampled rows)."""
@@ -330,14 +352,20 @@ def test_prefill_shape_full_size_sampled():
     assert_close(np.concatenate(gpu_vals), np.concatenate(ref_vals), False, "prefill sampled")
     pad = torch.from_numpy(mi < 0).cuda()
     assert bool((d.view(torch.int16)[pad] == -1).all()), "padding rows written"
+    # the whole of the largest expert: every one of its rows x every output column
+    e = int(np.argmax(w.counts))
+    rows = np.nonzero(mi == e)[0]
+    oqb, osfb, _ = oracle.quant_block_128x128(b[e:e + 1].cpu())
+    np.testing.assert_array_equal(qb[e].cpu().numpy(), oqb[0])
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a[torch.from_numpy(rows).cuda()].cpu())
+    ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, np.zeros(rows.size, np.int32))
+    assert_close(to_f64(d[torch.from_numpy(rows).cuda()]), ref_out(ref, False), False, f"prefill expert {e} whole")
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("mode", ["m_indices", "psum"])
-def test_determinism_10000_calls(mgrouped_kernel, mode):
+def test_determinism_10000_calls(mode):
     """Ragged segments routed by m_indices or psum: 10,000 calls, each bitwise equal to the first."""
-    if mgrouped_kernel == "pair":
-        pytest.skip("the default kernel")
     counts = [130, 0, 1, 128, 257, 9]
     G, N, K = len(counts), 1024, 512
     m_max = wl.contiguous_capacity(sum(counts), G)

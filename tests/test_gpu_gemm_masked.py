@@ -9,18 +9,21 @@ from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, DG_STATUS_COUNT_GT_CA
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_bits, ref_out, sentinel_like,
-                         sentinel_value, set_mgrouped_bn, set_mgrouped_kernel, set_mgrouped_store, sync,
+                         sentinel_value, set_mgrouped_bn, set_mgrouped_kernel, set_mgrouped_store, set_mgrouped_warps, sync,
                          to_f64)
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["auto", "pair"], autouse=True)
-def mgrouped_kernel(request):
-    """Every case runs on the kernel the library picks ("auto": single-CTA tiles, 128 x 256 when
-    N % 256 == 0 and N >= 1024); small cases also run on the CTA-pair kernel."""
-    if request.param == "pair" and request.node.get_closest_marker("slow"):
-        pytest.skip("full-size cases run on the default kernel")
+@pytest.fixture(params=["auto", "promotion"], autouse=True)
+def ue8m0_kernel(request):
+    """Calls with UE8M0 scales run on the kernel the library picks (the block-scaled MMA kernel) and
+    again on the promotion kernel; fp32-scale cases and full-size cases run once."""
+    if request.param == "promotion":
+        cs = getattr(request.node, "callspec", None)
+        fmt = cs.params.get("fmt") if cs is not None else None
+        if request.node.get_closest_marker("slow") or (fmt != DG_SF_UE8M0 and not request.node.get_closest_marker("ue8m0")):
+            pytest.skip("one kernel for this case")
     set_mgrouped_kernel(request.param)
     yield request.param
     set_mgrouped_kernel("auto")
@@ -93,8 +96,8 @@ def test_formats_and_output_dtypes(fmt, out):
     masked_case(a, b, [200, 77, 129], fmt=fmt, out=out)
 
 
-def test_pair_tiles_odd_blocks_and_column_tail():
-    """Groups of 5 and 4 m-blocks (the last pair of the first is half empty), N = 640."""
+def test_odd_blocks_and_narrow_tiles():
+    """Groups of 5 and 4 m-blocks (partial last blocks), N = 640 (five 128-column tiles)."""
     G, cap, N, K = 2, 640, 640, 256
     a = wl.randn_bf16((G, cap, K), 97)
     b = wl.randn_bf16((G, N, K), 98, 0.05)
@@ -102,24 +105,28 @@ def test_pair_tiles_odd_blocks_and_column_tail():
 
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
-def test_wide_tiles(fmt):
-    """N = 1024: the single-CTA kernel runs 128 x 256 tiles (bitwise equal to the pair kernel,
-    checked in the test above for the narrow case)."""
-    G, cap, N, K = 3, 300, 1024, 384
+@pytest.mark.parametrize("K", [384, 4224])
+def test_wide_tiles_promotion_warps_bitwise_equal(fmt, K):
+    """N = 1024: 128 x 256 tiles, promoted by 16 warps (64 accumulators per thread, the default)
+    or by 8 (128 each); both pass the oracle check and give the same bits, with owner-thread stores
+    (K = 384) and staged TMA stores (K = 4224, 33 blocks)."""
+    G, cap, N = 3, 300, 1024
     a = wl.randn_bf16((G, cap, K), 15, 2.0)
     b = wl.randn_bf16((G, N, K), 16, 0.02)
-    d, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
-    set_mgrouped_kernel("pair")
-    d2, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
-    set_mgrouped_kernel("auto")
-    assert np.array_equal(out_bits(d), out_bits(d2))
+    outs = []
+    try:
+        for warps in (16, 8):
+            set_mgrouped_warps(warps)
+            d, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
+            outs.append(out_bits(d))
+    finally:
+        set_mgrouped_warps(0)
+    assert np.array_equal(outs[0], outs[1])
 
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
-def test_tile_widths_bitwise_equal(mgrouped_kernel, fmt):
+def test_tile_widths_bitwise_equal(fmt):
     """The same call on 128- and 256-column tiles: both pass the oracle check, same bits."""
-    if mgrouped_kernel == "pair":
-        pytest.skip("tile widths belong to the single-CTA kernel")
     G, cap, N, K = 3, 260, 512, 640
     a = wl.randn_bf16((G, cap, K), 19, 2.0)
     b = wl.randn_bf16((G, N, K), 20, 0.02)
@@ -151,42 +158,24 @@ def test_expected_m_does_not_change_result():
     assert np.array_equal(out_bits(d1), out_bits(d2))
 
 
-@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
-def test_single_and_pair_kernels_bitwise_equal(mgrouped_kernel, fmt):
-    """Both m-grouped kernels give the same bits, so the choice between them has no numerical effect."""
-    if mgrouped_kernel == "pair":
-        pytest.skip("runs both kernels itself")
-    G, cap, N, K = 3, 300, 640, 512
-    a = wl.randn_bf16((G, cap, K), 13, 2.0)
-    b = wl.randn_bf16((G, N, K), 14, 0.02)
-    outs = []
-    for which in ("single", "pair"):
-        set_mgrouped_kernel(which)
-        d, _ = masked_case(a, b, [300, 77, 129], fmt=fmt)
-        outs.append(out_bits(d))
-    assert np.array_equal(outs[0], outs[1])
-
-
 @pytest.mark.parametrize("N,out", [(512, torch.bfloat16), (1024, torch.bfloat16), (384, torch.float32)])
-def test_store_paths_bitwise_equal(mgrouped_kernel, N, out):
-    """Tile stores by TMA (issued by thread 0 of the promotion warps or by a separate store warp)
-    or from registers by each row's owner thread: each passes the oracle check (valid rows,
-    untouched padding rows) and all give the same bits, on 128- and 256-column tiles, with
-    partial tiles that need owner-thread tails."""
-    if mgrouped_kernel == "pair":
-        pytest.skip("the store paths belong to the single-CTA kernel")
+def test_store_paths_bitwise_equal(N, out):
+    """Tile stores by TMA (issued by thread 0 of the promotion warps) or from registers by each
+    row's owner thread: each passes the oracle check (valid rows, untouched padding rows) and both
+    give the same bits, on 128- and 256-column tiles, with partial tiles that need owner-thread
+    tails."""
     G, cap, K = 3, 300, 512
     a = wl.randn_bf16((G, cap, K), 17, 1.5)
     b = wl.randn_bf16((G, N, K), 18, 0.02)
     outs = []
     try:
-        for which in ("thread0", "warp", "direct"):
+        for which in ("thread0", "direct"):
             set_mgrouped_store(which)
             d, _ = masked_case(a, b, [300, 77, 133], out=out, calls=2)
             outs.append(out_bits(d))
     finally:
         set_mgrouped_store("auto")
-    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert np.array_equal(outs[0], outs[1])
 
 
 def test_counts_out_of_range_are_clamped_and_flagged():
@@ -244,6 +233,14 @@ def test_decode_shape_full_size_sampled():
     rows = torch.arange(cap, device="cuda")[None, :]
     pad = rows >= cnt[:, None]
     assert bool((d.view(torch.int16)[pad] == -1).all()), "padding rows written"
+    # the whole of the largest expert: every valid row x every output column
+    g = int(np.argmax(w.counts))
+    c = int(w.counts[g])
+    oqb, osfb, _ = oracle.quant_block_128x128(b[g:g + 1].cpu())
+    np.testing.assert_array_equal(qb[g].cpu().numpy(), oqb[0])
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a[g, :c].cpu())
+    ref = oracle.gemm_masked(oqa.reshape(1, c, K), osfa.reshape(1, c, K // 128), oqb, osfb, [c])
+    assert_close(to_f64(d[g, :c]), ref_out(ref[0], False), False, f"decode expert {g} whole")
 
 
 def test_graph_replay_with_changed_counts():
@@ -305,11 +302,9 @@ def test_graph_replay_with_changed_counts():
 
 
 @pytest.mark.slow
-def test_determinism_10000_calls(mgrouped_kernel):
+def test_determinism_10000_calls():
     """The pages' reproduction shape (G=8, cap=32, N=K=256, its counts): 10,000 calls, each
     bitwise equal to the first; and 2,000 on a 128 x 256-tile shape with partial blocks."""
-    if mgrouped_kernel == "pair":
-        pytest.skip("the default kernel")
     for (G, cap, N, K, counts, iters) in [(8, 32, 256, 256, [0, 1, 16, 31, 32, 1, 32, 32], 10000),
                                           (4, 300, 1024, 768, [300, 7, 129, 0], 2000)]:
         a = wl.randn_bf16((G, cap, K), 37, 1.0, device="cuda")
