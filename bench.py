@@ -815,7 +815,10 @@ def run_ours(args, ws, rank, local):
         _lib.check(_lib.load().dg_testing_mgrouped_warps(args.promotion_warps))
         _lib.check(_lib.load().dg_testing_mgrouped_kernel({"auto": 0, "promotion": 1, "mx": 2}[args.ue8m0_kernel]))
     if getattr(wk, "fmt", 0) == 1 and wk.kernel_name == "k_grouped_gemm" and args.ue8m0_kernel != "promotion":
-        wk.kernel_name = "k_grouped_gemm_mx"
+        # the library's rule: UE8M0 scales with N % 256 == 0 run the block-scaled kernel when K has
+        # at least 16 blocks (or when it is forced)
+        if wk.w.N % 256 == 0 and (wk.w.K // 128 >= 16 or args.ue8m0_kernel == "mx"):
+            wk.kernel_name = "k_grouped_gemm_mx"
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
 

@@ -70,8 +70,8 @@ struct Plan {
     static constexpr int SFG = BN == 256 ? 2 : 4;
     static constexpr int CGROUPS = EW / 4;             // column groups (warps per TMEM lane quarter)
     // Columns of the partial loaded per tcgen05.ld round: all 64 at once when the registers allow
-    // (8 warps with 64 accumulators: 352 threads, 168 registers each), 16 beside 128 accumulators,
-    // 32 with 16 warps (608 threads, 104 registers each).
+    // (8 warps with 64 accumulators: 352 threads, 168 registers each), 16 beside 128 accumulators
+    // (8 warps of a 128 x 256 tile), 16 with 16 warps (104 registers each after the split).
     static constexpr int RC = EW == 16 ? 16 : (BN / CGROUPS == 64 ? 64 : 16);
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
@@ -594,21 +594,29 @@ CUtensorMapDataType out_tmap_type(int out) {
 }
 
 // Kernel choice for UE8M0 scales: the block-scaled MMA kernel (gemm_mx.cu: the tensor core applies
-// the power-of-two scales and accumulates the whole K, no per-block promotion), or the promotion
-// kernel above (fp32 promotion per 128-K block; the only choice for fp32 scales).  The two round
-// differently (the tensor core's accumulation order against fp32 promotion), each within the
-// oracle's tolerance.  testing: 0 automatic, 1 promotion, 2 block-scaled MMA.
+// the power-of-two scales and accumulates the whole K of a 128 x 256 tile, no per-block promotion)
+// when N % 256 == 0 and K has at least MX_MIN_KB blocks, else the promotion kernel above (fp32
+// promotion per 128-K block; the only choice for fp32 scales).  Measured: the block-scaled kernel
+// 0.704 ms against 0.812 ms on a compute-bound shape (8 x 4096 rows, N = 4096, K = 7168), equal or
+// up to 4% faster on the many-expert w13 shapes (K = 4096); with K = 256 (w2) its single
+// accumulator leaves the tensor core idle during each tile's drain and the promotion kernel wins.
+// The two round differently (the tensor core's accumulation order against fp32 promotion), each
+// within the oracle's tolerance.  testing: 0 automatic, 1 promotion, 2 block-scaled MMA wherever
+// N % 256 == 0.
 std::atomic<int> g_force_kernel{0};
+constexpr int MX_MIN_KB = 16;
 
-bool use_mx(int fmt) {
-    if (fmt != DG_SF_UE8M0) return false;
-    return g_force_kernel.load(std::memory_order_relaxed) != 1;
+bool use_mx(int fmt, int64_t N, int64_t K) {
+    if (fmt != DG_SF_UE8M0 || N % MX_BN != 0) return false;
+    const int f = g_force_kernel.load(std::memory_order_relaxed);
+    if (f == 1 || g_force_bn.load(std::memory_order_relaxed) == MG_BN) return false;
+    return f == 2 || K / BK >= MX_MIN_KB;
 }
 
 template <Layout L>
 int dispatch_mgrouped(int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD,
                       const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
-    if (use_mx(fmt)) return launch_mgrouped_mx(L, out == DG_OUT_FP32, tA, tB, args, s);
+    if (use_mx(fmt, args.N, args.K)) return launch_mgrouped_mx(L, out == DG_OUT_FP32, tA, tB, args, s);
     const int bn = single_bn(out, args.N);
     args.num_nb = static_cast<int>(args.N / bn);
     // bf16 output stages half as much as fp32, which leaves room for a fifth ring stage
@@ -683,7 +691,7 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = use_mx(sf_format) ? 128u : static_cast<uint32_t>(single_bn(out_dtype, N));
+        const uint32_t brows = static_cast<uint32_t>(use_mx(sf_format, N, K) ? MX_BN : single_bn(out_dtype, N));
         uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
@@ -748,7 +756,7 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = use_mx(sf_format) ? 128u : static_cast<uint32_t>(single_bn(out_dtype, N));
+        const uint32_t brows = static_cast<uint32_t>(use_mx(sf_format, N, K) ? MX_BN : single_bn(out_dtype, N));
         uint32_t box[3] = {BK, brows, 1};
         if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
@@ -854,7 +862,7 @@ extern "C" int dg_testing_mgrouped_store(int which) {
 }
 
 // The m-grouped kernel of UE8M0-scale calls: 0 automatic, 1 the promotion kernel, 2 the
-// block-scaled MMA kernel.
+// block-scaled MMA kernel wherever N % 256 == 0 (and no 128-column tile width is forced).
 extern "C" int dg_testing_mgrouped_kernel(int which) {
     DG_CHECK_ARG(which >= 0 && which <= 2, "which must be 0 (automatic), 1 (promotion) or 2 (block-scaled MMA)");
     g_force_kernel.store(which, std::memory_order_relaxed);

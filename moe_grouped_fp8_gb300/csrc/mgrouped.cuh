@@ -199,8 +199,9 @@ __device__ int tile_prefix(int R, int num_nb, const RunTable& rt, int* s_scan, i
     return *s_ntiles;
 }
 
-// The block-scaled MMA kernel for UE8M0 scales (gemm_mx.cu): 128 x 128 tiles; its B tensor map has
-// boxes of 128 (K) x 128 rows.  Returns DG_OK or an error.
+// The block-scaled MMA kernel for UE8M0 scales (gemm_mx.cu): 128 x 256 tiles, N % 256 == 0; its
+// B tensor map has boxes of 128 (K) x 256 rows.  Returns DG_OK or an error.
+constexpr int MX_BN = 256;
 int launch_mgrouped_mx(Layout L, bool out_fp32, const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
                        cudaStream_t stream);
 

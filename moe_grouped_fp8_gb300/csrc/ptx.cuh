@@ -256,10 +256,10 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint6
 // K-major), an fp32 accumulator and UE8M0 scale factors: bits 4-5 B scale-factor id, 7-9 A format
 // (0 = e4m3), 10-12 B format (0 = e4m3), 15/16 A/B major (0 = K), 17-22 N >> 3, 23 scale type
 // (1 = UE8M0), 24-28 M >> 4, 29-30 A scale-factor id, 31 K size (0 = dense K 32).  The scale-factor
-// ids pick the byte of each 32-bit tensor-memory word that holds a row's scale; both are 0 here.
-__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3_ue8m0(int M, int N) {
-    return (0u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(M >> 4) << 24) | (0u << 29);
+// ids pick the byte of each 32-bit tensor-memory word that holds a row's scale (id i: bits 8i..8i+7).
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3_ue8m0(int M, int N, uint32_t sfa_id = 0, uint32_t sfb_id = 0) {
+    return ((sfb_id & 3u) << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | ((sfa_id & 3u) << 29);
 }
 
 // D[tmem] (+)= (A . 2^sfa)[smem] * (B . 2^sfb)[smem]^T, M x N x 32 (e4m3) with one UE8M0 scale per

@@ -14,11 +14,12 @@ from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_b
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["auto", "promotion"], autouse=True)
+@pytest.fixture(params=["auto", "promotion", "mx"], autouse=True)
 def ue8m0_kernel(request):
-    """Calls with UE8M0 scales run on the kernel the library picks (the block-scaled MMA kernel) and
-    again on the promotion kernel; fp32-scale cases and full-size cases run once."""
-    if request.param == "promotion":
+    """Calls with UE8M0 scales run on the kernel the library picks, then forced onto the promotion
+    kernel and onto the block-scaled MMA kernel (where N % 256 == 0); fp32-scale cases and full-size
+    cases run once, on the library's choice."""
+    if request.param != "auto":
         cs = getattr(request.node, "callspec", None)
         fmt = cs.params.get("fmt") if cs is not None else None
         if request.node.get_closest_marker("slow") or (fmt != DG_SF_UE8M0 and not request.node.get_closest_marker("ue8m0")):
@@ -128,9 +129,12 @@ def test_store_paths_bitwise_equal(N):
 
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
-def test_promotion_warps_bitwise_equal(fmt):
-    """128 x 256 tiles promoted by 16 warps (64 accumulators each) or by 8 (128 each): each passes
-    the oracle check and both give the same bits, with both store paths."""
+def test_promotion_warps_bitwise_equal(ue8m0_kernel, fmt):
+    """128 x 256 tiles of the promotion kernel promoted by 16 warps (64 accumulators each) or by 8
+    (128 each): each passes the oracle check and both give the same bits, with both store paths."""
+    if ue8m0_kernel != "auto":
+        pytest.skip("a property of the promotion kernel, forced below")
+    set_mgrouped_kernel("promotion")
     counts = [130, 0, 1, 128, 257, 9]
     mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
     for K in (384, 4224):                               # owner-thread stores / staged TMA stores
@@ -360,6 +364,32 @@ def test_prefill_shape_full_size_sampled():
     oqa, osfa, _ = oracle.quant_per_token_1x128(a[torch.from_numpy(rows).cuda()].cpu())
     ref = oracle.gemm_contiguous(oqa, osfa, oqb, osfb, np.zeros(rows.size, np.int32))
     assert_close(to_f64(d[torch.from_numpy(rows).cuda()]), ref_out(ref, False), False, f"prefill expert {e} whole")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["m_indices", "psum"])
+def test_block_scaled_determinism_10000_calls(mode):
+    """UE8M0 scales, N = 1024, K = 2048 (the block-scaled MMA kernel) on ragged segments routed by
+    m_indices or psum: 10,000 calls, each bitwise equal to the first."""
+    counts = [130, 0, 1, 128, 257, 9]
+    G, N, K = len(counts), 1024, 2048
+    m_max = wl.contiguous_capacity(sum(counts), G)
+    a = wl.randn_bf16((m_max, K), 57, 1.0, device="cuda")
+    b = wl.randn_bf16((G, N, K), 58, 0.02, device="cuda")
+    qa, sfa = gpu_quant_tokens(a, DG_SF_UE8M0)
+    qb, sfb = gpu_quant_blocks(b, DG_SF_UE8M0)
+    route = wl.contiguous_psum(counts) if mode == "psum" else wl.contiguous_m_indices(counts, m_max)
+    r = torch.tensor(route, dtype=torch.int32, device="cuda")
+    fn = api.dg_m_grouped_fp8_contiguous_psum if mode == "psum" else api.dg_m_grouped_fp8_contiguous
+    d = torch.zeros(m_max, N, dtype=torch.bfloat16, device="cuda")
+    fn(qa, sfa, qb, sfb, d, r, DG_SF_UE8M0)
+    first = d.clone()
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(10000):
+        fn(qa, sfa, qb, sfb, d, r, DG_SF_UE8M0)
+        bad += (d.view(torch.int16) != first.view(torch.int16)).any().to(torch.int64)
+    sync()
+    assert bad.item() == 0, f"{bad.item()} of 10000 calls differ"
 
 
 @pytest.mark.slow

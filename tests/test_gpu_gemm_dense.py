@@ -75,6 +75,14 @@ def test_plain_gemm_fp32_accumulate(M, N, K, accumulate):
     dense_case(M, N, K, out=torch.float32, accumulate=accumulate, seed=M + 1)
 
 
+@pytest.mark.parametrize("out,accumulate", [(torch.bfloat16, None), (torch.float32, None), (torch.float32, "c"),
+                                          (torch.float32, "inplace")])
+def test_plain_gemm_ue8m0_long_k(out, accumulate):
+    """UE8M0 scales with K = 2304 (18 blocks) and N % 256 == 0: the block-scaled MMA kernel, bf16 and
+    fp32 outputs, C added separately and in place, repeated calls bitwise equal."""
+    dense_case(261, 768, 2304, DG_SF_UE8M0, out=out, accumulate=accumulate, calls=3, seed=17)
+
+
 def test_plain_gemm_fp32_out_and_repeat_bitwise():
     dense_case(200, 512, 768, out=torch.float32, calls=8, seed=5)
     dense_case(200, 1024, 768, out=torch.bfloat16, calls=8, seed=6)

@@ -15,11 +15,12 @@ from gpu_helpers import (assert_close, gpu_quant_blocks, gpu_quant_tokens, out_b
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["auto", "promotion"], autouse=True)
+@pytest.fixture(params=["auto", "promotion", "mx"], autouse=True)
 def ue8m0_kernel(request):
-    """Calls with UE8M0 scales run on the kernel the library picks (the block-scaled MMA kernel) and
-    again on the promotion kernel; fp32-scale cases and full-size cases run once."""
-    if request.param == "promotion":
+    """Calls with UE8M0 scales run on the kernel the library picks, then forced onto the promotion
+    kernel and onto the block-scaled MMA kernel (where N % 256 == 0); fp32-scale cases and full-size
+    cases run once, on the library's choice."""
+    if request.param != "auto":
         cs = getattr(request.node, "callspec", None)
         fmt = cs.params.get("fmt") if cs is not None else None
         if request.node.get_closest_marker("slow") or (fmt != DG_SF_UE8M0 and not request.node.get_closest_marker("ue8m0")):
@@ -106,10 +107,13 @@ def test_odd_blocks_and_narrow_tiles():
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
 @pytest.mark.parametrize("K", [384, 4224])
-def test_wide_tiles_promotion_warps_bitwise_equal(fmt, K):
-    """N = 1024: 128 x 256 tiles, promoted by 16 warps (64 accumulators per thread, the default)
-    or by 8 (128 each); both pass the oracle check and give the same bits, with owner-thread stores
-    (K = 384) and staged TMA stores (K = 4224, 33 blocks)."""
+def test_wide_tiles_promotion_warps_bitwise_equal(ue8m0_kernel, fmt, K):
+    """N = 1024: 128 x 256 tiles of the promotion kernel, promoted by 16 warps (64 accumulators per
+    thread, the default) or by 8 (128 each); both pass the oracle check and give the same bits, with
+    owner-thread stores (K = 384) and staged TMA stores (K = 4224, 33 blocks)."""
+    if ue8m0_kernel != "auto":
+        pytest.skip("a property of the promotion kernel, forced below")
+    set_mgrouped_kernel("promotion")
     G, cap, N = 3, 300, 1024
     a = wl.randn_bf16((G, cap, K), 15, 2.0)
     b = wl.randn_bf16((G, N, K), 16, 0.02)
@@ -125,12 +129,15 @@ def test_wide_tiles_promotion_warps_bitwise_equal(fmt, K):
 
 
 @pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
-def test_tile_widths_bitwise_equal(fmt):
-    """The same call on 128- and 256-column tiles: both pass the oracle check, same bits."""
+def test_tile_widths_bitwise_equal(ue8m0_kernel, fmt):
+    """The promotion kernel on 128- and 256-column tiles: both pass the oracle check, same bits."""
+    if ue8m0_kernel != "auto":
+        pytest.skip("a property of the promotion kernel, forced below")
     G, cap, N, K = 3, 260, 512, 640
     a = wl.randn_bf16((G, cap, K), 19, 2.0)
     b = wl.randn_bf16((G, N, K), 20, 0.02)
     outs = []
+    set_mgrouped_kernel("promotion")
     try:
         for bn in (128, 256):
             set_mgrouped_bn(bn)
