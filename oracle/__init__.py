@@ -54,6 +54,15 @@ def _load():
             lib.oracle_e4m3_encode_array.argtypes = [P, i64, P]
             lib.oracle_e4m3_decode_array.argtypes = [P, i64, P]
             lib.oracle_scale_from_amax.argtypes = [P, i64, f32, i32, P, P]
+            lib.oracle_e2m1_decode.restype = ctypes.c_double
+            lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+            lib.oracle_e2m1_encode.argtypes = [f32]
+            lib.oracle_e2m1_encode_array.argtypes = [P, i64, P]
+            lib.oracle_e2m1_decode_array.argtypes = [P, i64, P]
+            lib.oracle_quant_block_128x128_fp4.argtypes = [P, i32, i64, i64, f32, P, P]
+            lib.oracle_gemm_contiguous_fp4.argtypes = [P, P, P, P, P, i64, i32, i64, i64, P]
+            lib.oracle_gemm_masked_fp4.argtypes = [P, P, P, P, P, i32, i64, i64, i64, P]
             lib.oracle_quant_per_token_1x128.argtypes = [P, i64, i64, i64, P, i32, f32, i32, P, P, P]
             lib.oracle_quant_block_128x128.argtypes = [P, i32, i64, i64, f32, i32, P, P, P]
             lib.oracle_quant_per_channel_128.argtypes = [P, i64, i64, f32, P, P]
@@ -110,6 +119,22 @@ def e4m3_encode(values) -> np.ndarray:
     return out
 
 
+def e2m1_decode(codes) -> np.ndarray:
+    """Values of FP4 (e2m1) codes 0..15 (one code per array element, not packed)."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e2m1_decode_array(_p(c), c.size, _p(out))
+    return out
+
+
+def e2m1_encode(values) -> np.ndarray:
+    """FP4 (e2m1) codes 0..15 of fp32 values (one code per array element)."""
+    v = _c(values, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e2m1_encode_array(_p(v), v.size, _p(out))
+    return out
+
+
 def scale_from_amax(amax, sf_zero: float, ue8m0: bool):
     a = _c(amax, np.float32)
     sf = np.empty(a.shape, np.float32)
@@ -155,6 +180,19 @@ def quant_block_128x128(w, sf_zero: float = 1e-30, ue8m0: bool = False):
     return q, sf, ue
 
 
+def quant_block_128x128_fp4(w, sf_zero: float = 1e-30):
+    """w: bf16 [G, N, K].  FP4 weights with power-of-two block scales: returns q_packed
+    [G, N, K/2] (two e2m1 codes per byte, the even element in the low nibble) and the UE8M0
+    bytes [G, N/128, K/128]."""
+    wb = _bf16_bits(w)
+    G, N, K = wb.shape
+    assert N % 128 == 0 and K % 128 == 0
+    q = np.empty((G, N, K // 2), np.uint8)
+    ue = np.empty((G, N // 128, K // 128), np.uint8)
+    _load().oracle_quant_block_128x128_fp4(_p(wb), G, N, K, sf_zero, _p(q), _p(ue))
+    return q, ue
+
+
 def quant_per_channel_128(x, sf_zero: float = 1e-30):
     """x: bf16 [T, C] token-major.  Returns q [T, C] and sf [T/128, C]."""
     xb = _bf16_bits(x)
@@ -186,6 +224,30 @@ def gemm_contiguous(qa, sfa, qb, sfb, m_indices) -> np.ndarray:
     G, N, _ = qb.shape
     d = np.full((M, N), np.nan, np.float64)
     _load().oracle_gemm_contiguous(_p(qa), _p(sfa), _p(qb), _p(sfb), _p(mi), M, G, N, K, _p(d))
+    return d
+
+
+def gemm_contiguous_fp4(qa, sfa, qb_packed, sfb, m_indices) -> np.ndarray:
+    """gemm_contiguous with FP4 weights: qb_packed [G, N, K/2] packed e2m1 codes."""
+    qa, sfa, qb, sfb = _c(qa, np.uint8), _c(sfa, np.float32), _c(qb_packed, np.uint8), _c(sfb, np.float32)
+    mi = _c(m_indices, np.int32)
+    M, K = qa.shape
+    G, N, K2 = qb.shape
+    assert K2 * 2 == K
+    d = np.full((M, N), np.nan, np.float64)
+    _load().oracle_gemm_contiguous_fp4(_p(qa), _p(sfa), _p(qb), _p(sfb), _p(mi), M, G, N, K, _p(d))
+    return d
+
+
+def gemm_masked_fp4(qa, sfa, qb_packed, sfb, counts) -> np.ndarray:
+    """gemm_masked with FP4 weights: qb_packed [G, N, K/2] packed e2m1 codes."""
+    qa, sfa, qb, sfb = _c(qa, np.uint8), _c(sfa, np.float32), _c(qb_packed, np.uint8), _c(sfb, np.float32)
+    cnt = _c(counts, np.int32)
+    G, cap, K = qa.shape
+    N = qb.shape[1]
+    assert qb.shape[2] * 2 == K
+    d = np.full((G, cap, N), np.nan, np.float64)
+    _load().oracle_gemm_masked_fp4(_p(qa), _p(sfa), _p(qb), _p(sfb), _p(cnt), G, cap, N, K, _p(d))
     return d
 
 

@@ -22,7 +22,8 @@
  *    matmuls rounded to bf16, and FP8 references use the actual quantized inputs and scales.
  *  - "SM120 m_grouped_fp8 contiguous kernel: illegal memory access at CUDA graph replay"
  *    (#444), description: m-grouped contiguous rows routed by m_indices; UE8M0 power-of-two
- *    scale factors on both operands.
+ *    scale factors on both operands; the kernel's name, m_grouped_fp8_fp4_gemm_nt_contiguous,
+ *    gives FP8 activations with FP4 weights as the second operand form.
  *
  * Readings where the pages leave a step open (each is listed in the design notes):
  *  - the 1x128 per-token and 128x128 per-block casts reuse the per-channel rules exactly,
@@ -32,7 +33,12 @@
  *    the exponent bumped when any mantissa bit is set); the stored byte is the biased
  *    exponent, value 2^(byte-127);
  *  - rows with m_indices outside [0, G), masked rows r >= min(count, cap), and experts whose
- *    K_e is not a multiple of 128 or overflows K_cap are not computed (outputs untouched).
+ *    K_e is not a multiple of 128 or overflows K_cap are not computed (outputs untouched);
+ *  - FP4 weights (named only): OCP e2m1 codes with the weight-scale rule of the FP8 path over
+ *    128x128 blocks, the maximum 448 replaced by e2m1's 6 and the scale rounded up to a power of
+ *    two (the page's "2^k" weight scales); e2m1 conversion is round-to-nearest-even with
+ *    saturation to +-6 (NaN -> +6); two codes per byte along K, the even element in the low
+ *    nibble.
  *
  * All dot products accumulate in fp64 over dequantized values decode(q) * sf, with no
  * blocking or reordering beyond the definition.  Compile with -ffp-contract=off.
@@ -91,6 +97,56 @@ uint8_t oracle_e4m3_encode(float y) {
     return (uint8_t)(sign | 0x7E); /* not reached: a < 448 = g_pos[126] */
 }
 
+/* ----------------------------------------------------------------------------------------
+ * e2m1 (OCP FP4 E2M1): 1 sign bit (bit 3), 2 exponent bits (bias 1), 1 mantissa bit, no inf or
+ * NaN.  Normal (e > 0): (1 + m/2) * 2^(e-1); subnormal (e = 0): m/2.  Non-negative values, by
+ * code 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ * --------------------------------------------------------------------------------------*/
+double oracle_e2m1_decode(uint8_t code) {
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 0x3;
+    int m = code & 0x1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+static double g_pos4[8];
+static double g_dec4[16];
+
+__attribute__((constructor)) static void oracle_init_fp4(void) {
+    for (int c = 0; c < 8; ++c) g_pos4[c] = oracle_e2m1_decode((uint8_t)c);
+    for (int c = 0; c < 16; ++c) g_dec4[c] = oracle_e2m1_decode((uint8_t)c);
+}
+
+/* Nearest e2m1 value to y; on a tie the code with the even mantissa (even code) wins;
+ * |y| >= 6 saturates to +-6; NaN -> +6 (0x7); the sign of zero is kept. */
+uint8_t oracle_e2m1_encode(float y) {
+    if (isnan(y)) return 0x7;
+    uint8_t sign = signbit(y) ? 0x8 : 0x0;
+    double a = fabs((double)y);
+    if (a >= 6.0) return (uint8_t)(sign | 0x7);
+    for (int c = 0; c < 7; ++c) {
+        double lo = g_pos4[c], hi = g_pos4[c + 1];
+        if (a <= hi) {
+            double dlo = a - lo, dhi = hi - a;
+            int pick;
+            if (dlo < dhi) pick = c;
+            else if (dhi < dlo) pick = c + 1;
+            else pick = (c % 2 == 0) ? c : c + 1;
+            return (uint8_t)(sign | pick);
+        }
+    }
+    return (uint8_t)(sign | 0x7); /* not reached: a < 6 = g_pos4[7] */
+}
+
+void oracle_e2m1_encode_array(const float* y, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_encode(y[i]);
+}
+
+void oracle_e2m1_decode_array(const uint8_t* c, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_decode(c[i]);
+}
+
 /* bf16 bits -> fp32 (exact) */
 static float bf16_to_float(uint16_t h) {
     uint32_t u = ((uint32_t)h) << 16;
@@ -105,9 +161,9 @@ static float bf16_to_float(uint16_t h) {
  * then optionally rounded up to a power of two (UE8M0).  Returns the scale; *ue_byte gets
  * the UE8M0 byte (biased exponent) when ue8m0 != 0.
  * --------------------------------------------------------------------------------------*/
-static float scale_rule(float amax, float sf_zero, int ue8m0, uint8_t* ue_byte) {
+static float scale_rule_max(float amax, float qmax, float sf_zero, int ue8m0, uint8_t* ue_byte) {
     const float floor_sf = 1e-30f;
-    float sf = amax / 448.0f;
+    float sf = amax / qmax;
     if (sf == 0.0f) sf = sf_zero;
     if (sf < floor_sf) sf = floor_sf;
     if (ue8m0) {
@@ -119,6 +175,10 @@ static float scale_rule(float amax, float sf_zero, int ue8m0, uint8_t* ue_byte) 
         if (ue_byte) *ue_byte = (uint8_t)e;
     }
     return sf;
+}
+
+static float scale_rule(float amax, float sf_zero, int ue8m0, uint8_t* ue_byte) {
+    return scale_rule_max(amax, 448.0f, sf_zero, ue8m0, ue_byte);
 }
 
 /* q = e4m3(fl32(x * fl32(1/sf))) */
@@ -214,6 +274,49 @@ void oracle_quant_block_128x128(const uint16_t* w, int G, int64_t N, int64_t K, 
 }
 
 /* ----------------------------------------------------------------------------------------
+ * FP4 weight cast (the FP4 operand of m_grouped_fp8_fp4_gemm_nt_contiguous, #444): per 128x128
+ * block of w [G][N][K], amax in fp32; sf = amax / 6, zero -> sf_zero, >= 1e-30, rounded up to a
+ * power of two (UE8M0 byte = biased exponent); q = e2m1(fl32(x * fl32(1/sf))).
+ * Outputs: q_packed [G][N][K/2] (element k of a row in byte k/2, the low nibble for even k),
+ * ue [G][N/128][K/128].
+ * --------------------------------------------------------------------------------------*/
+void oracle_quant_block_128x128_fp4(const uint16_t* w, int G, int64_t N, int64_t K, float sf_zero,
+                                    uint8_t* q_packed, uint8_t* ue) {
+    int64_t NB = N / 128, KB = K / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t g = 0; g < G; ++g) {
+        for (int64_t nb = 0; nb < NB; ++nb) {
+            for (int64_t kb = 0; kb < KB; ++kb) {
+                const uint16_t* base = w + (g * N + nb * 128) * K + kb * 128;
+                float amax = 0.0f;
+                for (int r = 0; r < 128; ++r)
+                    for (int c = 0; c < 128; ++c) {
+                        float v = fabsf(bf16_to_float(base[r * K + c]));
+                        if (v > amax) amax = v;
+                    }
+                uint8_t byte = 0;
+                float s = scale_rule_max(amax, 6.0f, sf_zero, 1, &byte);
+                ue[(g * NB + nb) * KB + kb] = byte;
+                float rcp = 1.0f / s;
+                for (int r = 0; r < 128; ++r)
+                    for (int c = 0; c < 128; c += 2) {
+                        int64_t off = (g * N + nb * 128 + r) * K + kb * 128 + c;
+                        uint8_t lo = oracle_e2m1_encode(bf16_to_float(w[off]) * rcp);
+                        uint8_t hi = oracle_e2m1_encode(bf16_to_float(w[off + 1]) * rcp);
+                        q_packed[off / 2] = (uint8_t)(lo | (hi << 4));
+                    }
+            }
+        }
+    }
+}
+
+/* Value of weight element (e, n, k) of packed FP4 codes [G][N][K/2]. */
+static double fp4_at(const uint8_t* qb_packed, int64_t e, int64_t n, int64_t k, int64_t N, int64_t K) {
+    uint8_t byte = qb_packed[(e * N + n) * (K / 2) + k / 2];
+    return g_dec4[(k & 1) ? (byte >> 4) : (byte & 0xF)];
+}
+
+/* ----------------------------------------------------------------------------------------
  * Per-channel cast over 128-token blocks (#365 repro, `_per_channel_cast_to_fp8`).
  * x: bf16 [T][C] token-major, T % 128 == 0.  Outputs q [T][C] and sf [T/128][C].
  * --------------------------------------------------------------------------------------*/
@@ -302,6 +405,54 @@ void oracle_gemm_masked(const uint8_t* qa, const float* sfa, const uint8_t* qb, 
                                 (double)sfa[(g * cap + r) * KB + k / 128];
                     double xb = g_dec[qb[(g * N + n) * K + k]] *
                                 (double)sfb[(g * NB + n / 128) * KB + k / 128];
+                    acc += xa * xb;
+                }
+                d[(g * cap + r) * N + n] = acc;
+            }
+        }
+    }
+}
+
+/* ----------------------------------------------------------------------------------------
+ * The contiguous and masked GEMMs above with FP4 weights (#444: FP8 activations, FP4 weights):
+ * the same sums with decode(qb) the e2m1 value of the packed code.  qb_packed [G][N][K/2].
+ * --------------------------------------------------------------------------------------*/
+void oracle_gemm_contiguous_fp4(const uint8_t* qa, const float* sfa, const uint8_t* qb_packed,
+                                const float* sfb, const int32_t* m_indices, int64_t M, int G,
+                                int64_t N, int64_t K, double* d) {
+    int64_t KB = K / 128, NB = N / 128;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        int64_t e = m_indices[m];
+        if (e < 0 || e >= G) continue;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double xa = g_dec[qa[m * K + k]] * (double)sfa[m * KB + k / 128];
+                double xb = fp4_at(qb_packed, e, n, k, N, K) * (double)sfb[(e * NB + n / 128) * KB + k / 128];
+                acc += xa * xb;
+            }
+            d[m * N + n] = acc;
+        }
+    }
+}
+
+void oracle_gemm_masked_fp4(const uint8_t* qa, const float* sfa, const uint8_t* qb_packed,
+                            const float* sfb, const int32_t* counts, int G, int64_t cap, int64_t N,
+                            int64_t K, double* d) {
+    int64_t KB = K / 128, NB = N / 128;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t g = 0; g < G; ++g) {
+        for (int64_t r = 0; r < cap; ++r) {
+            int64_t v = counts[g];
+            if (v < 0) v = 0;
+            if (v > cap) v = cap;
+            if (r >= v) continue;
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double xa = g_dec[qa[(g * cap + r) * K + k]] * (double)sfa[(g * cap + r) * KB + k / 128];
+                    double xb = fp4_at(qb_packed, g, n, k, N, K) * (double)sfb[(g * NB + n / 128) * KB + k / 128];
                     acc += xa * xb;
                 }
                 d[(g * cap + r) * N + n] = acc;

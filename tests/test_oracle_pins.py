@@ -621,6 +621,127 @@ def test_batched_gemm_equals_masked_at_full_counts_and_contiguous_single_expert(
     np.testing.assert_array_equal(got[0], cont)
 
 
+# ------------------------------------------------------------------------------ FP4 (e2m1) weights
+
+def e2m1_grid():
+    """The non-negative e2m1 values by code 0..7, from the format definition (exponent bias 1,
+    one mantissa bit, subnormal at exponent 0), not from the oracle."""
+    vals = []
+    for e in range(4):
+        for m in range(2):
+            vals.append(m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1))
+    return np.array(vals)
+
+
+def test_e2m1_decode_matches_format_definition():
+    grid = e2m1_grid()
+    np.testing.assert_array_equal(grid, [0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    got = oracle.e2m1_decode(np.arange(16, dtype=np.uint8))
+    np.testing.assert_array_equal(got[:8], grid)
+    np.testing.assert_array_equal(got[8:], -grid)
+    assert math.copysign(1.0, got[8]) == -1.0            # code 8 is -0
+
+
+def test_e2m1_encode_roundtrip_midpoints_and_saturation():
+    grid = e2m1_grid()
+    codes = np.arange(16, dtype=np.uint8)
+    vals = oracle.e2m1_decode(codes)
+    np.testing.assert_array_equal(oracle.e2m1_encode(vals.astype(np.float32)), codes)
+    mids = (grid[:-1] + grid[1:]) / 2                  # ties go to the even code
+    got = oracle.e2m1_encode(mids.astype(np.float32))
+    want = np.array([c if c % 2 == 0 else c + 1 for c in range(7)], np.uint8)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(oracle.e2m1_encode(-mids.astype(np.float32)), want | 8)
+    big = np.array([6.0, 6.5, 7.0, 1e30, np.inf], np.float32)
+    np.testing.assert_array_equal(oracle.e2m1_encode(big), 7)
+    np.testing.assert_array_equal(oracle.e2m1_encode(-big), 15)
+    # brute force: every other value goes to the nearest grid point
+    rng = np.random.default_rng(5)
+    y = rng.uniform(-7, 7, 20000).astype(np.float32)
+    q = oracle.e2m1_encode(y)
+    dec = oracle.e2m1_decode(q)
+    full = np.concatenate([grid, -grid])
+    nearest = np.abs(np.abs(y.astype(np.float64))[:, None] - grid[None, :]).min(axis=1)
+    sat = np.abs(y) >= 6
+    np.testing.assert_array_equal(np.abs(np.abs(y[~sat]) - np.abs(dec[~sat])), nearest[~sat])
+    assert np.all(np.sign(dec[dec != 0]) == np.sign(y[dec != 0]))
+    assert set(np.unique(dec)) <= set(full)
+
+
+def _unpack_fp4(q_packed):
+    lo, hi = q_packed & 0xF, q_packed >> 4
+    out = np.empty(q_packed.shape[:-1] + (q_packed.shape[-1] * 2,), np.uint8)
+    out[..., 0::2], out[..., 1::2] = lo, hi
+    return out
+
+
+def test_fp4_block_cast_pins():
+    """Zero blocks take sf_zero rounded up to a power of two with zero codes; a block whose amax is
+    6 * 2^k gets the scale 2^k and reproduces grid values exactly; every code is the nearest
+    e2m1 value of x / sf (brute force over the grid); the even element sits in the low nibble."""
+    grid = e2m1_grid()
+    G, N, K = 2, 128, 256
+    rng = np.random.default_rng(9)
+    w = np.zeros((G, N, K))
+    w[0, :, :128] = rng.choice(np.concatenate([grid, -grid]), (128, 128)) * 4.0   # amax 24 = 6 * 2^2
+    w[0, 0, 0] = 24.0
+    w[1] = rng.standard_normal((N, K)) * 0.3                                      # block (1, 0, *)
+    wt = bf16_from_f64(np.asarray(torch.tensor(w).to(torch.bfloat16).double()))
+    q, ue = oracle.quant_block_128x128_fp4(wt, sf_zero=1e-30)
+    assert q.shape == (G, N, K // 2) and ue.shape == (G, 1, 2)
+    codes = _unpack_fp4(q)
+    assert ue[0, 0, 0] == 127 + 2
+    np.testing.assert_array_equal(oracle.e2m1_decode(codes[0, :, :128]) * 4.0, w[0, :, :128])
+    # the zero block: sf_zero = 1e-30 rounds up to 2^-99
+    assert ue[0, 0, 1] == 127 - 99 and np.all(codes[0, :, 128:] == 0)
+    # random block: scale = 2^ceil(log2(amax / 6)) in fp32, codes nearest to x / sf
+    wf = wt.double().numpy()
+    for kb in range(2):
+        blk = wf[1, :, kb * 128:(kb + 1) * 128]
+        amax = np.float32(np.abs(blk).max())
+        sf = np.float32(amax / np.float32(6.0))
+        e = int(np.frexp(sf)[1]) - 1 + (0 if np.frexp(sf)[0] == 0.5 else 1)
+        assert ue[1, 0, kb] == 127 + e
+        y = blk / 2.0 ** e
+        dec = oracle.e2m1_decode(codes[1, :, kb * 128:(kb + 1) * 128])
+        nearest = np.abs(np.abs(y)[..., None] - grid).min(axis=-1)
+        np.testing.assert_array_equal(np.abs(np.abs(y) - np.abs(dec)), nearest)
+    # packing: element 2i in the low nibble, 2i + 1 in the high nibble
+    np.testing.assert_array_equal(q & 0xF, codes[..., 0::2])
+    np.testing.assert_array_equal(q >> 4, codes[..., 1::2])
+
+
+def test_fp4_gemms_equal_the_fp8_gemms_on_the_same_values():
+    """Every e2m1 value is an e4m3 value, so the FP4-weight GEMMs must equal the (pinned) FP8 GEMMs
+    fed the e4m3 codes of the same weight values, bit for bit; and numpy's einsum."""
+    rng = np.random.default_rng(13)
+    G, N, K, M = 3, 128, 256, 7
+    q4 = rng.integers(0, 16, (G, N, K), dtype=np.uint8)
+    packed = (q4[..., 0::2] | (q4[..., 1::2] << 4)).astype(np.uint8)
+    q8 = oracle.e4m3_encode(oracle.e2m1_decode(q4).astype(np.float32))
+    np.testing.assert_array_equal(oracle.e4m3_decode(q8), oracle.e2m1_decode(q4))
+    qa = _random_codes(rng, (M, K))
+    sfa = rng.uniform(0.5, 2.0, (M, K // 128)).astype(np.float32)
+    sfb = np.ldexp(np.float32(1.0), rng.integers(-4, 4, (G, N // 128, K // 128))).astype(np.float32)
+    mi = np.array([0, 2, -1, 1, 2, 0, 5], np.int32)
+    got = oracle.gemm_contiguous_fp4(qa, sfa, packed, sfb, mi)
+    want = oracle.gemm_contiguous(qa, sfa, q8, sfb, mi)
+    np.testing.assert_array_equal(got, want)
+    A = oracle.e4m3_decode(qa) * np.repeat(sfa.astype(np.float64), 128, axis=1)
+    B = oracle.e2m1_decode(q4) * np.repeat(np.repeat(sfb.astype(np.float64), 128, axis=1), 128, axis=2)
+    for m in range(M):
+        if 0 <= mi[m] < G:
+            np.testing.assert_allclose(got[m], B[mi[m]] @ A[m], rtol=1e-12, atol=1e-12 * np.abs(B).max())
+        else:
+            assert np.all(np.isnan(got[m]))
+    cap = 3
+    qam = _random_codes(rng, (G, cap, K))
+    sfam = rng.uniform(0.5, 2.0, (G, cap, K // 128)).astype(np.float32)
+    counts = np.array([3, 0, 2], np.int32)
+    np.testing.assert_array_equal(oracle.gemm_masked_fp4(qam, sfam, packed, sfb, counts),
+                                  oracle.gemm_masked(qam, sfam, q8, sfb, counts))
+
+
 # Plumbing that computes nothing the path does (compilation, thread count).
 _NOT_ARITHMETIC = {"build", "num_threads"}
 
