@@ -409,6 +409,10 @@ class MGroupedWorkload:
     def __init__(self, kind, device, ours=True):
         from moe_grouped_fp8_gb300 import workloads as wl
         DG_SF_FP32, DG_SF_UE8M0 = 0, 1
+        # "_fp4": the same shape with FP4 (e2m1) weights and UE8M0 scales on both operands
+        self.fp4 = kind.endswith("_fp4")
+        if self.fp4:
+            kind = kind[:-len("_fp4")]
         if kind == "masked_decode":
             self.w = wl.masked_decode()
         elif kind == "masked_repro":
@@ -430,12 +434,14 @@ class MGroupedWorkload:
             self.w = wl.many_expert(int(e[1:]), which)
         else:
             raise SystemExit(f"unknown workload {kind}")
-        self.kind = kind
+        self.kind = kind + ("_fp4" if self.fp4 else "")
         self.masked = isinstance(self.w, wl.Masked)
         # the kernel the library runs for these calls (bf16 output, single-CTA tiles)
         self.kernel_name = "k_grouped_gemm"
         w = self.w
-        self.fmt = DG_SF_UE8M0 if getattr(w, "ue8m0", False) else DG_SF_FP32
+        self.fmt = DG_SF_UE8M0 if (getattr(w, "ue8m0", False) or self.fp4) else DG_SF_FP32
+        if self.fp4:
+            self.kernel_name = "k_grouped_gemm_mx"
         a, b = w.draw(device=device)
         G, N, K = w.G, w.N, w.K
         M = G * w.cap if self.masked else w.m_max
@@ -454,17 +460,21 @@ class MGroupedWorkload:
         self.a_rows = self.a[torch.from_numpy(rows).to(self.a.device)].cpu()
         self.b_slab = b[self.e_sample].cpu()
         self.R = 1
-        self.name = f"{kind}_G{G}_N{N}_K{K}"
+        self.name = f"{self.kind}_G{G}_N{N}_K{K}"
         if not ours:
             return
         from moe_grouped_fp8_gb300 import api
         self.api = api
         self.qa = torch.empty(M, K, dtype=torch.uint8, device=device)
         self.sfa = api.empty_sfa(M, K, self.fmt, device)
-        self.qb = torch.empty(G, N, K, dtype=torch.uint8, device=device)
         self.sfb = torch.empty(G, N // 128, K // 128, dtype=torch.float32 if self.fmt == DG_SF_FP32 else torch.uint8,
                                device=device)
-        api.dg_quant_block_128x128(b, self.qb, self.sfb, self.fmt)
+        if self.fp4:
+            self.qb = torch.empty(G, N, K // 2, dtype=torch.uint8, device=device)
+            api.dg_quant_block_128x128_fp4(b, self.qb, self.sfb)
+        else:
+            self.qb = torch.empty(G, N, K, dtype=torch.uint8, device=device)
+            api.dg_quant_block_128x128(b, self.qb, self.sfb, self.fmt)
         del b
         if self.masked:
             self.counts = torch.tensor(w.counts, dtype=torch.int32, device=device)
@@ -483,13 +493,22 @@ class MGroupedWorkload:
         else:
             self.api.dg_quant_per_token_1x128_routed(self.a, self.qa, self.sfa, self.mi, self.fmt)
 
-    def gemm_only(self, r):
+    def gemm_into(self, d, route):
+        """The GEMM of a step into output d, routed by `route` (counts or m_indices)."""
         w = self.w
-        if self.masked:
-            self.api.dg_m_grouped_fp8_masked(self.qa.view(w.G, w.cap, w.K), self.sfa, self.qb, self.sfb, self.d,
-                                             self.counts, w.expected_m, self.fmt)
+        if self.fp4 and self.masked:
+            self.api.dg_m_grouped_fp8_fp4_masked(self.qa.view(w.G, w.cap, w.K), self.sfa, self.qb, self.sfb, d, route,
+                                                 w.expected_m)
+        elif self.fp4:
+            self.api.dg_m_grouped_fp8_fp4_contiguous(self.qa, self.sfa, self.qb, self.sfb, d, route)
+        elif self.masked:
+            self.api.dg_m_grouped_fp8_masked(self.qa.view(w.G, w.cap, w.K), self.sfa, self.qb, self.sfb, d, route,
+                                             w.expected_m, self.fmt)
         else:
-            self.api.dg_m_grouped_fp8_contiguous(self.qa, self.sfa, self.qb, self.sfb, self.d, self.mi, self.fmt)
+            self.api.dg_m_grouped_fp8_contiguous(self.qa, self.sfa, self.qb, self.sfb, d, route, self.fmt)
+
+    def gemm_only(self, r):
+        self.gemm_into(self.d, self.counts if self.masked else self.mi)
 
     wgrad = gemm_only
 
@@ -505,7 +524,8 @@ class MGroupedWorkload:
         live = int((counts > 0).sum())
         valid = int(counts.sum())
         sf = 4 if self.fmt == 0 else 1
-        return (live * w.N * w.K + valid * w.K + valid * (w.K // 128) * sf + live * (w.N // 128) * (w.K // 128) * sf
+        wbytes = live * w.N * w.K // (2 if self.fp4 else 1)
+        return (wbytes + valid * w.K + valid * (w.K // 128) * sf + live * (w.N // 128) * (w.K // 128) * sf
                 + valid * w.N * 2)
 
     def cast_bytes(self):
@@ -565,12 +585,9 @@ class MGroupedWorkload:
             with torch.cuda.stream(stream):
                 if self.masked:
                     self.api.dg_quant_per_token_1x128(x["a"], self.qa, self.sfa, self.fmt, row_counts=x["route"])
-                    self.api.dg_m_grouped_fp8_masked(self.qa.view(w.G, w.cap, w.K), self.sfa, self.qb, self.sfb,
-                                                     x["d"].view(w.G, w.cap, w.N), x["route"], w.expected_m, self.fmt)
                 else:
                     self.api.dg_quant_per_token_1x128_routed(x["a"], self.qa, self.sfa, x["route"], self.fmt)
-                    self.api.dg_m_grouped_fp8_contiguous(self.qa, self.sfa, self.qb, self.sfb, x["d"], x["route"],
-                                                         self.fmt)
+                self.gemm_into(x["d"].view(self.d.shape), x["route"])
             ev["comp"][b].record(stream)
             s_out.wait_event(ev["comp"][b])
             with torch.cuda.stream(s_out):
@@ -605,8 +622,12 @@ class MGroupedWorkload:
         rows = self.a_rows.shape[0]
         t0 = time.perf_counter()
         qa, sa, _ = oracle.quant_per_token_1x128(self.a_rows, ue8m0=ue)
-        qb, sb, _ = oracle.quant_block_128x128(self.b_slab[:n].unsqueeze(0), ue8m0=ue)
-        oracle.gemm_contiguous(qa, sa, qb, sb, np.zeros(rows, np.int32))
+        if self.fp4:
+            qb, ueb = oracle.quant_block_128x128_fp4(self.b_slab[:n].unsqueeze(0))
+            oracle.gemm_contiguous_fp4(qa, sa, qb, oracle.ue8m0_value(ueb), np.zeros(rows, np.int32))
+        else:
+            qb, sb, _ = oracle.quant_block_128x128(self.b_slab[:n].unsqueeze(0), ue8m0=ue)
+            oracle.gemm_contiguous(qa, sa, qb, sb, np.zeros(rows, np.int32))
         dt = time.perf_counter() - t0
         return dt, 2.0 * rows * n * w.K
 

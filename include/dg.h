@@ -301,6 +301,43 @@ int dg_quant_per_channel_128_pair_psum(const void* x_a, int64_t C_a, uint8_t* q_
                                        int64_t C_b, uint8_t* q_b, float* sf_b, int64_t K_cap, const int32_t* psum,
                                        int G, float sf_zero, int32_t* status, void* stream);
 
+/*
+ * FP4 weights ([P3]: the kernel is named m_grouped_fp8_fp4_gemm_nt_contiguous, FP8 activations
+ * with FP8 or FP4 weights, "weights requantized to 2^k scales").  The pages name the FP4 form
+ * only; reading taken: OCP e2m1 codes (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives)
+ * with one power-of-two (UE8M0) scale per 128x128 block, the rule of the FP8 weight cast with
+ * e2m1's maximum 6 in place of 448.
+ *
+ * dg_quant_block_128x128_fp4: per 128x128 block of w, amax (fp32), sf = amax / 6, sf == 0 ->
+ * sf_zero, sf = max(sf, 1e-30), rounded up to a power of two; q = e2m1_rne_satfinite(x * (1/sf)).
+ *   w: bf16 [G, N, K] (16-byte aligned).  q_packed: [G, N, K/2] bytes, two codes per byte along K,
+ *   element 2i in the low nibble and 2i+1 in the high nibble (4-byte aligned).
+ *   sfb: UE8M0 bytes [G][N/128][K/128].  N, K multiples of 128.
+ */
+int dg_quant_block_128x128_fp4(const void* w, int G, int64_t N, int64_t K, uint8_t* q_packed,
+                               uint8_t* sfb, float sf_zero, void* stream);
+
+/*
+ * m-grouped contiguous and masked GEMMs with FP4 weights ([P3]
+ * m_grouped_fp8_fp4_gemm_nt_contiguous): the results of dg_m_grouped_fp8_contiguous /
+ * dg_m_grouped_fp8_masked with sf_format DG_SF_UE8M0, with each weight element the e2m1 value
+ * of its code times its block's scale.
+ *   a: e4m3 [M, K] / [G, cap, K].  sfa: UE8M0 bytes [K/128][round_up(M or G*cap, 16)].
+ *   b_packed: FP4 codes [G, N, K/2] as written by dg_quant_block_128x128_fp4 (16-byte aligned).
+ *   sfb: UE8M0 bytes [G][N/128][K/128].  d: bf16 or fp32 (out_dtype).
+ *   m_indices / counts, G, cap, expected_m, status, stream: as for the FP8 calls.
+ *   N must be a multiple of 256 (DG_ERR_UNSUPPORTED otherwise): these calls run on the
+ *   block-scaled MMA kernel's 128 x 256 tiles.  Rows that are not valid are never written.
+ */
+int dg_m_grouped_fp8_fp4_contiguous(const uint8_t* a, const uint8_t* sfa, const uint8_t* b_packed,
+                                    const uint8_t* sfb, void* d, int out_dtype,
+                                    const int32_t* m_indices, int64_t M, int G, int64_t N, int64_t K,
+                                    int32_t* status, void* stream);
+int dg_m_grouped_fp8_fp4_masked(const uint8_t* a, const uint8_t* sfa, const uint8_t* b_packed,
+                                const uint8_t* sfb, void* d, int out_dtype, const int32_t* counts,
+                                int G, int64_t cap, int64_t N, int64_t K, int expected_m,
+                                int32_t* status, void* stream);
+
 /* Largest G accepted by dg_k_grouped_fp8_wgrad_noalloc. */
 #define DG_NOALLOC_MAX_GROUPS 256
 

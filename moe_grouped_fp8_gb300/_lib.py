@@ -46,6 +46,9 @@ SIGNATURES = {
     "dg_k_grouped_fp8_wgrad_from_bf16": (I32, [P, P, P, I32, I64, I64, I64, P, P, P, P, P, P, F32, P, SZ, P, P]),
     "dg_k_grouped_fp8_wgrad_from_bf16_psum": (I32, [P, P, P, I32, I64, I64, I64, P, P, P, P, P, P, F32, P, SZ, P, P]),
     "dg_k_grouped_fp8_wgrad_noalloc": (I32, [P, P, P, P, P, P, P, I32, I64, I64, I64, P, P]),
+    "dg_quant_block_128x128_fp4": (I32, [P, I32, I64, I64, P, P, F32, P]),
+    "dg_m_grouped_fp8_fp4_contiguous": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, P, P]),
+    "dg_m_grouped_fp8_fp4_masked": (I32, [P, P, P, P, P, I32, P, I32, I64, I64, I64, I32, P, P]),
 }
 # test hooks exported by the library (not part of include/dg.h)
 TESTING_SIGNATURES = {

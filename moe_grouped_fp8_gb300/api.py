@@ -15,7 +15,7 @@ from ._lib import DG_OP_K_GROUPED_WGRAD, DG_OUT_BF16, DG_OUT_FP32, DG_SF_FP32, D
 
 __all__ = [
     "dg_quant_per_token_1x128", "dg_quant_per_token_1x128_routed", "dg_quant_per_channel_128", "dg_quant_per_channel_128_pair",
-    "dg_quant_block_128x128",
+    "dg_quant_block_128x128", "dg_quant_block_128x128_fp4", "dg_m_grouped_fp8_fp4_contiguous", "dg_m_grouped_fp8_fp4_masked",
     "dg_m_grouped_fp8_contiguous", "dg_m_grouped_fp8_masked", "dg_k_grouped_fp8_wgrad", "dg_fp8_gemm_nt",
     "dg_fp8_gemm_nt_batched",
     "dg_k_grouped_fp8_wgrad_noalloc", "dg_k_grouped_fp8_wgrad_from_bf16", "dg_k_grouped_fp8_wgrad_from_bf16_psum",
@@ -148,6 +148,19 @@ def dg_quant_block_128x128(w, q, sfb, sf_format=DG_SF_FP32, sf_zero=1e-30, strea
     check(load().dg_quant_block_128x128(_p(w), G, N, K, _p(q), _p(sfb), sf_format, sf_zero, _s(stream)))
 
 
+def dg_quant_block_128x128_fp4(w, q_packed, sfb, sf_zero=1e-30, stream=None):
+    """w bf16 [G, N, K] -> FP4 codes q_packed uint8 [G, N, K/2] (two per byte, the even element in the
+    low nibble) and UE8M0 block scales sfb uint8 [G][N/128][K/128]."""
+    _dev(w, q_packed, sfb)
+    _need(w.dim() == 3 and w.dtype == torch.bfloat16 and w.is_contiguous(), "w must be contiguous bf16 [G, N, K]")
+    G, N, K = w.shape
+    _need(q_packed.is_contiguous() and q_packed.dtype == torch.uint8 and q_packed.numel() == G * N * K // 2,
+          "q_packed must be uint8 [G, N, K/2]")
+    _need(sfb.is_contiguous() and sfb.dtype == torch.uint8 and sfb.numel() >= G * (N // 128) * (K // 128),
+          "sfb must be uint8 [G][N/128][K/128]")
+    check(load().dg_quant_block_128x128_fp4(_p(w), G, N, K, _p(q_packed), _p(sfb), sf_zero, _s(stream)))
+
+
 def _out_code(d):
     if d.dtype == torch.bfloat16:
         return DG_OUT_BF16
@@ -214,6 +227,38 @@ def dg_fp8_gemm_nt_batched(a, sfa, b, sfb, d, c=None, sf_format=DG_SF_FP32, stat
         _need(c.dtype == torch.float32 and tuple(c.shape) == (Bt, M, N) and c.is_contiguous(), "c fp32 [B, M, N]")
     check(load().dg_fp8_gemm_nt_batched(_p(a), _p(sfa), _p(b), _p(sfb), _p(c), _p(d), _out_code(d), Bt, M, N, K,
                                         sf_format, _p(status), _s(stream)))
+
+
+def dg_m_grouped_fp8_fp4_contiguous(a, sfa, b_packed, sfb, d, m_indices, status=None, stream=None):
+    """a [M, K] e4m3 with UE8M0 sfa, b_packed [G, N, K/2] FP4 codes with UE8M0 sfb, d [M, N] bf16/fp32,
+    m_indices int32 [M]."""
+    _dev(a, sfa, b_packed, sfb, d, m_indices, status)
+    M, K = a.shape
+    G, N, K2 = b_packed.shape
+    _need(K == 2 * K2 and tuple(d.shape) == (M, N) and d.is_contiguous() and a.is_contiguous()
+          and b_packed.is_contiguous(), "shapes")
+    _need(m_indices.dtype == torch.int32 and m_indices.numel() == M, "m_indices must be int32 [M]")
+    _need(sfa.dtype == torch.uint8 and sfb.dtype == torch.uint8, "UE8M0 scales are uint8")
+    _need(sfa.numel() >= (K // 128) * sfa_padded_rows(M, 1), "sfa size")
+    _need(sfb.numel() >= G * (N // 128) * (K // 128), "sfb size")
+    check(load().dg_m_grouped_fp8_fp4_contiguous(_p(a), _p(sfa), _p(b_packed), _p(sfb), _p(d), _out_code(d),
+                                                 _p(m_indices), M, G, N, K, _p(status), _s(stream)))
+
+
+def dg_m_grouped_fp8_fp4_masked(a, sfa, b_packed, sfb, d, counts, expected_m=0, status=None, stream=None):
+    """a [G, cap, K] e4m3 with UE8M0 sfa, b_packed [G, N, K/2] FP4 codes with UE8M0 sfb,
+    d [G, cap, N] bf16/fp32, counts int32 [G]."""
+    _dev(a, sfa, b_packed, sfb, d, counts, status)
+    G, cap, K = a.shape
+    G2, N, K2 = b_packed.shape
+    _need(G == G2 and K == 2 * K2 and tuple(d.shape) == (G, cap, N), "shapes")
+    _need(a.is_contiguous() and b_packed.is_contiguous() and d.is_contiguous(), "contiguity")
+    _need(counts.dtype == torch.int32 and counts.numel() == G, "counts must be int32 [G]")
+    _need(sfa.dtype == torch.uint8 and sfb.dtype == torch.uint8, "UE8M0 scales are uint8")
+    _need(sfa.numel() >= (K // 128) * sfa_padded_rows(G * cap, 1), "sfa size")
+    _need(sfb.numel() >= G * (N // 128) * (K // 128), "sfb size")
+    check(load().dg_m_grouped_fp8_fp4_masked(_p(a), _p(sfa), _p(b_packed), _p(sfb), _p(d), _out_code(d), _p(counts),
+                                             G, cap, N, K, int(expected_m), _p(status), _s(stream)))
 
 
 def dg_m_grouped_fp8_masked(a, sfa, b, sfb, d, counts, expected_m=0, sf_format=DG_SF_FP32, status=None,

@@ -614,9 +614,10 @@ bool use_mx(int fmt, int64_t N, int64_t K) {
 }
 
 template <Layout L>
-int dispatch_mgrouped(int out, int fmt, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD,
-                      const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
-    if (use_mx(fmt, args.N, args.K)) return launch_mgrouped_mx(L, out == DG_OUT_FP32, tA, tB, args, s);
+int dispatch_mgrouped(int out, int fmt, bool b_fp4, const CUtensorMap& tA, const CUtensorMap& tB,
+                      const CUtensorMap& tD, const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
+    if (b_fp4) return launch_mgrouped_mx(L, out == DG_OUT_FP32, true, tA, tB, args, s);
+    if (use_mx(fmt, args.N, args.K)) return launch_mgrouped_mx(L, out == DG_OUT_FP32, false, tA, tB, args, s);
     const int bn = single_bn(out, args.N);
     args.num_nb = static_cast<int>(args.N / bn);
     // bf16 output stages half as much as fp32, which leaves room for a fifth ring stage
@@ -648,6 +649,26 @@ int check_ptrs_mg(const uint8_t* a, const void* sfa, const uint8_t* b, const voi
     return DG_OK;
 }
 
+// The weight tensor map: FP8 codes [G, N, K], or (b_fp4) FP4 codes packed two per byte
+// [G, N, K/2] that the TMA unpacks to 16-byte groups of 16 codes in shared memory; boxes of 128 (K)
+// x brows rows.
+int encode_weights(CUtensorMap* tB, const uint8_t* b, bool b_fp4, int G, int64_t N, int64_t K, uint32_t brows) {
+    uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
+    const uint64_t row = b_fp4 ? static_cast<uint64_t>(K / 2) : static_cast<uint64_t>(K);
+    uint64_t str[2] = {row, row * static_cast<uint64_t>(N)};
+    uint32_t box[3] = {BK, brows, 1};
+    return encode_tmap(tB, b_fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims,
+                       str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// FP4 weights run only on the block-scaled kernel: UE8M0 scales and N % 256 == 0.
+int check_fp4(bool b_fp4, int fmt, int64_t N) {
+    if (!b_fp4) return DG_OK;
+    DG_CHECK_ARG(fmt == DG_SF_UE8M0, "FP4 weights need UE8M0 scales");
+    DG_CHECK_SUPPORTED(N % MX_BN == 0, "FP4 weights need N %% %d == 0 (N=%lld)", MX_BN, (long long)N);
+    return DG_OK;
+}
+
 }  // namespace
 }  // namespace dg
 
@@ -666,9 +687,10 @@ int check_accumulator(const float* c, int out_dtype) {
 // The masked layout [G, cap, K]; dense: every group has cap rows (a batched GEMM), no counts.
 int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, const float* c, void* d,
                      int out_dtype, const int32_t* counts, bool dense, int G, int64_t cap, int64_t N, int64_t K,
-                     int expected_m, int sf_format, int32_t* status, void* stream) {
+                     int expected_m, int sf_format, int32_t* status, void* stream, bool b_fp4 = false) {
     DG_CHECK_ARG(cap >= 0, "cap must be >= 0");
     if (int rc = check_shape_mg(out_dtype, G, N, K, sf_format)) return rc;
+    if (int rc = check_fp4(b_fp4, sf_format, N)) return rc;
     DG_CHECK_ARG(c == nullptr || out_dtype == DG_OUT_FP32, "accumulation (c != NULL) needs fp32 output");
     if (cap == 0) return DG_OK;
     if (int rc = check_ptrs_mg(a, sfa, b, sfb, d)) return rc;
@@ -689,13 +711,9 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
             return rc;
     }
     {
-        uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
-        uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = static_cast<uint32_t>(use_mx(sf_format, N, K) ? MX_BN : single_bn(out_dtype, N));
-        uint32_t box[3] = {BK, brows, 1};
-        if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
-                                 CU_TENSOR_MAP_SWIZZLE_128B))
-            return rc;
+        const bool mx = b_fp4 || use_mx(sf_format, N, K);
+        const uint32_t brows = static_cast<uint32_t>(mx ? MX_BN : single_bn(out_dtype, N));
+        if (int rc = encode_weights(&tB, b, b_fp4, G, N, K, brows)) return rc;
     }
     {
         uint64_t dims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(cap), static_cast<uint64_t>(G)};
@@ -725,7 +743,7 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     args.KB = static_cast<int>(K / BK);
     args.n128 = static_cast<int>(N / 128);
     args.N = N;
-    return dispatch_mgrouped<Layout::Masked>(out_dtype, sf_format, tA, tB, tD, tD8, args,
+    return dispatch_mgrouped<Layout::Masked>(out_dtype, b_fp4, sf_format, tA, tB, tD, tD8, args,
                                              static_cast<cudaStream_t>(stream));
 }
 
@@ -733,9 +751,10 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
 // one expert owning all M rows (a plain GEMM), no routing tensor.
 int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, const float* c,
                          void* d, int out_dtype, const int32_t* routing, bool psum, bool dense, int64_t M, int G,
-                         int64_t N, int64_t K, int sf_format, int32_t* status, void* stream) {
+                         int64_t N, int64_t K, int sf_format, int32_t* status, void* stream, bool b_fp4 = false) {
     DG_CHECK_ARG(M >= 0, "M must be >= 0");
     if (int rc = check_shape_mg(out_dtype, G, N, K, sf_format)) return rc;
+    if (int rc = check_fp4(b_fp4, sf_format, N)) return rc;
     DG_CHECK_ARG(c == nullptr || out_dtype == DG_OUT_FP32, "accumulation (c != NULL) needs fp32 output");
     if (M == 0) return DG_OK;
     if (int rc = check_ptrs_mg(a, sfa, b, sfb, d)) return rc;
@@ -754,13 +773,9 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
             return rc;
     }
     {
-        uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
-        uint64_t str[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N * K)};
-        const uint32_t brows = static_cast<uint32_t>(use_mx(sf_format, N, K) ? MX_BN : single_bn(out_dtype, N));
-        uint32_t box[3] = {BK, brows, 1};
-        if (int rc = encode_tmap(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, str, box,
-                                 CU_TENSOR_MAP_SWIZZLE_128B))
-            return rc;
+        const bool mx = b_fp4 || use_mx(sf_format, N, K);
+        const uint32_t brows = static_cast<uint32_t>(mx ? MX_BN : single_bn(out_dtype, N));
+        if (int rc = encode_weights(&tB, b, b_fp4, G, N, K, brows)) return rc;
     }
     {
         uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
@@ -791,7 +806,7 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     args.KB = static_cast<int>(K / BK);
     args.n128 = static_cast<int>(N / 128);
     args.N = N;
-    return dispatch_mgrouped<Layout::Contiguous>(out_dtype, sf_format, tA, tB, tD, tD8, args,
+    return dispatch_mgrouped<Layout::Contiguous>(out_dtype, b_fp4, sf_format, tA, tB, tD, tD8, args,
                                                  static_cast<cudaStream_t>(stream));
 }
 
@@ -841,6 +856,22 @@ extern "C" int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sf
     (void)workspace_bytes;
     return m_grouped_contiguous(a, sfa, b, sfb, nullptr, d, out_dtype, psum, true, false, M, G, N, K, sf_format,
                                 status, stream);
+}
+
+extern "C" int dg_m_grouped_fp8_fp4_contiguous(const uint8_t* a, const uint8_t* sfa, const uint8_t* b_packed,
+                                               const uint8_t* sfb, void* d, int out_dtype, const int32_t* m_indices,
+                                               int64_t M, int G, int64_t N, int64_t K, int32_t* status,
+                                               void* stream) {
+    return m_grouped_contiguous(a, sfa, b_packed, sfb, nullptr, d, out_dtype, m_indices, false, false, M, G, N, K,
+                                DG_SF_UE8M0, status, stream, true);
+}
+
+extern "C" int dg_m_grouped_fp8_fp4_masked(const uint8_t* a, const uint8_t* sfa, const uint8_t* b_packed,
+                                           const uint8_t* sfb, void* d, int out_dtype, const int32_t* counts, int G,
+                                           int64_t cap, int64_t N, int64_t K, int expected_m, int32_t* status,
+                                           void* stream) {
+    return m_grouped_masked(a, sfa, b_packed, sfb, nullptr, d, out_dtype, counts, false, G, cap, N, K, expected_m,
+                            DG_SF_UE8M0, status, stream, true);
 }
 
 // ------------------------------------------------------------------------- test hooks

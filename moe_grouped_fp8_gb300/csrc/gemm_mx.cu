@@ -28,6 +28,14 @@
 // the row's scale for 128-K block u of the group, which the MMAs of that block select with
 // scale-factor id u: one copy of 1 KB serves four blocks.
 //
+// FP4 weights (the FP8 x FP4 form of the same kernel name, m_grouped_fp8_fp4_gemm_nt_contiguous):
+// B holds e2m1 codes, two per byte in global memory; the TMA unpacks each 16-code group of 8 bytes
+// into 16 bytes of shared memory (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B), the form kind::mxf8f6f4
+// reads for 4-bit operands, so a 128-K block of B takes the same 128 bytes per row of shared memory
+// as FP8 and every descriptor and swizzle is unchanged; the instruction's B format changes, and the
+// stage's transaction count, which counts the packed bytes the load reads (a count of the unpacked
+// footprint never completed: every wait ran out).
+//
 // The schedule comes from the device-side routing tensor in every CTA on every launch (as in
 // gemm.cu), so graph replays with changed routing never use stale state.  The K order of the
 // accumulation is fixed, with no split-K and no atomics, so every call is bitwise reproducible.
@@ -138,13 +146,16 @@ __device__ __forceinline__ uint32_t pack4(const uint8_t (&b)[SFG]) {
            (static_cast<uint32_t>(b[3]) << 24);
 }
 
-template <Layout L, bool OUT_FP32>
+template <Layout L, bool OUT_FP32, bool B_FP4>
 __global__ void __launch_bounds__(NT, 1)
     k_grouped_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const GemmArgs a) {
     using P = Plan;
     constexpr int BN = P::BN, STAGES = P::STAGES, ACC = P::ACC, A_BYTES = P::A_BYTES, STAGE_BYTES = P::STAGE_BYTES;
     constexpr int SF_SLOT = P::SF_SLOT, NB128 = P::NB128;
+    // Bytes a stage's TMA loads complete: an unpacking FP4 load counts the packed bytes it reads
+    // (half a B tile), though it fills the same shared-memory footprint as FP8.
+    constexpr uint32_t STAGE_TX = A_BYTES + (B_FP4 ? P::B_BYTES / 2 : P::B_BYTES);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int kb = 0; kb < ti.kbt; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     uint8_t* sa = ring + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], STAGE_TX);
                     if constexpr (L == Layout::Masked)
                         tma_load_3d(sa, &tmA, &full[stage], kb * BK, ti.row0, ti.e);
                     else
@@ -314,7 +325,7 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                     if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t idesc = idesc_mxf8_e4m3_ue8m0(BM, BN, u, u);
+                    const uint32_t idesc = idesc_mxf8_e4m3_ue8m0(BM, BN, u, u, B_FP4 ? MXF_E2M1 : MXF_E4M3);
                     const uint32_t sa = smem_u32(ring + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
@@ -426,9 +437,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
-template <Layout L, bool OUT_FP32>
+template <Layout L, bool OUT_FP32, bool B_FP4>
 int launch(const CUtensorMap& tA, const CUtensorMap& tB, GemmArgs args, cudaStream_t stream) {
-    auto kern = k_grouped_gemm_mx<L, OUT_FP32>;
+    auto kern = k_grouped_gemm_mx<L, OUT_FP32, B_FP4>;
     DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan::TOTAL));
     int sms = 0;
     if (int rc = device_sm_count(&sms)) return rc;
@@ -436,15 +447,20 @@ int launch(const CUtensorMap& tA, const CUtensorMap& tB, GemmArgs args, cudaStre
     return launch_pdl(kern, dim3(sms), dim3(NT), Plan::TOTAL, stream, tA, tB, args);
 }
 
+template <Layout L>
+int launch_l(bool out_fp32, bool b_fp4, const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
+             cudaStream_t stream) {
+    if (b_fp4)
+        return out_fp32 ? launch<L, true, true>(tA, tB, args, stream) : launch<L, false, true>(tA, tB, args, stream);
+    return out_fp32 ? launch<L, true, false>(tA, tB, args, stream) : launch<L, false, false>(tA, tB, args, stream);
+}
+
 }  // namespace mx
 
-int launch_mgrouped_mx(Layout L, bool out_fp32, const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
-                       cudaStream_t stream) {
-    if (L == Layout::Masked)
-        return out_fp32 ? mx::launch<Layout::Masked, true>(tA, tB, args, stream)
-                        : mx::launch<Layout::Masked, false>(tA, tB, args, stream);
-    return out_fp32 ? mx::launch<Layout::Contiguous, true>(tA, tB, args, stream)
-                    : mx::launch<Layout::Contiguous, false>(tA, tB, args, stream);
+int launch_mgrouped_mx(Layout L, bool out_fp32, bool b_fp4, const CUtensorMap& tA, const CUtensorMap& tB,
+                       const GemmArgs& args, cudaStream_t stream) {
+    if (L == Layout::Masked) return mx::launch_l<Layout::Masked>(out_fp32, b_fp4, tA, tB, args, stream);
+    return mx::launch_l<Layout::Contiguous>(out_fp32, b_fp4, tA, tB, args, stream);
 }
 
 }  // namespace dg

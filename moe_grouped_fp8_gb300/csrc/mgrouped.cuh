@@ -200,10 +200,11 @@ __device__ int tile_prefix(int R, int num_nb, const RunTable& rt, int* s_scan, i
 }
 
 // The block-scaled MMA kernel for UE8M0 scales (gemm_mx.cu): 128 x 256 tiles, N % 256 == 0; its
-// B tensor map has boxes of 128 (K) x 256 rows.  Returns DG_OK or an error.
+// B tensor map has boxes of 128 (K) x 256 rows (FP8 codes, or FP4 codes unpacked to 16-byte
+// groups when b_fp4).  Returns DG_OK or an error.
 constexpr int MX_BN = 256;
-int launch_mgrouped_mx(Layout L, bool out_fp32, const CUtensorMap& tA, const CUtensorMap& tB, const GemmArgs& args,
-                       cudaStream_t stream);
+int launch_mgrouped_mx(Layout L, bool out_fp32, bool b_fp4, const CUtensorMap& tA, const CUtensorMap& tB,
+                       const GemmArgs& args, cudaStream_t stream);
 
 // A tile of the launch's schedule (decoded from its index by every role of a CTA).
 struct TileInfo {

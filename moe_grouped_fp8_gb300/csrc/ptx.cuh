@@ -252,14 +252,17 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
-// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4 (block-scaled) with e4m3 A and B (both
-// K-major), an fp32 accumulator and UE8M0 scale factors: bits 4-5 B scale-factor id, 7-9 A format
-// (0 = e4m3), 10-12 B format (0 = e4m3), 15/16 A/B major (0 = K), 17-22 N >> 3, 23 scale type
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4 (block-scaled) with e4m3 A, e4m3 or e2m1 B
+// (both K-major), an fp32 accumulator and UE8M0 scale factors: bits 4-5 B scale-factor id, 7-9 A
+// format (0 = e4m3), 10-12 B format (0 = e4m3, 5 = e2m1), 15/16 A/B major (0 = K), 17-22 N >> 3, 23 scale type
 // (1 = UE8M0), 24-28 M >> 4, 29-30 A scale-factor id, 31 K size (0 = dense K 32).  The scale-factor
 // ids pick the byte of each 32-bit tensor-memory word that holds a row's scale (id i: bits 8i..8i+7).
-__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3_ue8m0(int M, int N, uint32_t sfa_id = 0, uint32_t sfb_id = 0) {
-    return ((sfb_id & 3u) << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(M >> 4) << 24) | ((sfa_id & 3u) << 29);
+// Operand formats of kind::mxf8f6f4 (bits 7-9 for A, 10-12 for B): e4m3 = 0, e2m1 = 5.
+constexpr uint32_t MXF_E4M3 = 0u, MXF_E2M1 = 5u;
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3_ue8m0(int M, int N, uint32_t sfa_id = 0, uint32_t sfb_id = 0,
+                                                             uint32_t b_fmt = MXF_E4M3) {
+    return ((sfb_id & 3u) << 4) | (MXF_E4M3 << 7) | ((b_fmt & 7u) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | ((sfa_id & 3u) << 29);
 }
 
 // D[tmem] (+)= (A . 2^sfa)[smem] * (B . 2^sfb)[smem]^T, M x N x 32 (e4m3) with one UE8M0 scale per

@@ -11,6 +11,7 @@
 #include <atomic>
 
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "host_common.hpp"
@@ -257,6 +258,74 @@ __global__ void __launch_bounds__(256) k_quant_block_128x128(const uint16_t* __r
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// 128x128 per-block cast of FP4 (e2m1) weights, the weight operand of the FP8 x FP4 m-grouped
+// GEMM ("SM120 m_grouped_fp8 contiguous kernel: illegal memory access at CUDA graph replay",
+// #444: m_grouped_fp8_fp4_gemm_nt_contiguous, weights with 2^k scales).  The FP8 block cast's
+// rule with e2m1's maximum 6 in place of 448: sf = amax / 6 (IEEE division), zero -> sf_zero,
+// >= 1e-30, rounded up to a power of two (UE8M0); codes e2m1(x * (1/sf)) with round-to-nearest-
+// even and saturation.  Two codes per byte along K, the even element in the low nibble.  The
+// thread layout is the FP8 block cast's.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_block_128x128_fp4(const uint16_t* __restrict__ w, int64_t N, int64_t K,
+                                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ sfb,
+                                                                 float sf_zero) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t NB = N / 128, KB = K / 128;
+    const int64_t blk = blockIdx.x;
+    const int64_t kb = blk % KB;
+    const int64_t nb = (blk / KB) % NB;
+    const int64_t g = blk / (KB * NB);
+    const int t = threadIdx.x;
+    const int c = t & 15, r0 = t >> 4;
+    const uint16_t* base = w + (g * N + nb * 128) * K + kb * 128;
+
+    uint4 raw[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        raw[j] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<int64_t>(r0 + 16 * j) * K) + c);
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float f[8];
+        bf16x8_to_float(raw[j], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    __shared__ float s_amax[8];
+    if ((t & 31) == 0) s_amax[t >> 5] = amax;
+    __syncthreads();
+    amax = s_amax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_amax[i]);
+
+    float sf = __fdiv_rn(amax, 6.0f);
+    if (sf == 0.0f) sf = sf_zero;
+    sf = fmaxf(sf, 1e-30f);
+    uint8_t byte = 0;
+    sf = ue8m0_round_up(sf, &byte);
+    const float r = __frcp_rn(sf);
+    // 16 consecutive bytes of a packed row hold 32 codes; this thread's 8 values are 4 bytes
+    uint8_t* qb = q + ((g * N + nb * 128) * K + kb * 128) / 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float f[8];
+        bf16x8_to_float(raw[j], f);
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_fp4x2_storage_t two = __nv_cvt_float2_to_fp4x2(
+                make_float2(__fmul_rn(f[2 * i], r), __fmul_rn(f[2 * i + 1], r)), __NV_E2M1, cudaRoundNearest);
+            word |= static_cast<uint32_t>(two) << (8 * i);
+        }
+        *reinterpret_cast<uint32_t*>(qb + static_cast<int64_t>(r0 + 16 * j) * (K / 2) + c * 4) = word;
+    }
+    if (t == 0) sfb[(g * NB + nb) * KB + kb] = byte;
+}
+
 // One or two operands cast per launch (the two operands of a k-grouped wgrad share ks).
 __global__ void __launch_bounds__(256) k_quant_channel_128(const ChannelOperand op0, const ChannelOperand op1,
                                                            int nblk0, int64_t K_cap, const int32_t* __restrict__ ks,
@@ -388,6 +457,20 @@ extern "C" int dg_quant_block_128x128(const void* w, int G, int64_t N, int64_t K
     if (sf_format == DG_SF_UE8M0)
         return launch_pdl(k_quant_block_128x128<true>, grid, dim3(256), 0, s, wp, N, K, q, sfb, sf_zero);
     return launch_pdl(k_quant_block_128x128<false>, grid, dim3(256), 0, s, wp, N, K, q, sfb, sf_zero);
+}
+
+extern "C" int dg_quant_block_128x128_fp4(const void* w, int G, int64_t N, int64_t K, uint8_t* q_packed,
+                                          uint8_t* sfb, float sf_zero, void* stream) {
+    DG_CHECK_ARG(G >= 0 && N >= 0 && K >= 0 && N % 128 == 0 && K % 128 == 0,
+                 "need N and K multiples of 128 (G=%d N=%lld K=%lld)", G, (long long)N, (long long)K);
+    const int64_t blocks = static_cast<int64_t>(G) * (N / 128) * (K / 128);
+    if (blocks == 0) return DG_OK;
+    DG_CHECK_ARG(w && q_packed && sfb, "null pointer argument");
+    DG_CHECK_ARG(aligned16(w) && ((reinterpret_cast<uintptr_t>(q_packed) & 3u) == 0),
+                 "w must be 16-byte and q_packed 4-byte aligned");
+    DG_CHECK_SUPPORTED(blocks < (1ll << 31), "too many 128x128 blocks");
+    return launch_pdl(k_quant_block_128x128_fp4, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                      static_cast<cudaStream_t>(stream), static_cast<const uint16_t*>(w), N, K, q_packed, sfb, sf_zero);
 }
 
 namespace dg {
