@@ -167,11 +167,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 }
 
 // Tile prefetches into L2 (no shared memory, no completion): a later load of the same box hits L2.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tm, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
 __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tm, int32_t x, int32_t y, int32_t z) {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(tm)),
@@ -374,135 +369,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : "memory");
 }
 
-// ------------------------------------------------------------------------------- CTA pairs
-// Helpers of the two-CTA (cluster of 2, tcgen05 cta_group::2) kernels.  A kernel that uses any
-// of the *_pair tcgen05 forms must use them for every tcgen05 allocation, MMA and commit.
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_count_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA of the cluster; orders earlier shared-memory writes (barrier
-// initialisation included) before the partner's later accesses.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-// Arrive on an mbarrier given by its cluster address (this CTA's or the partner's).  The
-// arrive keeps the default CTA-scope release: what it publishes to the partner is the
-// completion of this thread's tcgen05.ld (ordered by tcgen05.wait::ld and
-// tcgen05.fence::before_thread_sync), not global-memory data.  (Cluster-scope release and
-// acquire on the pair's barriers made the pair GEMM twice as slow.)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// try_wait on a barrier that the partner CTA or the pair's tensor core completes (the
-// default acquire, as for the barriers of single-CTA kernels).
-__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-static __device__ __noinline__ bool mbar_wait_cl_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait_cl(bar, parity)) return true;
-        if (*w.abort_flag) return false;
-        if (globaltimer_ns() - t0 > w.limit_ns) {
-            status_or(w.status, DG_STATUS_TIMEOUT);
-            *w.abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-// Bounded wait as mbar_wait, with cluster-scope acquire.
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    return mbar_wait_cl_slow(bar, parity, w);
-}
-
-// TMA tile loads into this CTA's shared memory whose completion is counted on an mbarrier
-// given by cluster address: this CTA's or the partner's.
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* tm, uint32_t bar_cl, int32_t x, int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cl)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* tm, uint32_t bar_cl, int32_t x, int32_t y,
-                                                 int32_t z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar_cl)
-        : "memory");
-}
-
-// Tensor memory of a CTA pair: one warp of each CTA executes these together.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// D[tmem of both CTAs] (+)= A[smem of both CTAs] * B[smem of both CTAs]^T: M = 256 rows (128 per
-// CTA), N columns (N / 2 B rows per CTA), K = 32 e4m3.  Issued by one thread of the even CTA.
-__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on the mbarrier at this shared-memory offset in every CTA of `cta_mask` when all
-// tcgen05 operations issued so far by this thread complete.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// acc0 += s * v0 and acc1 += s * v1 as one packed fp32 FMA; each lane rounds exactly like fmaf.
 // (y0, y1) = (x0 * s, x1 * s): one packed fp32 multiply, each lane rounded to nearest.
 __device__ __forceinline__ void fmul2(float& y0, float& y1, float x0, float x1, float s) {
     asm("{\n\t.reg .b64 d, a, b;\n\t"
@@ -521,6 +387,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+// acc0 += s * v0 and acc1 += s * v1 as one packed fp32 FMA; each lane rounds exactly like fmaf.
 __device__ __forceinline__ void ffma2(float& acc0, float& acc1, float s, float v0, float v1) {
     asm("{\n\t.reg .b64 d, a, b;\n\t"
         "mov.b64 a, {%2, %3};\n\t"
@@ -530,18 +397,6 @@ __device__ __forceinline__ void ffma2(float& acc0, float& acc1, float s, float v
         "mov.b64 {%0, %1}, d;\n\t}"
         : "+f"(acc0), "+f"(acc1)
         : "f"(v0), "f"(v1), "f"(s));
-}
-
-// Asynchronous 4-byte global -> shared copy (per thread), grouped with cp.async.commit_group.
-__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
-                 "l"(reinterpret_cast<uint64_t>(gsrc))
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 }  // namespace dg
