@@ -621,29 +621,44 @@ class MGroupedWorkload:
         d2h = rows * w.N * 2
         return ms, h2d, d2h
 
-    def oracle_step(self, channels=None):
-        """The oracle (casts of the rows and the weight slab, fp64 GEMM) on a bounded sample: every
-        row of the expert with the most tokens x its first `channels` output columns (all N by
-        default; a multiple of 128)."""
+    def _oracle_weights(self):
+        """The oracle's cast of the sampled expert's weight slab, once (weights are cast ahead of the
+        steps, on the GPU path too)."""
+        import oracle
+        if not hasattr(self, "_ow"):
+            if self.fp4:
+                qb, ueb = oracle.quant_block_128x128_fp4(self.b_slab.unsqueeze(0))
+                self._ow = (qb, oracle.ue8m0_value(ueb))
+            else:
+                qb, sb, _ = oracle.quant_block_128x128(self.b_slab.unsqueeze(0), ue8m0=bool(self.fmt))
+                self._ow = (qb, sb)
+        return self._ow
+
+    def oracle_step(self, channels=None, rows=None):
+        """One oracle step (the per-token cast of the rows, the fp64 GEMM) on a bounded sample: the
+        first `rows` rows (all by default) of the expert with the most tokens x its first `channels`
+        output columns (all N by default; a multiple of 128)."""
         import oracle
         w = self.w
-        ue = bool(self.fmt)
         n = w.N if channels is None else channels
-        rows = self.a_rows.shape[0]
+        r = self.a_rows.shape[0] if rows is None else rows
+        qb, sb = self._oracle_weights()
+        nb = n // 128
+        qb_n, sb_n = np.ascontiguousarray(qb[:, :n]), np.ascontiguousarray(sb[:, :nb])
         t0 = time.perf_counter()
-        qa, sa, _ = oracle.quant_per_token_1x128(self.a_rows, ue8m0=ue)
+        qa, sa, _ = oracle.quant_per_token_1x128(self.a_rows[:r], ue8m0=bool(self.fmt))
         if self.fp4:
-            qb, ueb = oracle.quant_block_128x128_fp4(self.b_slab[:n].unsqueeze(0))
-            oracle.gemm_contiguous_fp4(qa, sa, qb, oracle.ue8m0_value(ueb), np.zeros(rows, np.int32))
+            oracle.gemm_contiguous_fp4(qa, sa, qb_n, sb_n, np.zeros(r, np.int32))
         else:
-            qb, sb, _ = oracle.quant_block_128x128(self.b_slab[:n].unsqueeze(0), ue8m0=ue)
-            oracle.gemm_contiguous(qa, sa, qb, sb, np.zeros(rows, np.int32))
+            oracle.gemm_contiguous(qa, sa, qb_n, sb_n, np.zeros(r, np.int32))
         dt = time.perf_counter() - t0
-        return dt, 2.0 * rows * n * w.K
+        return dt, 2.0 * r * n * w.K
 
-    def oracle_sample(self, channels=None):
+    def oracle_sample(self, channels=None, rows=None):
         n = self.w.N if channels is None else channels
-        return f"all {self.a_rows.shape[0]} rows of expert {self.e_sample} x {n} of {self.w.N} output columns"
+        r = self.a_rows.shape[0] if rows is None else rows
+        return (f"{r} of the {self.a_rows.shape[0]} rows of expert {self.e_sample} x {n} of {self.w.N} output "
+                "columns (activation cast + fp64 GEMM; weights cast once, ahead, as on the GPU path)")
 
     def config(self):
         w = self.w
@@ -976,22 +991,34 @@ def run_reference(args, ws, rank, local):
         dt64, _ = wk.oracle_step(64)
         per_ch = dt64 / 64
         n = int(max(1, min(wk.N, budget / per_ch)))
-    elif hasattr(wk, "oracle_sample"):
-        dt128, _ = wk.oracle_step(128)            # output columns in blocks of 128 (the weight-cast unit)
-        n = int(max(1, min(wk.w.N // 128, budget / dt128))) * 128
+    rows = None
+    if hasattr(wk, "oracle_sample"):
+        # cost of one row x one 128-column block, then as many blocks of all rows as the budget
+        # allows, or fewer rows when one block of all of them is already too long
+        all_rows = wk.a_rows.shape[0]
+        probe = min(8, all_rows)
+        wk.oracle_step(128, probe)
+        dt, _ = wk.oracle_step(128, probe)
+        unit = dt / probe
+        nblk = int(budget / (unit * all_rows))
+        if nblk >= 1:
+            n, rows = min(wk.w.N // 128, nblk) * 128, all_rows
+        else:
+            n, rows = 128, int(max(1, min(all_rows, budget / unit)))
+    step = (lambda: wk.oracle_step(n, rows)) if rows is not None else (lambda: wk.oracle_step(n))
     for _ in range(args.warmup):
-        wk.oracle_step(n)
+        step()
     t0 = time.perf_counter()
     flops = 0.0
     for _ in range(args.steps):
-        _, fl = wk.oracle_step(n)
+        _, fl = step()
         flops += fl
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     if isinstance(wk, KGroupedWorkload):
         sample = f"{n} of {wk.N} grad_y channels x all {wk.T} tokens x {wk.H} act channels per step"
     elif hasattr(wk, "oracle_sample"):
-        sample = wk.oracle_sample(n) + " per step"
+        sample = wk.oracle_sample(n, rows) + " per step"
     else:
         sample = "4 routed rows x one 128-column block per step"
     line = {"impl": "reference", "metric": getattr(wk, "metric", "grouped FP8 GEMM TFLOP/s on valid rows; % of GB300 FP8 tensor/HBM roofline"),

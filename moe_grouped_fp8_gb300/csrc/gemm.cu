@@ -613,10 +613,14 @@ bool use_mx(int fmt, int64_t N, int64_t K) {
     return f == 2 || K / BK >= MX_MIN_KB;
 }
 
+// The element type of the weight operand (a distinct type, so that it cannot be passed for an
+// int argument).
+enum class Weights { Fp8, Fp4 };
+
 template <Layout L>
-int dispatch_mgrouped(int out, int fmt, bool b_fp4, const CUtensorMap& tA, const CUtensorMap& tB,
+int dispatch_mgrouped(int out, int fmt, Weights wt, const CUtensorMap& tA, const CUtensorMap& tB,
                       const CUtensorMap& tD, const CUtensorMap& tD8, GemmArgs args, cudaStream_t s) {
-    if (b_fp4) return launch_mgrouped_mx(L, out == DG_OUT_FP32, true, tA, tB, args, s);
+    if (wt == Weights::Fp4) return launch_mgrouped_mx(L, out == DG_OUT_FP32, true, tA, tB, args, s);
     if (use_mx(fmt, args.N, args.K)) return launch_mgrouped_mx(L, out == DG_OUT_FP32, false, tA, tB, args, s);
     const int bn = single_bn(out, args.N);
     args.num_nb = static_cast<int>(args.N / bn);
@@ -743,7 +747,8 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     args.KB = static_cast<int>(K / BK);
     args.n128 = static_cast<int>(N / 128);
     args.N = N;
-    return dispatch_mgrouped<Layout::Masked>(out_dtype, b_fp4, sf_format, tA, tB, tD, tD8, args,
+    return dispatch_mgrouped<Layout::Masked>(out_dtype, sf_format, b_fp4 ? Weights::Fp4 : Weights::Fp8, tA, tB, tD,
+                                             tD8, args,
                                              static_cast<cudaStream_t>(stream));
 }
 
@@ -806,7 +811,8 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     args.KB = static_cast<int>(K / BK);
     args.n128 = static_cast<int>(N / 128);
     args.N = N;
-    return dispatch_mgrouped<Layout::Contiguous>(out_dtype, b_fp4, sf_format, tA, tB, tD, tD8, args,
+    return dispatch_mgrouped<Layout::Contiguous>(out_dtype, sf_format, b_fp4 ? Weights::Fp4 : Weights::Fp8, tA, tB,
+                                                 tD, tD8, args,
                                                  static_cast<cudaStream_t>(stream));
 }
 
