@@ -553,10 +553,10 @@ class MGroupedWorkload:
     def e2e(self, steps, stream):
         """The same step through the C ABI from pinned host buffers: every step copies each expert's
         token rows (bf16) and the routing tensor (counts or m_indices) host -> device, runs the cast
-        and the GEMM, and copies each expert's output rows device -> host.  Double-buffered as a
-        serving loop runs it: device buffers alternate between two sets, copies in and out run on
-        their own streams, so step i's D2H overlaps step i + 1's H2D and compute; events order each
-        buffer's reuse.  A step's per-expert copies (one per expert each way) are captured once per
+        and the GEMM, and copies each expert's output rows device -> host.  Pipelined as a serving
+        loop runs it: device buffers rotate over NBUF sets, copies in and out run on their own
+        streams, so step i's D2H, step i + 1's compute and step i + 2's H2D overlap; events order
+        each buffer's reuse.  A step's per-expert copies (one per expert each way) are captured once per
         buffer set as a CUDA graph and replayed, so that issuing them costs one launch instead of
         one host call per expert.  Returns ms per step and the bytes copied each way per step."""
         w = self.w
@@ -566,13 +566,14 @@ class MGroupedWorkload:
         route_dev = self.counts if self.masked else self.mi
         route_h = route_dev.cpu().pin_memory()
         d_flat = self.d.view(-1, w.N)
-        d_h = [torch.empty(rows, w.N, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        NBUF = 3
+        d_h = [torch.empty(rows, w.N, dtype=torch.bfloat16).pin_memory() for _ in range(NBUF)]
         bufs = [dict(a=torch.empty_like(self.a), route=torch.empty_like(route_dev), d=torch.empty_like(d_flat))
-                for _ in range(2)]
+                for _ in range(NBUF)]
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
-        g_in, g_out = [torch.cuda.CUDAGraph() for _ in range(2)], [torch.cuda.CUDAGraph() for _ in range(2)]
-        for b in range(2):
+        ev = {k: [torch.cuda.Event() for _ in range(NBUF)] for k in ("in", "comp", "out")}
+        g_in, g_out = [torch.cuda.CUDAGraph() for _ in range(NBUF)], [torch.cuda.CUDAGraph() for _ in range(NBUF)]
+        for b in range(NBUF):
             x = bufs[b]
             with torch.cuda.graph(g_in[b], stream=s_in):
                 for r0, h0, n in segs:
@@ -582,11 +583,11 @@ class MGroupedWorkload:
                 for r0, h0, n in segs:
                     d_h[b][h0:h0 + n].copy_(x["d"][r0:r0 + n], non_blocking=True)
         torch.cuda.synchronize()
-        for b in range(2):
+        for b in range(NBUF):
             ev["out"][b].record(stream)
 
         def one(i):
-            b = i & 1
+            b = i % NBUF
             x = bufs[b]
             s_in.wait_event(ev["out"][b])
             with torch.cuda.stream(s_in):
@@ -951,9 +952,10 @@ def run_ours(args, ws, rank, local):
         ms_e2e, h2d, d2h = e2e
         line["e2e"] = {"value": round(ws * wk.flops / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
-                       "loop": "pinned host buffers, two device buffer sets; step i's D2H overlaps step i+1's H2D"
-                    + ("; per-expert copies replayed from a CUDA graph per buffer set"
-                       if isinstance(wk, MGroupedWorkload) else "")}
+                       "loop": ("pinned host buffers, three device buffer sets rotating: step i's D2H, step i+1's compute "
+                     "and step i+2's H2D overlap; per-expert copies replayed from a CUDA graph per buffer set"
+                     if isinstance(wk, MGroupedWorkload) else
+                     "pinned host buffers, two device buffer sets; step i's D2H overlaps step i+1's H2D")}
     else:
         line["e2e"] = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
