@@ -131,10 +131,10 @@ class ClockSampler:
 # The sources each GEMM kernel is compiled from: a profile summary stays valid while they are
 # unchanged (its kernel_source_sha line records their hash at capture time).
 KERNEL_SOURCES = {
-    "k_kgrouped_gemm": ["kgrouped.cu", "kernel_common.cuh", "ptx.cuh"],
-    "k_grouped_gemm": ["gemm.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
-    "k_grouped_gemm_mx": ["gemm_mx.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
-    "k_grouped_gemm_bf16": ["gemm_bf16.cu", "mgrouped.cuh", "kernel_common.cuh", "ptx.cuh"],
+    "k_kgrouped_gemm": ["kgrouped.cu", "kernel_common.cuh", "debug.cuh", "ptx.cuh"],
+    "k_grouped_gemm": ["gemm.cu", "mgrouped.cuh", "kernel_common.cuh", "debug.cuh", "ptx.cuh"],
+    "k_grouped_gemm_mx": ["gemm_mx.cu", "mgrouped.cuh", "kernel_common.cuh", "debug.cuh", "ptx.cuh"],
+    "k_grouped_gemm_bf16": ["gemm_bf16.cu", "mgrouped.cuh", "kernel_common.cuh", "debug.cuh", "ptx.cuh"],
 }
 
 
@@ -550,15 +550,24 @@ class MGroupedWorkload:
                 h += int(n)
         return segs, h
 
+    def e2e_loop_note(self):
+        moves = ("the experts' rows packed, one copy each way: the cast reads them packed, the output's "
+                 "valid rows are packed on the device before their copy" if self.masked else
+                 "per-expert copies")
+        return ("pinned host buffers, three device buffer sets rotating: step i's D2H, step i+1's compute and "
+                f"step i+2's H2D overlap; {moves}; copies replayed from a CUDA graph per buffer set")
+
     def e2e(self, steps, stream):
         """The same step through the C ABI from pinned host buffers: every step copies each expert's
         token rows (bf16) and the routing tensor (counts or m_indices) host -> device, runs the cast
         and the GEMM, and copies each expert's output rows device -> host.  Pipelined as a serving
         loop runs it: device buffers rotate over NBUF sets, copies in and out run on their own
         streams, so step i's D2H, step i + 1's compute and step i + 2's H2D overlap; events order
-        each buffer's reuse.  A step's per-expert copies (one per expert each way) are captured once per
-        buffer set as a CUDA graph and replayed, so that issuing them costs one launch instead of
-        one host call per expert.  Returns ms per step and the bytes copied each way per step."""
+        each buffer's reuse.  Masked layouts move the rows packed (one copy each way: the packed
+        cast reads them at the front of the activation buffer, and the output's valid rows are
+        packed on the device); contiguous layouts copy each expert's segment.  A step's copies are
+        captured once per buffer set as a CUDA graph and replayed.  Returns ms per step and the
+        bytes copied each way per step."""
         w = self.w
         segs, rows = self.segments()
         idx = torch.cat([torch.arange(r0, r0 + n) for r0, _, n in segs]).to(self.a.device)
@@ -570,18 +579,29 @@ class MGroupedWorkload:
         d_h = [torch.empty(rows, w.N, dtype=torch.bfloat16).pin_memory() for _ in range(NBUF)]
         bufs = [dict(a=torch.empty_like(self.a), route=torch.empty_like(route_dev), d=torch.empty_like(d_flat))
                 for _ in range(NBUF)]
+        if self.masked:
+            # masked: the experts' rows travel packed (one copy each way); the cast reads them packed
+            # and the output's valid rows are packed on the device before their copy out
+            for x in bufs:
+                x["d_pk"] = torch.empty_like(d_flat)
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         ev = {k: [torch.cuda.Event() for _ in range(NBUF)] for k in ("in", "comp", "out")}
         g_in, g_out = [torch.cuda.CUDAGraph() for _ in range(NBUF)], [torch.cuda.CUDAGraph() for _ in range(NBUF)]
         for b in range(NBUF):
             x = bufs[b]
             with torch.cuda.graph(g_in[b], stream=s_in):
-                for r0, h0, n in segs:
-                    x["a"][r0:r0 + n].copy_(a_h[h0:h0 + n], non_blocking=True)
+                if self.masked:
+                    x["a"][:rows].copy_(a_h, non_blocking=True)
+                else:
+                    for r0, h0, n in segs:
+                        x["a"][r0:r0 + n].copy_(a_h[h0:h0 + n], non_blocking=True)
                 x["route"].copy_(route_h, non_blocking=True)
             with torch.cuda.graph(g_out[b], stream=s_out):
-                for r0, h0, n in segs:
-                    d_h[b][h0:h0 + n].copy_(x["d"][r0:r0 + n], non_blocking=True)
+                if self.masked:
+                    d_h[b].copy_(x["d_pk"][:rows], non_blocking=True)
+                else:
+                    for r0, h0, n in segs:
+                        d_h[b][h0:h0 + n].copy_(x["d"][r0:r0 + n], non_blocking=True)
         torch.cuda.synchronize()
         for b in range(NBUF):
             ev["out"][b].record(stream)
@@ -596,10 +616,12 @@ class MGroupedWorkload:
             stream.wait_event(ev["in"][b])
             with torch.cuda.stream(stream):
                 if self.masked:
-                    self.api.dg_quant_per_token_1x128(x["a"], self.qa, self.sfa, self.fmt, row_counts=x["route"])
+                    self.api.dg_quant_per_token_1x128_packed(x["a"], self.qa, self.sfa, x["route"], self.fmt)
                 else:
                     self.api.dg_quant_per_token_1x128_routed(x["a"], self.qa, self.sfa, x["route"], self.fmt)
                 self.gemm_into(x["d"].view(self.d.shape), x["route"])
+                if self.masked:
+                    self.api.dg_pack_masked_rows(x["d"].view(self.d.shape), x["route"], x["d_pk"])
             ev["comp"][b].record(stream)
             s_out.wait_event(ev["comp"][b])
             with torch.cuda.stream(s_out):
@@ -952,10 +974,8 @@ def run_ours(args, ws, rank, local):
         ms_e2e, h2d, d2h = e2e
         line["e2e"] = {"value": round(ws * wk.flops / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
-                       "loop": ("pinned host buffers, three device buffer sets rotating: step i's D2H, step i+1's compute "
-                     "and step i+2's H2D overlap; per-expert copies replayed from a CUDA graph per buffer set"
-                     if isinstance(wk, MGroupedWorkload) else
-                     "pinned host buffers, two device buffer sets; step i's D2H overlaps step i+1's H2D")}
+                       "loop": wk.e2e_loop_note() if isinstance(wk, MGroupedWorkload) else
+                       "pinned host buffers, two device buffer sets; step i's D2H overlaps step i+1's H2D"}
     else:
         line["e2e"] = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -101,6 +101,33 @@ int dg_quant_per_token_1x128_routed(const void* x, int64_t M, int64_t K, int64_t
                                     const int32_t* m_indices, void* stream);
 
 /*
+ * The masked per-token cast reading its rows packed: the tokens routed to each expert arrive
+ * one expert after another ([P2] masked call: group g holds masked_m[g] valid rows of its
+ * [cap, K] slice), and are cast straight into the masked [G, cap, K] layout the masked GEMM
+ * reads, with no scatter in between.  Group g's valid rows r < v_g = clamp(row_counts[g], 0, cap)
+ * are rows P_g + r of x, P_g = v_0 + ... + v_(g-1); each is cast exactly as by
+ * dg_quant_per_token_1x128 into row g*cap + r of q and sfa.  Rows of q and sfa at or past a
+ * group's count are not written.
+ *   x:  bf16, the packed rows at its front; its capacity is G*cap rows (row stride ldx).
+ *   q, sfa: as for dg_quant_per_token_1x128 with M = G*cap.   row_counts: int32 [G].
+ *   1 <= G <= DG_MAX_GROUPS.
+ */
+int dg_quant_per_token_1x128_packed(const void* x, int64_t K, int64_t ldx, uint8_t* q, void* sfa,
+                                    int sf_format, float sf_zero, const int32_t* row_counts, int G,
+                                    int64_t cap, void* stream);
+
+/*
+ * The inverse movement for an output: the valid rows of a masked [G, cap] array of rows (the
+ * masked GEMM's [G, cap, N] output, [P2] 3-D store) packed one group after another, so that
+ * they leave the device in one copy.  Row r < v_g of group g (v_g as above) is copied byte for
+ * byte to row P_g + r of dst.
+ *   src: [G, cap] rows of row_bytes bytes (a multiple of 16); dst: capacity G*cap rows of
+ *   row_bytes; both 16-byte aligned.   counts: int32 [G].   1 <= G <= DG_MAX_GROUPS.
+ */
+int dg_pack_masked_rows(const void* src, int G, int64_t cap, int64_t row_bytes, const int32_t* counts,
+                        void* dst, void* stream);
+
+/*
  * Per-channel cast over 128-token blocks with the per-expert K-major pack ([P1] repro:
  * `_per_channel_cast_to_fp8(x, gran_k=128, sf_val)` then `_pack_kmajor`).  For every
  * 128-token block tb inside sum(ks) and every column c: amax over the 128 tokens, then the
@@ -364,6 +391,39 @@ int dg_m_grouped_fp8_fp4_masked(const uint8_t* a, const uint8_t* sfa, const uint
 int dg_k_grouped_fp8_wgrad_noalloc(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
                                    const float* sfb, const float* c, float* d, const int32_t* ks, int G,
                                    int64_t K_cap, int64_t N, int64_t H, int32_t* status, void* stream);
+
+/*
+ * Debug aids ([P3], "What fails" and "Evidence / repro kit": the arguments of the failing
+ * call were dumped inside the serving process and replayed offline).  Here the same search uses
+ * a host-side argument log, and a debug build whose kernels check the indices they compute
+ * (the kernels never trap, so a bad index shows as a bit, not as a fault).
+ *
+ * Argument log.  dg_set_arg_log(path) makes every entry point above append one text line to
+ * the file `path` before it checks its arguments: a sequence number, the entry point's name
+ * and name=value for every argument (pointers in hex, sizes in decimal, floats with 9
+ * significant digits).  NULL or "" stops the log.  The environment variable DG_ARG_LOG, read
+ * when the library is loaded, sets the first path.  The log reads nothing from the device, so
+ * it is safe inside stream capture; it records calls, not graph replays.  Returns DG_OK.
+ *
+ * Debug build.  Built with -DDG_DEBUG=1 (libdg_debug.so), every kernel checks each index it
+ * computes for a scale read, an owner-thread store, a C read or a cast's element access against
+ * the extent the layouts above give that buffer; an index outside it ORs a DG_DEBUG_* bit into
+ * the library's debug word and the access is skipped.  In the release build nothing is checked.
+ *   dg_debug_build(): 1 for the debug build, 0 for the release build.
+ *   dg_debug_word(out, clear): waits for the current device (cudaDeviceSynchronize), then
+ *   stores in *out (a HOST pointer) the OR of the bits raised on it since the last clear, and
+ *   clears them if `clear` != 0.  The release build stores 0.  Returns DG_OK or DG_ERR_CUDA.
+ */
+enum dg_debug_bits {
+    DG_DEBUG_A_SCALE = 1,  /* an activation-scale (sfa) index outside [K/128][Mp] */
+    DG_DEBUG_B_SCALE = 2,  /* a weight-scale (sfb) index outside [G][N/128][K/128] */
+    DG_DEBUG_OUT = 4,      /* an output (or C) row or column outside D */
+    DG_DEBUG_CAST_IN = 8,  /* a cast's input element outside x / w */
+    DG_DEBUG_CAST_OUT = 16 /* a cast's code or scale outside q / sf */
+};
+int dg_set_arg_log(const char* path);
+int dg_debug_build(void);
+int dg_debug_word(uint32_t* out, int clear);
 
 #ifdef __cplusplus
 }

@@ -6,7 +6,7 @@ import ctypes
 import os
 import threading
 
-from .build import LIB
+from .build import library_path
 
 DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_CUDA = 0, 1, 2, 3
 DG_SF_FP32, DG_SF_UE8M0 = 0, 1
@@ -17,6 +17,7 @@ DG_STATUS_K_NOT_ALIGNED = 4
 DG_STATUS_K_OVERFLOW = 8
 DG_STATUS_TIMEOUT = 16
 DG_STATUS_TOO_MANY_RUNS = 32
+DG_DEBUG_A_SCALE, DG_DEBUG_B_SCALE, DG_DEBUG_OUT, DG_DEBUG_CAST_IN, DG_DEBUG_CAST_OUT = 1, 2, 4, 8, 16
 DG_OP_M_GROUPED_CONTIGUOUS, DG_OP_M_GROUPED_MASKED, DG_OP_K_GROUPED_WGRAD = 0, 1, 2
 DG_MAX_GROUPS = 1024
 DG_MAX_M_BLOCKS = 4096
@@ -49,6 +50,11 @@ SIGNATURES = {
     "dg_quant_block_128x128_fp4": (I32, [P, I32, I64, I64, P, P, F32, P]),
     "dg_m_grouped_fp8_fp4_contiguous": (I32, [P, P, P, P, P, I32, P, I64, I32, I64, I64, P, P]),
     "dg_m_grouped_fp8_fp4_masked": (I32, [P, P, P, P, P, I32, P, I32, I64, I64, I64, I32, P, P]),
+    "dg_quant_per_token_1x128_packed": (I32, [P, I64, I64, P, P, I32, F32, P, I32, I64, P]),
+    "dg_pack_masked_rows": (I32, [P, I32, I64, I64, P, P, P]),
+    "dg_set_arg_log": (I32, [ctypes.c_char_p]),
+    "dg_debug_build": (I32, []),
+    "dg_debug_word": (I32, [ctypes.POINTER(ctypes.c_uint32), I32]),
 }
 # test hooks exported by the library (not part of include/dg.h)
 TESTING_SIGNATURES = {
@@ -61,6 +67,7 @@ TESTING_SIGNATURES = {
     "dg_testing_mgrouped_store": (I32, [I32]),
     "dg_testing_mgrouped_bn": (I32, [I32]),
     "dg_testing_token_items_per_cta": (I32, [I32]),
+    "dg_testing_debug_out_rows": (I32, [I64]),
 }
 
 _lock = threading.Lock()
@@ -74,13 +81,16 @@ class DGError(RuntimeError):
 
 
 def load() -> ctypes.CDLL:
+    """The library of this process: libdg.so, or the debug build libdg_debug.so when the
+    environment sets DG_DEBUG=1."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB):
-                raise RuntimeError(f"{LIB} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
-                                   "(or moe_grouped_fp8_gb300.build.build()); there is no fallback path")
-            lib = ctypes.CDLL(LIB)
+            path = library_path(os.environ.get("DG_DEBUG", "0") == "1")
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                                   "(or moe_grouped_fp8_gb300.build.build(debug=...)); there is no fallback path")
+            lib = ctypes.CDLL(path)
             for name, (res, args) in {**SIGNATURES, **TESTING_SIGNATURES}.items():
                 fn = getattr(lib, name)
                 fn.restype = res

@@ -100,6 +100,34 @@ def dg_quant_per_token_1x128_routed(x, q, sfa, m_indices, sf_format=DG_SF_FP32, 
                                                  _p(m_indices), _s(stream)))
 
 
+def dg_quant_per_token_1x128_packed(x, q, sfa, row_counts, sf_format=DG_SF_FP32, sf_zero=1e-30, stream=None):
+    """The masked cast from packed rows: x bf16 [G*cap, K] holds each group's valid rows packed at
+    its front, group after group; q e4m3/uint8 [G, cap, K] (or [G*cap, K]), sfa [K/128][Mp]
+    (Mp from G*cap) receive them at the masked positions; row_counts int32 [G]."""
+    _dev(x, q, sfa, row_counts)
+    _need(row_counts.dtype == torch.int32 and row_counts.is_contiguous(), "row_counts must be int32")
+    G = row_counts.numel()
+    qq = q.view(-1, q.shape[-1])
+    _need(G >= 1 and qq.shape[0] % G == 0, "q rows must be G x cap")
+    cap = qq.shape[0] // G
+    M, K = _token_cast_shapes(x, qq, sfa, sf_format)
+    _need(M == G * cap, "x must have G x cap rows")
+    check(load().dg_quant_per_token_1x128_packed(_p(x), K, x.stride(0), _p(qq), _p(sfa), sf_format, sf_zero,
+                                                 _p(row_counts), G, cap, _s(stream)))
+
+
+def dg_pack_masked_rows(src, counts, dst, stream=None):
+    """src [G, cap, ...] (contiguous) -> dst (capacity G*cap rows of the same row size): each
+    group's first clamp(count, 0, cap) rows, packed group after group; counts int32 [G]."""
+    _dev(src, counts, dst)
+    _need(src.is_contiguous() and dst.is_contiguous() and src.dim() >= 2, "contiguous src [G, cap, ...] and dst")
+    G, cap = src.shape[0], src.shape[1]
+    _need(counts.dtype == torch.int32 and counts.numel() == G, "counts must be int32 [G]")
+    row_bytes = src[0, 0].numel() * src.element_size() if cap > 0 else 0
+    _need(dst.numel() * dst.element_size() >= G * cap * row_bytes, "dst must hold G x cap rows")
+    check(load().dg_pack_masked_rows(_p(src), G, cap, row_bytes, _p(counts), _p(dst), _s(stream)))
+
+
 def dg_quant_per_channel_128(x, ks, q_packed, sf, sf_zero=1e-30, status=None, stream=None, _fn="dg_quant_per_channel_128"):
     """x bf16 [K_cap, C] token-major -> q_packed [K_cap*C] per-expert K-major, sf fp32 [K_cap/128][C]."""
     _dev(x, ks, q_packed, sf, status)
@@ -372,3 +400,23 @@ def dg_k_grouped_fp8_wgrad_noalloc(a_packed, sfa, b_packed, sfb, c, d, ks, K_cap
     _need(a_packed.numel() >= K_cap * N and b_packed.numel() >= K_cap * H, "packed operand size")
     check(load().dg_k_grouped_fp8_wgrad_noalloc(_p(a_packed), _p(sfa), _p(b_packed), _p(sfb), _p(c), _p(d), _p(ks),
                                                 G, K_cap, N, H, _p(status), _s(stream)))
+
+
+# ---- debug aids
+
+def dg_set_arg_log(path: str | None) -> None:
+    """Append one line per entry-point call (name and arguments) to `path`; None stops it."""
+    check(load().dg_set_arg_log(None if not path else str(path).encode()))
+
+
+def dg_debug_build() -> bool:
+    """True when the loaded library is the debug build (kernels check their computed indices)."""
+    return bool(load().dg_debug_build())
+
+
+def dg_debug_word(clear: bool = True) -> int:
+    """Waits for the current device, then returns the DG_DEBUG_* bits the debug build's index
+    checks raised since the last clear (always 0 for the release build)."""
+    w = ctypes.c_uint32(0)
+    check(load().dg_debug_word(ctypes.byref(w), 1 if clear else 0))
+    return int(w.value)

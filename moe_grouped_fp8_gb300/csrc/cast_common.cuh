@@ -99,61 +99,57 @@ constexpr int CH_COLS = 64;
 constexpr int CH_PITCH = 132;  // bytes per transposed column row (128 tokens + 4 pad)
 
 // Expert lookup for token `tok`: returns the expert index with its token offset and K_e, or
-// -1 when the token lies past the last valid expert.  Walks ks with a block-wide scan in
-// chunks of blockDim.x (<= 256 threads) and stops at the first bad expert (K_e < 0,
-// K_e % 128 != 0, or a span past K_cap); *bad_bits gets the DG_STATUS_* bits it met.
+// -1 when the token lies past the last valid expert.  Warp 0 walks ks in chunks of blockDim.x
+// experts (32 at a time, with warp shuffles only) and stops after the chunk that holds the token or
+// the first bad expert (K_e < 0, K_e % 128 != 0, or a span past K_cap); *bad_bits gets the
+// DG_STATUS_* bits of every bad expert in the chunks it walked.  One CTA barrier publishes the
+// answer.
 __device__ int find_expert(const int32_t* __restrict__ ks, int psum, int G, int64_t K_cap, int64_t tok,
                            int64_t* o_out, int64_t* k_out, int* bad_bits) {
-    __shared__ long long s_warp[8];
-    __shared__ long long s_carry, s_o, s_k;
-    __shared__ int s_found, s_first_bad, s_bad;
-    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    const int nwarps = static_cast<int>(blockDim.x >> 5);
-    if (t == 0) {
-        s_carry = 0;
-        s_found = -1;
-        s_first_bad = 0x7fffffff;
-        s_bad = 0;
+    __shared__ long long s_o, s_k;
+    __shared__ int s_found, s_bad;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int chunk = static_cast<int>(blockDim.x);
+        long long carry = 0, o_f = 0, k_f = 0;
+        int found = -1, first_bad = 0x7fffffff, bits = 0;
+        for (int c0 = 0; c0 < G; c0 += chunk) {
+            for (int base = c0; base < G && base < c0 + chunk; base += 32) {
+                const int e = base + lane;
+                const long long k = e < G ? expert_k(ks, e, psum) : 0;
+                int bad = (e < G && (k < 0 || (k % 128) != 0)) ? DG_STATUS_K_NOT_ALIGNED : 0;
+                const long long kk = bad ? 0 : k;
+                long long incl = kk;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const long long o_e = carry + incl - kk;  // exclusive prefix of valid K_e
+                if (e < G && !bad && o_e + kk > K_cap) bad = DG_STATUS_K_OVERFLOW;
+                bits |= __reduce_or_sync(0xffffffffu, static_cast<unsigned>(bad));
+                const unsigned bad_lanes = __ballot_sync(0xffffffffu, bad != 0);
+                if (bad_lanes != 0 && first_bad == 0x7fffffff) first_bad = base + __ffs(bad_lanes) - 1;
+                const unsigned hit = __ballot_sync(
+                    0xffffffffu, e < G && e < first_bad && kk > 0 && tok >= o_e && tok < o_e + kk);
+                if (hit != 0) {
+                    const int src = __ffs(hit) - 1;
+                    found = base + src;
+                    o_f = __shfl_sync(0xffffffffu, o_e, src);
+                    k_f = __shfl_sync(0xffffffffu, kk, src);
+                }
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (found >= 0 || first_bad != 0x7fffffff) break;
+        }
+        if (lane == 0) {
+            s_found = found;
+            s_o = o_f;
+            s_k = k_f;
+            s_bad = bits;
+        }
     }
     __syncthreads();
-    for (int base = 0; base < G; base += blockDim.x) {
-        const int e = base + t;
-        const long long k = (e < G) ? expert_k(ks, e, psum) : 0;
-        int bad = (e < G && (k < 0 || (k % 128) != 0)) ? DG_STATUS_K_NOT_ALIGNED : 0;
-        const long long kk = bad ? 0 : k;
-        long long incl = kk;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) s_warp[wid] = incl;
-        __syncthreads();
-        long long wpre = 0;
-        for (int i = 0; i < wid; ++i) wpre += s_warp[i];
-        const long long o_e = s_carry + wpre + incl - kk;  // exclusive prefix of valid K_e
-        if (e < G && !bad && o_e + kk > K_cap) bad = DG_STATUS_K_OVERFLOW;
-        if (bad) {
-            atomicOr(&s_bad, bad);
-            atomicMin(&s_first_bad, e);
-        }
-        __syncthreads();
-        const int first_bad = s_first_bad;
-        if (e < G && e < first_bad && kk > 0 && tok >= o_e && tok < o_e + kk) {
-            s_found = e;
-            s_o = o_e;
-            s_k = kk;
-        }
-        __syncthreads();
-        const bool done = (s_found >= 0) || (first_bad != 0x7fffffff);
-        if (t == 0) {
-            long long tot = 0;
-            for (int i = 0; i < nwarps; ++i) tot += s_warp[i];
-            s_carry += tot;
-        }
-        __syncthreads();
-        if (done) break;
-    }
     *bad_bits = s_bad;
     const int f = s_found;
     if (f >= 0) {
@@ -202,9 +198,11 @@ __device__ __forceinline__ void channel_cast_cta(const ChannelOperand& op0, cons
     pdl_wait();
     // the bf16 loads do not depend on the expert lookup: issue them first (rows < K_cap exist)
     uint4 raw[4];
+    const bool in_ok = DG_CHECKED(tb * 128 + 128 <= K_cap && c0 + CH_COLS <= C, DG_DEBUG_CAST_IN);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        raw[j] = __ldg(reinterpret_cast<const uint4*>(x + (tb * 128 + rb + j) * C + c0) + c);
+        raw[j] = in_ok ? __ldg(reinterpret_cast<const uint4*>(x + (tb * 128 + rb + j) * C + c0) + c)
+                       : make_uint4(0, 0, 0, 0);
     int64_t o_e = 0, k_e = 0;
     int bad = 0;
     const int e = find_expert(ks, psum, G, K_cap, tb * 128, &o_e, &k_e, &bad);
@@ -234,7 +232,7 @@ __device__ __forceinline__ void channel_cast_cta(const ChannelOperand& op0, cons
         float sf, r;
         uint8_t unused;
         block_scale<false>(amax, sf_zero, sf, r, unused);
-        sf_out[tb * C + c0 + t] = sf;
+        if (DG_CHECKED(in_ok, DG_DEBUG_CAST_OUT)) sf_out[tb * C + c0 + t] = sf;
         s_r[t] = r;
     }
     __syncthreads();
@@ -257,7 +255,9 @@ __device__ __forceinline__ void channel_cast_cta(const ChannelOperand& op0, cons
         const int col = s >> 3, piece = s & 7;
         const uint32_t* src = reinterpret_cast<const uint32_t*>(&s_t[col * CH_PITCH + piece * 16]);
         uint4 v = make_uint4(src[0], src[1], src[2], src[3]);
-        *reinterpret_cast<uint4*>(dst_base + (c0 + col) * k_e + piece * 16) = v;
+        // the expert's [C, K_e] block lies inside the K_cap x C packed buffer
+        if (DG_CHECKED(in_ok && o_e + k_e <= K_cap && tb * 128 + 128 <= o_e + k_e, DG_DEBUG_CAST_OUT))
+            *reinterpret_cast<uint4*>(dst_base + (c0 + col) * k_e + piece * 16) = v;
     }
 }
 

@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(num_threads<EW>(), 1)
                     const int kbi = g * P::SFG + u;
                     sa[u] = 0u;
                     sb[u] = 0u;
-                    if (row_sc && kbi < ti.kbt) {
+                    if (row_sc && kbi < ti.kbt && DG_CHECKED(sfa_in<L>(a, kbi, grow), DG_DEBUG_A_SCALE) &&
+                        DG_CHECKED(sfb_in(a, ti.e, (ti.nb * BN + h2 * P::CPT) / 128, kbi), DG_DEBUG_B_SCALE)) {
                         const int64_t idx = static_cast<int64_t>(kbi) * a.sfa_ld + grow;
                         if constexpr (SF_UE8M0) {
                             sa[u] = __ldg(static_cast<const uint8_t*>(a.sfa) + idx);
@@ -410,7 +411,9 @@ __global__ void __launch_bounds__(num_threads<EW>(), 1)
             // ---- accumulate: D = C + result (fp32 output; C may alias D: each element is read by
             // the thread that later writes it, before any store of this tile)
             if constexpr (OUT_FP32) {
-                if (a.c != nullptr && row_ok && !failed) {
+                if (a.c != nullptr && row_ok && !failed &&
+                    DG_CHECKED(out_in<L>(a, grow, static_cast<int64_t>(ti.nb) * BN + h2 * P::CPT, P::CPT),
+                               DG_DEBUG_OUT)) {
                     const float* crow = a.c + grow * a.ldd + static_cast<int64_t>(ti.nb) * BN + h2 * P::CPT;
 #pragma unroll
                     for (int i = 0; i < P::CPT; i += 4) {
@@ -425,6 +428,9 @@ __global__ void __launch_bounds__(num_threads<EW>(), 1)
 
             // this thread's row of the tile (CPT columns), written from registers
             auto store_own_row = [&]() {
+                if (!DG_CHECKED(out_in<L>(a, grow, static_cast<int64_t>(ti.nb) * BN + h2 * P::CPT, P::CPT),
+                                DG_DEBUG_OUT))
+                    return;
                 uint8_t* dst = static_cast<uint8_t*>(a.d) +
                                ((grow * a.ldd) + ti.nb * BN + h2 * P::CPT) * static_cast<int64_t>(P::ESIZE);
                 constexpr int PIECES = P::CPT * P::ESIZE / 16;
@@ -514,6 +520,8 @@ namespace {
 constexpr int DIRECT_MAX_KB = 32;
 // testing: 0 automatic, 1 TMA stores issued by thread 0 of the promotion warps, 3 owner-thread stores
 std::atomic<int> g_force_store{0};
+// testing (debug build): the output rows the index checks let the stores reach; 0 = the layout's
+std::atomic<int64_t> g_debug_out_rows{0};
 
 int store_mode(int KB) {
     switch (g_force_store.load(std::memory_order_relaxed)) {
@@ -730,6 +738,9 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
             return rc;
     }
     GemmArgs args{};
+#if DG_DEBUG
+    args.dbg_rows = g_debug_out_rows.load(std::memory_order_relaxed);
+#endif
     args.routing = counts;
     args.dense = dense ? 1 : 0;
     args.c = c;
@@ -793,6 +804,9 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
             return rc;
     }
     GemmArgs args{};
+#if DG_DEBUG
+    args.dbg_rows = g_debug_out_rows.load(std::memory_order_relaxed);
+#endif
     args.routing = routing;
     args.psum = psum ? 1 : 0;
     args.dense = dense ? 1 : 0;
@@ -823,6 +837,8 @@ extern "C" int dg_m_grouped_fp8_contiguous(const uint8_t* a, const void* sfa, co
                                            void* d, int out_dtype, const int32_t* m_indices, int64_t M, int G,
                                            int64_t N, int64_t K, int sf_format, void* workspace,
                                            size_t workspace_bytes, int32_t* status, void* stream) {
+    DG_ARG_LOG(a, sfa, b, sfb, d, out_dtype, m_indices, M, G, N, K, sf_format, workspace, workspace_bytes, status,
+               stream);
     (void)workspace;
     (void)workspace_bytes;
     return m_grouped_contiguous(a, sfa, b, sfb, nullptr, d, out_dtype, m_indices, false, false, M, G, N, K,
@@ -833,6 +849,8 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
                                        int out_dtype, const int32_t* counts, int G, int64_t cap, int64_t N, int64_t K,
                                        int expected_m, int sf_format, void* workspace, size_t workspace_bytes,
                                        int32_t* status, void* stream) {
+    DG_ARG_LOG(a, sfa, b, sfb, d, out_dtype, counts, G, cap, N, K, expected_m, sf_format, workspace, workspace_bytes,
+               status, stream);
     (void)workspace;
     (void)workspace_bytes;
     return m_grouped_masked(a, sfa, b, sfb, nullptr, d, out_dtype, counts, false, G, cap, N, K, expected_m,
@@ -842,6 +860,7 @@ extern "C" int dg_m_grouped_fp8_masked(const uint8_t* a, const void* sfa, const 
 extern "C" int dg_fp8_gemm_nt(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb, const float* c,
                               void* d, int out_dtype, int64_t M, int64_t N, int64_t K, int sf_format,
                               int32_t* status, void* stream) {
+    DG_ARG_LOG(a, sfa, b, sfb, c, d, out_dtype, M, N, K, sf_format, status, stream);
     return m_grouped_contiguous(a, sfa, b, sfb, c, d, out_dtype, nullptr, true, true, M, 1, N, K, sf_format, status,
                                 stream);
 }
@@ -849,6 +868,7 @@ extern "C" int dg_fp8_gemm_nt(const uint8_t* a, const void* sfa, const uint8_t* 
 extern "C" int dg_fp8_gemm_nt_batched(const uint8_t* a, const void* sfa, const uint8_t* b, const void* sfb,
                                       const float* c, void* d, int out_dtype, int batch, int64_t M, int64_t N,
                                       int64_t K, int sf_format, int32_t* status, void* stream) {
+    DG_ARG_LOG(a, sfa, b, sfb, c, d, out_dtype, batch, M, N, K, sf_format, status, stream);
     return m_grouped_masked(a, sfa, b, sfb, c, d, out_dtype, nullptr, true, batch, M, N, K, static_cast<int>(M),
                             sf_format, status, stream);
 }
@@ -858,6 +878,7 @@ extern "C" int dg_m_grouped_fp8_contiguous_psum(const uint8_t* a, const void* sf
                                                 int64_t M, int G, int64_t N, int64_t K, int sf_format,
                                                 void* workspace, size_t workspace_bytes, int32_t* status,
                                                 void* stream) {
+    DG_ARG_LOG(a, sfa, b, sfb, d, out_dtype, psum, M, G, N, K, sf_format, workspace, workspace_bytes, status, stream);
     (void)workspace;
     (void)workspace_bytes;
     return m_grouped_contiguous(a, sfa, b, sfb, nullptr, d, out_dtype, psum, true, false, M, G, N, K, sf_format,
@@ -868,6 +889,7 @@ extern "C" int dg_m_grouped_fp8_fp4_contiguous(const uint8_t* a, const uint8_t* 
                                                const uint8_t* sfb, void* d, int out_dtype, const int32_t* m_indices,
                                                int64_t M, int G, int64_t N, int64_t K, int32_t* status,
                                                void* stream) {
+    DG_ARG_LOG(a, sfa, b_packed, sfb, d, out_dtype, m_indices, M, G, N, K, status, stream);
     return m_grouped_contiguous(a, sfa, b_packed, sfb, nullptr, d, out_dtype, m_indices, false, false, M, G, N, K,
                                 DG_SF_UE8M0, status, stream, true);
 }
@@ -876,6 +898,7 @@ extern "C" int dg_m_grouped_fp8_fp4_masked(const uint8_t* a, const uint8_t* sfa,
                                            const uint8_t* sfb, void* d, int out_dtype, const int32_t* counts, int G,
                                            int64_t cap, int64_t N, int64_t K, int expected_m, int32_t* status,
                                            void* stream) {
+    DG_ARG_LOG(a, sfa, b_packed, sfb, d, out_dtype, counts, G, cap, N, K, expected_m, status, stream);
     return m_grouped_masked(a, sfa, b_packed, sfb, nullptr, d, out_dtype, counts, false, G, cap, N, K, expected_m,
                             DG_SF_UE8M0, status, stream, true);
 }
@@ -883,6 +906,15 @@ extern "C" int dg_m_grouped_fp8_fp4_masked(const uint8_t* a, const uint8_t* sfa,
 // ------------------------------------------------------------------------- test hooks
 // Each selects, for later calls in this process, one choice the library otherwise makes
 // itself, so that the tests hold every variant to the oracle and to each other.
+// Debug build: the index checks of the m-grouped FP8 kernels' owner-thread stores treat the output
+// as `rows` rows (0 restores the layout's): rows past it are skipped and raise DG_DEBUG_OUT, which
+// exercises the checks without any access out of bounds.  No effect on the release build.
+extern "C" int dg_testing_debug_out_rows(int64_t rows) {
+    DG_CHECK_ARG(rows >= 0, "rows must be >= 0");
+    dg::g_debug_out_rows.store(rows, std::memory_order_relaxed);
+    return DG_OK;
+}
+
 // The single-CTA tile width: 0 automatic, 128, or 256 (where N allows).
 extern "C" int dg_testing_mgrouped_bn(int bn) {
     DG_CHECK_ARG(bn == 0 || bn == MG_BN || bn == MG_BN_WIDE, "bn must be 0, %d or %d", MG_BN, MG_BN_WIDE);
@@ -912,3 +944,7 @@ extern "C" int dg_testing_mgrouped_warps(int warps) {
     g_force_warps.store(warps, std::memory_order_relaxed);
     return DG_OK;
 }
+
+namespace dg {
+int debug_word_gemm(uint32_t* out, bool clear) { return debug_word_local(out, clear); }
+}  // namespace dg

@@ -324,7 +324,9 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 bulk_commit();
                 have_store = true;
             }
-            if (row_ok && row >= v8) {
+            if (row_ok && row >= v8 &&
+                DG_CHECKED(out_in<L>(a, grow, static_cast<int64_t>(ti.nb) * H_BN + h2 * P::CPT, P::CPT),
+                           DG_DEBUG_OUT)) {
                 uint8_t* dst = static_cast<uint8_t*>(a.d) +
                                ((grow * a.ldd) + ti.nb * H_BN + h2 * P::CPT) * static_cast<int64_t>(P::ESIZE);
                 constexpr int PIECES = P::CPT * P::ESIZE / 16;
@@ -428,6 +430,7 @@ using namespace dg;
 extern "C" int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, int out_dtype, const int32_t* counts,
                                         int G, int64_t cap, int64_t N, int64_t K, int expected_m, int32_t* status,
                                         void* stream) {
+    DG_ARG_LOG(a, b, d, out_dtype, counts, G, cap, N, K, expected_m, status, stream);
     (void)expected_m;
     DG_CHECK_ARG(cap >= 0, "cap must be >= 0");
     if (int rc = check_common_h(a, b, d, out_dtype, G, N, K)) return rc;
@@ -464,6 +467,7 @@ extern "C" int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, i
 extern "C" int dg_m_grouped_bf16_contiguous(const void* a, const void* b, void* d, int out_dtype,
                                             const int32_t* m_indices, int64_t M, int G, int64_t N, int64_t K,
                                             int32_t* status, void* stream) {
+    DG_ARG_LOG(a, b, d, out_dtype, m_indices, M, G, N, K, status, stream);
     DG_CHECK_ARG(M >= 0, "M must be >= 0");
     if (int rc = check_common_h(a, b, d, out_dtype, G, N, K)) return rc;
     DG_CHECK_ARG(m_indices != nullptr, "m_indices is null");
@@ -495,3 +499,7 @@ extern "C" int dg_m_grouped_bf16_contiguous(const void* a, const void* b, void* 
     args.n128 = static_cast<int>(N / 128);
     return dispatch_h<Layout::Contiguous>(out_dtype, tA, tB, tD, tD8, args, static_cast<cudaStream_t>(stream));
 }
+
+namespace dg {
+int debug_word_gemm_bf16(uint32_t* out, bool clear) { return debug_word_local(out, clear); }
+}  // namespace dg

@@ -134,10 +134,14 @@ __device__ __forceinline__ void load_group(const Walk<L>& w, const GemmArgs& a, 
             const int64_t r = static_cast<int64_t>(w.ti.row0) + j * 32 + lane;
             const bool in = kin && r < a.M;  // Masked: a.M = cap; Contiguous: rows
             const int64_t m = L == Layout::Masked ? static_cast<int64_t>(w.ti.e) * a.M + r : r;
-            ba[j][u] = in ? __ldg(sfa + kbase + m) : static_cast<uint8_t>(127);
+            ba[j][u] = in && DG_CHECKED(sfa_in<L>(a, w.kb0 + u, m), DG_DEBUG_A_SCALE) ? __ldg(sfa + kbase + m)
+                                                                                      : static_cast<uint8_t>(127);
         }
 #pragma unroll
-        for (int n = 0; n < NB128; ++n) bb[n][u] = kin ? __ldg(sfb + n * a.KB + w.kb0 + u) : static_cast<uint8_t>(127);
+        for (int n = 0; n < NB128; ++n)
+            bb[n][u] = kin && DG_CHECKED(sfb_in(a, w.ti.e, w.ti.nb * NB128 + n, w.kb0 + u), DG_DEBUG_B_SCALE)
+                           ? __ldg(sfb + n * a.KB + w.kb0 + u)
+                           : static_cast<uint8_t>(127);
     }
 }
 
@@ -391,8 +395,8 @@ __global__ void __launch_bounds__(NT, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[tb]);  // the accumulator is in registers
-            if (!row_ok) continue;
             const int64_t c0 = static_cast<int64_t>(ti.nb) * BN + h * CPT;
+            if (!row_ok || !DG_CHECKED(out_in<L>(a, grow, c0, CPT), DG_DEBUG_OUT)) continue;
             uint8_t* dst = static_cast<uint8_t*>(a.d) + (grow * a.ldd + c0) * ESIZE;
             if constexpr (OUT_FP32) {
                 const float* crow = a.c != nullptr ? a.c + grow * a.ldd + c0 : nullptr;
@@ -463,4 +467,8 @@ int launch_mgrouped_mx(Layout L, bool out_fp32, bool b_fp4, const CUtensorMap& t
     return mx::launch_l<Layout::Contiguous>(out_fp32, b_fp4, tA, tB, args, stream);
 }
 
+}  // namespace dg
+
+namespace dg {
+int debug_word_gemm_mx(uint32_t* out, bool clear) { return debug_word_local(out, clear); }
 }  // namespace dg

@@ -61,6 +61,36 @@ uint64_t wait_limit_ns() {
     return o != 0 ? o : drain_limit_ns();
 }
 
+namespace {
+std::mutex g_log_mu;
+std::string g_log_path;
+std::atomic<bool> g_log_on{false};
+uint64_t g_log_seq = 0;
+
+// the environment's log file, read once when the library is loaded
+[[maybe_unused]] const bool g_log_env = [] {
+    const char* p = std::getenv("DG_ARG_LOG");
+    if (p != nullptr && *p != '\0') {
+        g_log_path = p;
+        g_log_on.store(true);
+    }
+    return true;
+}();
+}  // namespace
+
+bool arg_log_on() { return g_log_on.load(std::memory_order_relaxed); }
+
+// One line per call: a sequence number, the entry point, then name=value for every argument.  It
+// reads nothing from the device, so it is safe in stream capture and before any check.
+void arg_log_write(const char* fn, const std::string& body) {
+    std::lock_guard<std::mutex> lk(g_log_mu);
+    if (g_log_path.empty()) return;
+    FILE* f = std::fopen(g_log_path.c_str(), "a");
+    if (f == nullptr) return;
+    std::fprintf(f, "%llu %s %s\n", static_cast<unsigned long long>(g_log_seq++), fn, body.c_str());
+    std::fclose(f);
+}
+
 int encode_tmap(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                 CUtensorMapSwizzle swizzle) {
@@ -87,7 +117,33 @@ int encode_tmap(CUtensorMap* tm, CUtensorMapDataType dtype, uint32_t rank, const
 
 extern "C" const char* dg_last_error(void) { return dg::last_error(); }
 
+extern "C" int dg_debug_build(void) {
+#if DG_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+extern "C" int dg_debug_word(uint32_t* out, int clear) {
+    DG_CHECK_ARG(out != nullptr, "out must not be NULL");
+    *out = 0;
+    DG_CHECK_CUDA(cudaDeviceSynchronize());
+    for (auto fn : {dg::debug_word_quant, dg::debug_word_gemm, dg::debug_word_gemm_mx, dg::debug_word_gemm_bf16,
+                    dg::debug_word_kgrouped})
+        if (int rc = fn(out, clear != 0)) return dg::set_error(rc, "reading a debug word failed");
+    return DG_OK;
+}
+
+extern "C" int dg_set_arg_log(const char* path) {
+    std::lock_guard<std::mutex> lk(dg::g_log_mu);
+    dg::g_log_path = path != nullptr ? path : "";
+    dg::g_log_on.store(!dg::g_log_path.empty(), std::memory_order_relaxed);
+    return DG_OK;
+}
+
 extern "C" size_t dg_workspace_size(int op, int G, int64_t M, int64_t N, int64_t K) {
+    DG_ARG_LOG(op, G, M, N, K);
     (void)M;
     (void)N;
     (void)K;

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <string>
+#include <type_traits>
 #include <utility>
 
 #include "dg.h"
@@ -38,6 +39,47 @@ void clear_error();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---- argument log: when a log file is set (env DG_ARG_LOG, or dg_set_arg_log), every entry point
+// appends one line with its name and arguments before it checks them.
+bool arg_log_on();
+void arg_log_write(const char* fn, const std::string& body);
+
+template <typename T>
+void arg_log_value(std::string& s, const T& v) {
+    char b[48];
+    if constexpr (std::is_pointer_v<T>)
+        snprintf(b, sizeof(b), "%p", static_cast<const void*>(v));
+    else if constexpr (std::is_floating_point_v<T>)
+        snprintf(b, sizeof(b), "%.9g", static_cast<double>(v));
+    else
+        snprintf(b, sizeof(b), "%lld", static_cast<long long>(v));
+    s += b;
+}
+
+// names: the comma-separated argument expressions as written at the call site
+template <typename... T>
+void arg_log(const char* fn, const char* names, const T&... v) {
+    std::string s;
+    const char* n = names;
+    auto one = [&](const auto& x) {
+        while (*n == ' ' || *n == ',') ++n;
+        const char* e = n;
+        while (*e != '\0' && *e != ',') ++e;
+        if (!s.empty()) s += ' ';
+        s.append(n, e);
+        s += '=';
+        arg_log_value(s, x);
+        n = e;
+    };
+    (one(v), ...);
+    arg_log_write(fn, s);
+}
+
+#define DG_ARG_LOG(...)                                                                       \
+    do {                                                                                      \
+        if (::dg::arg_log_on()) ::dg::arg_log(__func__, #__VA_ARGS__, __VA_ARGS__);           \
+    } while (0)
+
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count(int* out);
 
@@ -47,6 +89,14 @@ uint64_t wait_limit_ns();
 // Upper bound of the waits that drain a kernel's copies and MMAs on its way out (the default limit,
 // never shortened by the test hook).
 uint64_t drain_limit_ns();
+
+// The debug words of the kernels' translation units (each ORs its word into *out, then clears it
+// if `clear`); dg_debug_word() combines them.
+int debug_word_quant(uint32_t* out, bool clear);
+int debug_word_gemm(uint32_t* out, bool clear);
+int debug_word_gemm_mx(uint32_t* out, bool clear);
+int debug_word_gemm_bf16(uint32_t* out, bool clear);
+int debug_word_kgrouped(uint32_t* out, bool clear);
 
 // cuTensorMapEncodeTiled through cudaGetDriverEntryPointByVersion; returns DG_OK or an error
 // code with a message.

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 
+#include "debug.cuh"
 #include "ptx.cuh"
 
 namespace dg {

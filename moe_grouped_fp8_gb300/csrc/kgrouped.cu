@@ -268,8 +268,16 @@ __global__ void __launch_bounds__(NT, 1) k_kgrouped_gemm(const __grid_constant__
                     tma_load_2d(st, mA, &full[stage], kb * BK, ti.n0);
                     tma_load_2d(st + A_BYTES, mB, &full[stage], kb * BK, ti.h0);
                     mbar_arrive_expect_tx(&sfull[sslot], SCALE_TX);
-                    bulk_load(sc, a.sfa + kbg * a.N + ti.n0, BM * 4, &sfull[sslot]);
-                    bulk_load(sc + SFB_OFF, a.sfb + kbg * a.H + ti.h0, BN * 4, &sfull[sslot]);
+                    // a debug build copies from the buffer's start where a slice would leave it
+                    // (the slot still receives its bytes, so no wait is left open)
+                    const int64_t ia =
+                        DG_CHECKED(kbg >= 0 && kbg < a.K_cap / BK && ti.n0 >= 0 && ti.n0 + BM <= a.N, DG_DEBUG_A_SCALE)
+                            ? kbg * a.N + ti.n0 : 0;
+                    const int64_t ib =
+                        DG_CHECKED(kbg >= 0 && kbg < a.K_cap / BK && ti.h0 >= 0 && ti.h0 + BN <= a.H, DG_DEBUG_B_SCALE)
+                            ? kbg * a.H + ti.h0 : 0;
+                    bulk_load(sc, a.sfa + ia, BM * 4, &sfull[sslot]);
+                    bulk_load(sc + SFB_OFF, a.sfb + ib, BN * 4, &sfull[sslot]);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     if (++sslot == SSLOTS) { sslot = 0; sphase ^= 1u; }
@@ -711,6 +719,7 @@ extern "C" int dg_k_grouped_fp8_wgrad(const uint8_t* a_packed, const float* sfa,
                                       const float* sfb, const float* c, float* d, const int32_t* ks, int G,
                                       int64_t K_cap, int64_t N, int64_t H, void* workspace, size_t workspace_bytes,
                                       int32_t* status, void* stream) {
+    DG_ARG_LOG(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes, status, stream);
     return kg::launch(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, workspace, workspace_bytes, status,
                       static_cast<cudaStream_t>(stream), true);
 }
@@ -720,6 +729,8 @@ extern "C" int dg_k_grouped_fp8_wgrad_from_bf16(const void* grad_y, const void* 
                                                 uint8_t* b_packed, float* sfb, const float* c, float* d,
                                                 float sf_zero, void* workspace, size_t workspace_bytes,
                                                 int32_t* status, void* stream) {
+    DG_ARG_LOG(grad_y, act, ks, G, K_cap, N, H, a_packed, sfa, b_packed, sfb, c, d, sf_zero, workspace,
+               workspace_bytes, status, stream);
     return kg::launch_from_bf16(grad_y, act, ks, 0, G, K_cap, N, H, a_packed, sfa, b_packed, sfb, c, d, sf_zero,
                                 workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream));
 }
@@ -729,6 +740,8 @@ extern "C" int dg_k_grouped_fp8_wgrad_from_bf16_psum(const void* grad_y, const v
                                                      float* sfa, uint8_t* b_packed, float* sfb, const float* c,
                                                      float* d, float sf_zero, void* workspace,
                                                      size_t workspace_bytes, int32_t* status, void* stream) {
+    DG_ARG_LOG(grad_y, act, psum, G, K_cap, N, H, a_packed, sfa, b_packed, sfb, c, d, sf_zero, workspace,
+               workspace_bytes, status, stream);
     return kg::launch_from_bf16(grad_y, act, psum, 1, G, K_cap, N, H, a_packed, sfa, b_packed, sfb, c, d, sf_zero,
                                 workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream));
 }
@@ -737,6 +750,7 @@ extern "C" int dg_k_grouped_fp8_wgrad_psum(const uint8_t* a_packed, const float*
                                            const float* sfb, const float* c, float* d, const int32_t* psum, int G,
                                            int64_t K_cap, int64_t N, int64_t H, void* workspace,
                                            size_t workspace_bytes, int32_t* status, void* stream) {
+    DG_ARG_LOG(a_packed, sfa, b_packed, sfb, c, d, psum, G, K_cap, N, H, workspace, workspace_bytes, status, stream);
     return kg::launch(a_packed, sfa, b_packed, sfb, c, d, psum, G, K_cap, N, H, workspace, workspace_bytes, status,
                       static_cast<cudaStream_t>(stream), true, 1);
 }
@@ -812,6 +826,7 @@ int noalloc_scratch(void** out) {
 extern "C" int dg_k_grouped_fp8_wgrad_noalloc(const uint8_t* a_packed, const float* sfa, const uint8_t* b_packed,
                                               const float* sfb, const float* c, float* d, const int32_t* ks, int G,
                                               int64_t K_cap, int64_t N, int64_t H, int32_t* status, void* stream) {
+    DG_ARG_LOG(a_packed, sfa, b_packed, sfb, c, d, ks, G, K_cap, N, H, status, stream);
     DG_CHECK_SUPPORTED(G <= DG_NOALLOC_MAX_GROUPS,
                        "dg_k_grouped_fp8_wgrad_noalloc handles at most %d experts (its built-in scratch holds %d "
                        "descriptors); G=%d needs dg_k_grouped_fp8_wgrad with a workspace",
@@ -861,3 +876,7 @@ extern "C" int dg_testing_kgrouped_host_maps(const uint8_t* a_packed, const uint
     }
     return DG_OK;
 }
+
+namespace dg {
+int debug_word_kgrouped(uint32_t* out, bool clear) { return debug_word_local(out, clear); }
+}  // namespace dg

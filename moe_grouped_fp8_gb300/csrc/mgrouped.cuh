@@ -40,7 +40,35 @@ struct GemmArgs {
     int psum;        // Contiguous: routing holds per-expert end rows (prefix sums), not m_indices
     int dense;       // no routing tensor: Masked counts all equal cap; Contiguous (psum) one expert ending at M
     const float* c;  // fp32 accumulator added to the result (fp32 output only), row stride ldd; may alias d
+#if DG_DEBUG
+    int64_t dbg_rows;  // output rows the store checks allow if below the layout's (test hook); 0 = all
+#endif
 };
+
+#if DG_DEBUG
+// ---- debug-build index predicates (used through DG_CHECKED) against the extents the layouts
+// give each buffer.  Rows of A, of the output and of the sfa columns in use: Masked G x cap,
+// Contiguous M.
+template <Layout L>
+__device__ __forceinline__ int64_t layout_rows(const GemmArgs& a) {
+    return L == Layout::Masked ? static_cast<int64_t>(a.G) * a.M : a.M;
+}
+// sfa [K/128][sfa_ld]: element (kb, m)
+template <Layout L>
+__device__ __forceinline__ bool sfa_in(const GemmArgs& a, int64_t kb, int64_t m) {
+    return kb >= 0 && kb < a.KB && m >= 0 && m < layout_rows<L>(a) && layout_rows<L>(a) <= a.sfa_ld;
+}
+// sfb [G][N/128][K/128]: element (e, n-block, kb)
+__device__ __forceinline__ bool sfb_in(const GemmArgs& a, int64_t e, int64_t nblk, int64_t kb) {
+    return e >= 0 && e < a.G && nblk >= 0 && nblk < a.n128 && kb >= 0 && kb < a.KB;
+}
+// output (and C) row `row`, columns [c0, c0 + n) of a [rows][ldd] buffer with N columns in use
+template <Layout L>
+__device__ __forceinline__ bool out_in(const GemmArgs& a, int64_t row, int64_t c0, int n) {
+    const int64_t rows = a.dbg_rows > 0 && a.dbg_rows < layout_rows<L>(a) ? a.dbg_rows : layout_rows<L>(a);
+    return row >= 0 && row < rows && c0 >= 0 && c0 + n <= a.N && a.N <= a.ldd;
+}
+#endif
 
 // Shared-memory bytes of the run table used by build_runs / tile_prefix: int32 prefix and x,
 // int16 first / L / e (m-blocks < DG_MAX_M_BLOCKS, experts < DG_MAX_GROUPS).

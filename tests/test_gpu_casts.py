@@ -304,3 +304,58 @@ def test_per_channel_pair_equals_two_single_calls(ks, Ca, Cb):
     oq, osf = oracle.quant_per_channel_128(xb[:T], 1e-4)
     np.testing.assert_array_equal(qb2.cpu().numpy()[:T * Cb], oracle.pack_kmajor(oq, ks))
     np.testing.assert_array_equal(sb2.cpu().numpy()[:T // 128].view(np.uint32), osf.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [DG_SF_FP32, DG_SF_UE8M0])
+@pytest.mark.parametrize("counts,cap,K", [([3, 40, 0, 17, 40], 40, 384), ([0, 0, 0], 16, 256),
+                                          ([300, -2, 1, 129, 0, 257], 257, 7168), ([1] * 40, 8, 128)])
+def test_per_token_packed_equals_masked_cast(fmt, counts, cap, K):
+    """The cast from packed rows writes the same codes and scales, at the same masked positions,
+    as the masked cast of the same rows scattered into [G, cap, K] (itself pinned to the oracle
+    above); rows past the counts stay untouched, and rows of x past the packed ones are not read."""
+    G = len(counts)
+    M = G * cap
+    v = np.clip(counts, 0, cap)
+    x = wl.randn_bf16((M, K), 91, 0.5)
+    x[torch.from_numpy(np.arange(cap)[None, :].repeat(G, 0).ravel() >= np.repeat(v, cap))] = float("nan")
+    rows = np.concatenate([np.arange(g * cap, g * cap + v[g]) for g in range(G)]).astype(np.int64)
+    packed = torch.full((M, K), float("nan"), dtype=torch.bfloat16)  # NaN rows past the packed ones
+    packed[: len(rows)] = x[torch.from_numpy(rows)]
+    cnt = torch.tensor(np.asarray(counts, np.int32), device="cuda")
+    outs = []
+    for packed_in in (False, True):
+        q = torch.full((M, K), 0xA5, dtype=torch.uint8, device="cuda")
+        sfa = api.empty_sfa(M, K, fmt, "cuda")
+        sfa.view(torch.uint8).fill_(0x5A)
+        if packed_in:
+            api.dg_quant_per_token_1x128_packed(packed.cuda(), q, sfa, cnt, fmt)
+        else:
+            api.dg_quant_per_token_1x128(x.cuda(), q, sfa, fmt, row_counts=cnt)
+        sync()
+        outs.append((q.cpu().numpy(), sfa.view(torch.uint8).cpu().numpy()))
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+    if len(rows):
+        oq, osf, _ = oracle.quant_per_token_1x128(x[torch.from_numpy(rows)], ue8m0=fmt == DG_SF_UE8M0)
+        np.testing.assert_array_equal(outs[1][0][rows], oq)
+
+
+@pytest.mark.parametrize("counts,cap,width,dtype", [([5, 0, 130, 64], 130, 6144, torch.bfloat16),
+                                                    ([0, 0], 4, 256, torch.float32),
+                                                    ([3, -1, 9, 2000], 16, 8, torch.bfloat16),
+                                                    ([191] * 32, 256, 6144, torch.bfloat16)])
+def test_pack_masked_rows(counts, cap, width, dtype):
+    """Each group's first clamp(count, 0, cap) rows land packed, group after group, byte for byte;
+    dst past them is untouched."""
+    G = len(counts)
+    v = np.clip(counts, 0, cap)
+    src = wl.randn_bf16((G, cap, width), 92, 1.0).to(dtype)
+    dst = torch.full((G * cap, width), -1, dtype=torch.int16 if dtype == torch.bfloat16 else torch.int32,
+                     device="cuda").view(dtype)
+    api.dg_pack_masked_rows(src.cuda(), torch.tensor(np.asarray(counts, np.int32), device="cuda"), dst)
+    sync()
+    got = dst.cpu().contiguous().view(torch.uint8).numpy().reshape(G * cap, -1)
+    want = torch.cat([src[g, : v[g]] for g in range(G)]).contiguous().view(torch.uint8).numpy().reshape(-1, got.shape[1])
+    n = int(v.sum())
+    np.testing.assert_array_equal(got[:n], want)
+    assert np.all(got[n:] == 0xFF)

@@ -308,6 +308,72 @@ def test_graph_replay_with_changed_counts():
                          f"replay {it} expert {e}")
 
 
+def test_graph_replay_packed_rows_in_and_out():
+    """The packed movement around the masked call, captured once: packed cast -> GEMM -> packing of
+    the output's valid rows, replayed 12 times with re-drawn counts (each replay's packed rows
+    re-written in place).  The packed output equals the masked output's valid rows bitwise, and
+    sampled rows match the oracle."""
+    G, cap, N, K = 9, 256, 256, 512
+    src = wl.randn_bf16((G * cap, K), 84, 1.0)
+    b = wl.randn_bf16((G, N, K), 85, 0.02, device="cuda")
+    x_pk = torch.empty(G * cap, K, dtype=torch.bfloat16, device="cuda")
+    qa = torch.empty(G * cap, K, dtype=torch.uint8, device="cuda")
+    sfa = api.empty_sfa(G * cap, K, DG_SF_FP32, "cuda")
+    qb, sfb = gpu_quant_blocks(b, DG_SF_FP32)
+    cnt = torch.full((G,), 100, dtype=torch.int32, device="cuda")
+    d = sentinel_like((G, cap, N), torch.bfloat16)
+    d_pk = sentinel_like((G * cap, N), torch.bfloat16)
+
+    def step():
+        api.dg_quant_per_token_1x128_packed(x_pk, qa, sfa, cnt, DG_SF_FP32)
+        api.dg_m_grouped_fp8_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, 100, DG_SF_FP32)
+        api.dg_pack_masked_rows(d, cnt, d_pk)
+
+    step()
+    sync()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    sync()
+    oqb, osfb, _ = oracle.quant_block_128x128(b.cpu())
+    rng = np.random.default_rng(86)
+    for it in range(12):
+        counts = rng.integers(0, cap + 1, G).astype(np.int32)
+        if it == 3:
+            counts[:] = 0
+        if it == 7:
+            counts[::2] = cap + 9
+        v = np.clip(counts, 0, cap)
+        n = int(v.sum())
+        rows = torch.from_numpy(rng.permutation(G * cap)[:n])  # any rows serve as this step's tokens
+        x_pk[:n].copy_(src[rows].cuda())
+        cnt.copy_(torch.from_numpy(counts))
+        d.view(torch.int16).fill_(-1)
+        d_pk.view(torch.int16).fill_(-1)
+        g.replay()
+        sync()
+        valid = np.arange(cap)[None, :] < v[:, None]
+        dm = out_bits(d)
+        assert np.all(dm[~valid] == sentinel_value(torch.bfloat16)), f"replay {it}: padding row written"
+        pk = out_bits(d_pk)
+        np.testing.assert_array_equal(pk[:n], dm[valid])
+        assert np.all(pk[n:] == sentinel_value(torch.bfloat16))
+        off = np.concatenate([[0], np.cumsum(v)])
+        for e in rng.choice(G, 2, replace=False):
+            if v[e] == 0:
+                continue
+            r = np.unique(rng.integers(0, v[e], 3))
+            xr = src[rows[torch.from_numpy(off[e] + r)]]
+            oqa, osfa, _ = oracle.quant_per_token_1x128(xr)
+            ref = oracle.gemm_masked(oqa[None], osfa[None], oqb[int(e):int(e) + 1], osfb[int(e):int(e) + 1], [len(r)])
+            assert_close(to_f64(d[int(e), torch.from_numpy(r).cuda()]), ref_out(ref[0], False), False,
+                         f"replay {it} expert {e}")
+
+
 @pytest.mark.slow
 def test_determinism_10000_calls():
     """The pages' reproduction shape (G=8, cap=32, N=K=256, its counts): 10,000 calls, each
