@@ -24,6 +24,9 @@
  *     bits into it when they meet bad device-side data (an m_indices value outside [-1, G),
  *     count > cap, K_e not a multiple of 128, ks overflowing K_cap, a wait that timed out);
  *     the offending work is skipped.  Kernels never trap.  The caller clears it.
+ *   - Every wait inside a kernel is bounded: after DG_WAIT_LIMIT_MS milliseconds (environment,
+ *     read once per process; default 2000) the kernel sets DG_STATUS_TIMEOUT, drains the copies
+ *     and MMAs it issued, frees its tensor memory and returns.
  *   - Alignment: buffers read or written by TMA (fp8 operands, outputs, C) must be 16-byte
  *     aligned; N, K (and H) must be multiples of 128.
  *   - e4m3 = OCP FP8 E4M3FN (max 448).  bf16 buffers are passed as `const void*`.
@@ -408,7 +411,9 @@ int dg_k_grouped_fp8_wgrad_noalloc(const uint8_t* a_packed, const float* sfa, co
  * Debug build.  Built with -DDG_DEBUG=1 (libdg_debug.so), every kernel checks each index it
  * computes for a scale read, an owner-thread store, a C read or a cast's element access against
  * the extent the layouts above give that buffer; an index outside it ORs a DG_DEBUG_* bit into
- * the library's debug word and the access is skipped.  In the release build nothing is checked.
+ * the library's debug word and the access is skipped.  Its kernels' bounded waits give up after
+ * 250 ms instead of 2000 ms (DG_WAIT_LIMIT_MS overrides both).  In the release build nothing is
+ * checked.
  *   dg_debug_build(): 1 for the debug build, 0 for the release build.
  *   dg_debug_word(out, clear): waits for the current device (cudaDeviceSynchronize), then
  *   stores in *out (a HOST pointer) the OR of the bits raised on it since the last clear, and

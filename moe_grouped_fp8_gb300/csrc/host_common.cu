@@ -44,9 +44,14 @@ int device_sm_count(int* out) {
 
 uint64_t drain_limit_ns() {
     static uint64_t v = [] {
+#if DG_DEBUG
+        constexpr long long kDefaultMs = 250;  // the debug build gives up sooner
+#else
+        constexpr long long kDefaultMs = 2000;
+#endif
         const char* s = std::getenv("DG_WAIT_LIMIT_MS");
-        long long ms = s ? std::atoll(s) : 2000;
-        if (ms <= 0) ms = 2000;
+        long long ms = s ? std::atoll(s) : kDefaultMs;
+        if (ms <= 0) ms = kDefaultMs;
         return static_cast<uint64_t>(ms) * 1000000ull;
     }();
     return v;

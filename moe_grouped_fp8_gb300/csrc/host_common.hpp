@@ -83,8 +83,8 @@ void arg_log(const char* fn, const char* names, const T&... v) {
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count(int* out);
 
-// Upper bound, in nanoseconds, of the kernels' work waits (env DG_WAIT_LIMIT_MS, default 2000 ms;
-// a test hook may shorten it).
+// Upper bound, in nanoseconds, of the kernels' work waits (env DG_WAIT_LIMIT_MS, default 2000 ms,
+// 250 ms in the debug build; a test hook may shorten it).
 uint64_t wait_limit_ns();
 // Upper bound of the waits that drain a kernel's copies and MMAs on its way out (the default limit,
 // never shortened by the test hook).
