@@ -359,3 +359,39 @@ def test_pack_masked_rows(counts, cap, width, dtype):
     n = int(v.sum())
     np.testing.assert_array_equal(got[:n], want)
     assert np.all(got[n:] == 0xFF)
+
+
+@pytest.mark.slow
+def test_packed_cast_and_row_packing_at_decode_size():
+    """At the decode size (G=32, cap=4096, K=7168, N=6144, Poisson(192) counts): the packed cast
+    equals the masked cast of the same rows bitwise, and the row packing of a [32, 4096, 6144] bf16
+    buffer equals the valid rows gathered by index."""
+    w = wl.masked_decode()
+    G, cap, K, N = w.G, w.cap, w.K, w.N
+    counts = np.asarray(w.counts, np.int32)
+    v = np.clip(counts, 0, cap)
+    rows = torch.from_numpy(np.concatenate([np.arange(g * cap, g * cap + v[g]) for g in range(G)])).cuda()
+    x = wl.randn_bf16((G * cap, K), 93, 1.0, "cuda")
+    packed = torch.empty_like(x)
+    packed[: rows.numel()] = x[rows]
+    cnt = torch.tensor(counts, device="cuda")
+    outs = []
+    for packed_in in (False, True):
+        q = torch.zeros(G * cap, K, dtype=torch.uint8, device="cuda")
+        sfa = api.empty_sfa(G * cap, K, DG_SF_FP32, "cuda")
+        sfa.zero_()
+        if packed_in:
+            api.dg_quant_per_token_1x128_packed(packed, q, sfa, cnt, DG_SF_FP32)
+        else:
+            api.dg_quant_per_token_1x128(x, q, sfa, DG_SF_FP32, row_counts=cnt)
+        outs.append((q, sfa))
+    sync()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    del x, packed, outs
+    d = wl.randn_bf16((G, cap, N), 94, 1.0, "cuda")
+    dst = torch.full((G * cap, N), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    api.dg_pack_masked_rows(d, cnt, dst)
+    sync()
+    n = rows.numel()
+    assert torch.equal(dst[:n].view(torch.int16), d.view(G * cap, N)[rows].view(torch.int16))
+    assert bool((dst[n:].view(torch.int16) == -1).all())
