@@ -640,6 +640,11 @@ class MGroupedWorkload:
         ev1.record(stream)
         ev1.synchronize()
         ms = ev0.elapsed_time(ev1) / steps
+        # the loop computes what the device-resident steps computed: its last output, as the host
+        # received it, equals their D rows bit for bit
+        want = d_flat[idx].cpu()
+        if not torch.equal(d_h[(steps - 1) % NBUF].view(torch.int16), want.view(torch.int16)):
+            raise RuntimeError("the end-to-end loop's output differs from the device-resident step's output")
         h2d = rows * w.K * 2 + route_h.numel() * 4
         d2h = rows * w.N * 2
         return ms, h2d, d2h
