@@ -16,7 +16,7 @@
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless stated.  The
  *     library allocates nothing, never copies device data to the host and never
  *     synchronises: each call only enqueues kernels on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream).  Calls are therefore capturable into CUDA graphs, and a
+ *     legacy default stream).  The one exception is the debug aid dg_debug_word (end of file).  Calls are therefore capturable into CUDA graphs, and a
  *     captured call re-reads m_indices / counts / ks from device memory on every replay.
  *   - Return value: DG_OK, or an error code with nothing enqueued.  dg_last_error() gives a
  *     message for the calling thread's most recent failure.
