@@ -255,7 +255,8 @@ int dg_fp8_gemm_nt_batched(const uint8_t* a, const void* sfa, const uint8_t* b, 
  *   a: bf16 [G, cap, K].  b: bf16 [G, N, K].  d: [G, cap, N] bf16 or fp32 (out_dtype).
  *   counts: int32 [G] device (clamped to [0, cap]; out-of-range counts set
  *   DG_STATUS_COUNT_GT_CAP).  N % 128 == 0, K % 64 == 0; a, b, d 16-byte aligned.
- *   expected_m: a hint only; it never changes the result.
+ *   expected_m: a hint only (with the capacity it picks the tile width); it never changes the
+ *   result.
  */
 int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, int out_dtype, const int32_t* counts,
                              int G, int64_t cap, int64_t N, int64_t K, int expected_m, int32_t* status,

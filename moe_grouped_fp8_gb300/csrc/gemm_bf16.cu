@@ -5,16 +5,20 @@
 //
 // D[rows of expert e, :] = A[rows, :] . B_e^T with bf16 operands and fp32 accumulation over the
 // whole K in tensor memory - no scales, no promotion.  Per tile the MMA thread issues
-// tcgen05.mma.kind::f16 (M = 128, N = 128, K = 16, both operands bf16) for every 64-element K
+// tcgen05.mma.kind::f16 (M = 128, N = BN, K = 16, both operands bf16) for every 64-element K
 // stage into one of two TMEM tile buffers and commits once; the eight epilogue warps read the
 // finished tile, round it to bf16 (or keep fp32) and store it while the tensor core fills the
-// other buffer.  A 64-element bf16 stage row is 128 bytes, so the 128-byte-swizzled stage tiles
+// other buffer.  Tiles are 128 x 256 (bf16 output, N % 256 == 0: three 48 KB ring stages) or
+// 128 x 128 (five 32 KB stages for bf16, four for fp32 output); the wider tile moves 25% fewer
+// operand bytes from L2 into shared memory per MMA.  A 64-element bf16 stage row is 128 bytes, so the 128-byte-swizzled stage tiles
 // and the 32-byte K advance per MMA are those of the FP8 kernels.
 //
 // Schedule (rebuilt on device from counts / m_indices at every launch), row validity and the
 // row-exact store (3-D [G, cap, N] TMA boxes of 128 or 8 rows, owner-thread tails) follow the FP8
 // kernel of gemm.cu: rows that are not valid are never written.
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "host_common.hpp"
 #include "kernel_common.cuh"
@@ -29,18 +33,17 @@ constexpr int H_PRODUCER_WARP = 8;
 constexpr int H_MMA_WARP = 9;
 constexpr int H_THREADS = 320;
 constexpr int H_EPI_BAR = 1;
-constexpr int H_BN = 128;
 constexpr int H_BK = 64;     // bf16 elements of K per stage (128-byte rows)
-constexpr int H_TBUFS = 2;   // TMEM tile buffers (128 fp32 columns each)
+constexpr int H_TBUFS = 2;   // TMEM tile buffers (BN fp32 columns each)
 
-template <int STAGES, bool OUT_FP32>
+template <int BN, int STAGES, bool OUT_FP32>
 struct HPlan {
     static constexpr int A_BYTES = BM * H_BK * 2;
-    static constexpr int B_BYTES = H_BN * H_BK * 2;
+    static constexpr int B_BYTES = BN * H_BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int ESIZE = OUT_FP32 ? 4 : 2;
-    static constexpr int CPT = H_BN / 2;               // output columns per epilogue thread
-    static constexpr int CHUNKS = H_BN * ESIZE / 128;  // 128-byte column chunks of a tile row
+    static constexpr int CPT = BN / 2;               // output columns per epilogue thread
+    static constexpr int CHUNKS = BN * ESIZE / 128;  // 128-byte column chunks of a tile row
     static constexpr int CHUNK_BYTES = BM * 128;
     static constexpr int STG_BYTES = CHUNKS * CHUNK_BYTES;
     static constexpr int RING_OFF = 0;
@@ -51,14 +54,15 @@ struct HPlan {
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int MISC_BYTES = 256;
     static constexpr int TOTAL = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
-    static constexpr uint32_t TMEM_COLS = H_TBUFS * H_BN;
+    static constexpr uint32_t TMEM_COLS = H_TBUFS * BN;
     static_assert(H_BK * 2 == 128, "a stage row is one 128-byte swizzle row");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms");
     static_assert(STG_OFF % 1024 == 0 && SCHED_OFF % 1024 == 0, "TMA / swizzle buffers are 1024-byte aligned");
     static_assert(BAR_OFF % 8 == 0 && MISC_OFF % 8 == 0, "mbarrier objects are 8-byte aligned");
     static_assert(STG_BYTES >= 2 * DG_MAX_M_BLOCKS, "run scratch fits in the staging buffer");
-    static_assert(TMEM_COLS == 256, "TMEM allocation");
-    static_assert(CPT == 64, "two 32-column TMEM loads per epilogue thread");
+    static_assert(BN == 128 || (BN == 256 && !OUT_FP32), "256-column tiles stage bf16 output only");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation");
+    static_assert(CPT % 32 == 0, "32-column TMEM loads per epilogue thread");
     static_assert(TOTAL <= 232448, "shared memory");
 };
 
@@ -90,12 +94,12 @@ __device__ __forceinline__ HTile decode_h(int t, const RunTable& rt, int R, cons
     return ti;
 }
 
-template <Layout L, int STAGES, bool OUT_FP32>
+template <Layout L, int BN, int STAGES, bool OUT_FP32>
 __global__ void __launch_bounds__(H_THREADS, 1)
     k_grouped_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD8,
                         const GemmArgs a) {
-    using P = HPlan<STAGES, OUT_FP32>;
+    using P = HPlan<BN, STAGES, OUT_FP32>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                         tma_load_3d(sa, &tmA, &full[stage], kb * H_BK, ti.row0, ti.e);
                     else
                         tma_load_2d(sa, &tmA, &full[stage], kb * H_BK, ti.row0);
-                    tma_load_3d(sb, &tmB, &full[stage], kb * H_BK, ti.nb * H_BN, ti.e);
+                    tma_load_3d(sb, &tmB, &full[stage], kb * H_BK, ti.nb * BN, ti.e);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -187,10 +191,10 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             int stage = 0, tb = 0;
             uint32_t phase = 0, tphase = 0;
             bool ok = true, any = false;
-            constexpr uint32_t IDESC = idesc_bf16_f32(BM, H_BN);
+            constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 if (!mbar_wait(&tempty[tb], tphase ^ 1u, wc)) { ok = false; break; }
-                const uint32_t dt = tmem_base + static_cast<uint32_t>(tb * H_BN);
+                const uint32_t dt = tmem_base + static_cast<uint32_t>(tb * BN);
                 for (int kb = 0; kb < a.KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
@@ -248,17 +252,18 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             float acc[P::CPT];
             if (!failed) {
                 tc_fence_after();
-                uint32_t v[2][32];
+                constexpr int LOADS = P::CPT / 32;
+                uint32_t v[LOADS][32];
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2)
-                    tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * H_BN + h2 * P::CPT + c2 * 32), v[c2]);
+                for (int c2 = 0; c2 < LOADS; ++c2)
+                    tmem_ld_x32(tmem_base + t_lane + static_cast<uint32_t>(tb * BN + h2 * P::CPT + c2 * 32), v[c2]);
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) tmem_wait_ld(v[c2]);
+                for (int c2 = 0; c2 < LOADS; ++c2) tmem_wait_ld(v[c2]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[tb]);  // the accumulator is in registers
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2)
+                for (int c2 = 0; c2 < LOADS; ++c2)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) acc[c2 * 32 + i] = __uint_as_float(v[c2][i]);
             }
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(H_THREADS, 1)
             if (tid == 0 && v8 > 0) {
                 for (int c = 0; c < P::CHUNKS; ++c) {
                     const uint8_t* src = stg + c * P::CHUNK_BYTES;
-                    const int x = ti.nb * H_BN + c * (128 / P::ESIZE);
+                    const int x = ti.nb * BN + c * (128 / P::ESIZE);
                     if (v8 == BM) {
                         if constexpr (L == Layout::Contiguous) tma_store_2d(&tmD, src, x, ti.row0);
                         else tma_store_3d(&tmD, src, x, ti.row0, ti.e);
@@ -325,10 +330,10 @@ __global__ void __launch_bounds__(H_THREADS, 1)
                 have_store = true;
             }
             if (row_ok && row >= v8 &&
-                DG_CHECKED(out_in<L>(a, grow, static_cast<int64_t>(ti.nb) * H_BN + h2 * P::CPT, P::CPT),
+                DG_CHECKED(out_in<L>(a, grow, static_cast<int64_t>(ti.nb) * BN + h2 * P::CPT, P::CPT),
                            DG_DEBUG_OUT)) {
                 uint8_t* dst = static_cast<uint8_t*>(a.d) +
-                               ((grow * a.ldd) + ti.nb * H_BN + h2 * P::CPT) * static_cast<int64_t>(P::ESIZE);
+                               ((grow * a.ldd) + ti.nb * BN + h2 * P::CPT) * static_cast<int64_t>(P::ESIZE);
                 constexpr int PIECES = P::CPT * P::ESIZE / 16;
 #pragma unroll
                 for (int p = 0; p < PIECES; ++p) {
@@ -361,23 +366,40 @@ __global__ void __launch_bounds__(H_THREADS, 1)
 
 // ------------------------------------------------------------------------- host side
 
-template <Layout L, int STAGES, bool OUT_FP32>
+template <Layout L, int BN, int STAGES, bool OUT_FP32>
 int launch_h(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
              const GemmArgs& args, cudaStream_t stream) {
-    using P = HPlan<STAGES, OUT_FP32>;
-    auto kern = k_grouped_gemm_bf16<L, STAGES, OUT_FP32>;
+    using P = HPlan<BN, STAGES, OUT_FP32>;
+    auto kern = k_grouped_gemm_bf16<L, BN, STAGES, OUT_FP32>;
     DG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::TOTAL));
     int sms = 0;
     if (int rc = device_sm_count(&sms)) return rc;
     return launch_pdl(kern, dim3(sms), dim3(H_THREADS), P::TOTAL, stream, tA, tB, tD, tD8, args);
 }
 
+// testing: the tile width of later calls (0 automatic, 128, or 256 where N and the output allow)
+std::atomic<int> g_force_bn_h{0};
+
+// 128 x 256 tiles for bf16 output with N % 256 == 0 when they still fill the GPU (at least one
+// 256-column tile per SM for the m-blocks the call is expected to have), else 128 x 128: the
+// reproduction's shape (8 experts of 32 rows, N = 256) has 8 wide tiles, 5.2 us with 16 narrow
+// ones against 6.1 us; decode and prefill take 11% and 21% less time with wide tiles.
+int tile_bn(int out, int64_t N, int64_t m_blocks) {
+    const int f = g_force_bn_h.load(std::memory_order_relaxed);
+    if (f == 128 || out != DG_OUT_BF16 || N % 256 != 0) return 128;
+    if (f == 256) return 256;
+    int sms = 0;
+    if (device_sm_count(&sms) != DG_OK) sms = 1;
+    return m_blocks * (N / 256) >= sms ? 256 : 128;
+}
+
 template <Layout L>
 int dispatch_h(int out, const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tD, const CUtensorMap& tD8,
                const GemmArgs& args, cudaStream_t s) {
     // bf16 output stages half as much as fp32, which leaves room for a fifth ring stage
-    if (out == DG_OUT_FP32) return launch_h<L, 4, true>(tA, tB, tD, tD8, args, s);
-    return launch_h<L, 5, false>(tA, tB, tD, tD8, args, s);
+    if (out == DG_OUT_FP32) return launch_h<L, 128, 4, true>(tA, tB, tD, tD8, args, s);
+    if (args.num_nb * 256 == args.N) return launch_h<L, 256, 3, false>(tA, tB, tD, tD8, args, s);
+    return launch_h<L, 128, 5, false>(tA, tB, tD, tD8, args, s);
 }
 
 CUtensorMapDataType out_type(int out) {
@@ -396,11 +418,11 @@ int check_common_h(const void* a, const void* b, void* d, int out, int G, int64_
 }
 
 int encode_b_and_d(const void* b, void* d, int out, int G, int64_t rows, int64_t G_out, int64_t N, int64_t K,
-                   bool masked, CUtensorMap* tB, CUtensorMap* tD, CUtensorMap* tD8) {
+                   bool masked, int bn, CUtensorMap* tB, CUtensorMap* tD, CUtensorMap* tD8) {
     {
         uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(G)};
         uint64_t str[2] = {static_cast<uint64_t>(K * 2), static_cast<uint64_t>(N * K * 2)};
-        uint32_t box[3] = {H_BK, H_BN, 1};
+        uint32_t box[3] = {H_BK, static_cast<uint32_t>(bn), 1};
         if (int rc = encode_tmap(tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, str, box,
                                  CU_TENSOR_MAP_SWIZZLE_128B))
             return rc;
@@ -431,7 +453,6 @@ extern "C" int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, i
                                         int G, int64_t cap, int64_t N, int64_t K, int expected_m, int32_t* status,
                                         void* stream) {
     DG_ARG_LOG(a, b, d, out_dtype, counts, G, cap, N, K, expected_m, status, stream);
-    (void)expected_m;
     DG_CHECK_ARG(cap >= 0, "cap must be >= 0");
     if (int rc = check_common_h(a, b, d, out_dtype, G, N, K)) return rc;
     DG_CHECK_ARG(counts != nullptr, "counts is null");
@@ -446,7 +467,9 @@ extern "C" int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, i
                                  CU_TENSOR_MAP_SWIZZLE_128B))
             return rc;
     }
-    if (int rc = encode_b_and_d(b, d, out_dtype, G, cap, G, N, K, true, &tB, &tD, &tD8)) return rc;
+    const int64_t rows_hint = expected_m > 0 && expected_m < cap ? expected_m : cap;
+    const int bn = tile_bn(out_dtype, N, static_cast<int64_t>(G) * ((rows_hint + BM - 1) / BM));
+    if (int rc = encode_b_and_d(b, d, out_dtype, G, cap, G, N, K, true, bn, &tB, &tD, &tD8)) return rc;
     GemmArgs args{};
     args.routing = counts;
     args.d = d;
@@ -459,7 +482,7 @@ extern "C" int dg_m_grouped_bf16_masked(const void* a, const void* b, void* d, i
     args.G = G;
     args.K = static_cast<int>(K);
     args.KB = static_cast<int>(K / H_BK);
-    args.num_nb = static_cast<int>(N / H_BN);
+    args.num_nb = static_cast<int>(N / bn);
     args.n128 = static_cast<int>(N / 128);
     return dispatch_h<Layout::Masked>(out_dtype, tA, tB, tD, tD8, args, static_cast<cudaStream_t>(stream));
 }
@@ -482,7 +505,8 @@ extern "C" int dg_m_grouped_bf16_contiguous(const void* a, const void* b, void* 
                                  CU_TENSOR_MAP_SWIZZLE_128B))
             return rc;
     }
-    if (int rc = encode_b_and_d(b, d, out_dtype, G, M, 1, N, K, false, &tB, &tD, &tD8)) return rc;
+    const int bn = tile_bn(out_dtype, N, (M + BM - 1) / BM);
+    if (int rc = encode_b_and_d(b, d, out_dtype, G, M, 1, N, K, false, bn, &tB, &tD, &tD8)) return rc;
     GemmArgs args{};
     args.routing = m_indices;
     args.d = d;
@@ -495,9 +519,17 @@ extern "C" int dg_m_grouped_bf16_contiguous(const void* a, const void* b, void* 
     args.G = G;
     args.K = static_cast<int>(K);
     args.KB = static_cast<int>(K / H_BK);
-    args.num_nb = static_cast<int>(N / H_BN);
+    args.num_nb = static_cast<int>(N / bn);
     args.n128 = static_cast<int>(N / 128);
     return dispatch_h<Layout::Contiguous>(out_dtype, tA, tB, tD, tD8, args, static_cast<cudaStream_t>(stream));
+}
+
+// Test hook: the BF16 GEMM's tile width for later calls (0 automatic, 128, or 256 where the output
+// is bf16 and N % 256 == 0).
+extern "C" int dg_testing_bf16_bn(int bn) {
+    DG_CHECK_ARG(bn == 0 || bn == 128 || bn == 256, "bn must be 0, 128 or 256");
+    dg::g_force_bn_h.store(bn, std::memory_order_relaxed);
+    return DG_OK;
 }
 
 namespace dg {

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from moe_grouped_fp8_gb300 import DG_STATUS_BAD_INDEX, DG_STATUS_COUNT_GT_CAP, api
+from moe_grouped_fp8_gb300 import DG_STATUS_BAD_INDEX, DG_STATUS_COUNT_GT_CAP, _lib, api
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import assert_close, out_bits, ref_out, sentinel_like, sentinel_value, sync, to_f64
@@ -134,6 +134,34 @@ def test_bf16_contiguous_bad_indices_flagged_and_skipped():
     assert_close(to_f64(d)[:10], ref_out(ref[:10], False), False, "rows of expert 0")
     bits = out_bits(d)
     assert np.all(bits[10:] == sentinel_value(torch.bfloat16))
+
+
+def set_bf16_bn(bn: int) -> None:
+    """Test hook: the BF16 GEMM's tile width for later calls (0 automatic, 128, 256)."""
+    _lib.check(_lib.load().dg_testing_bf16_bn(int(bn)))
+
+
+@pytest.mark.parametrize("layout", ["masked", "contiguous"])
+def test_bf16_tile_widths_bitwise_equal(layout):
+    """128 x 256 tiles (the automatic choice for bf16 output with N % 256 == 0 on calls with enough
+    tiles) and 128 x 128 tiles write the same bits: every output element sums the same K-ordered
+    products either way."""
+    outs = []
+    for bn in (256, 128):
+        set_bf16_bn(bn)
+        try:
+            if layout == "masked":
+                d, _, _, _ = masked_bf16_case(wl.randn_bf16((4, 200, 320), 61), wl.randn_bf16((4, 512, 320), 62, 0.05),
+                                              [200, 77, 0, 130])
+            else:
+                counts = [130, 0, 257, 5]
+                mi = wl.contiguous_m_indices(counts, m_max=wl.contiguous_capacity(sum(counts), len(counts)))
+                d, _ = contiguous_bf16_case(wl.randn_bf16((mi.size, 1024), 63, 1.0),
+                                            wl.randn_bf16((4, 256, 1024), 64, 0.05), mi)
+            outs.append(out_bits(d))
+        finally:
+            set_bf16_bn(0)
+    assert np.array_equal(outs[0], outs[1])
 
 
 @pytest.mark.slow

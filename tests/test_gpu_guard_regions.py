@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, api
+from moe_grouped_fp8_gb300 import DG_SF_FP32, DG_SF_UE8M0, _lib, api
 from moe_grouped_fp8_gb300 import workloads as wl
 
 from gpu_helpers import gpu_quant_blocks, gpu_quant_tokens, sync
@@ -150,9 +150,14 @@ def test_guards_contiguous_dense_batched_fp4_bf16():
     # BF16 masked and contiguous
     ab = wl.randn_bf16((3, 90, 512), 15, 1.0, "cuda")
     bb = wl.randn_bf16((3, 256, 512), 16, 1.0, "cuda")
-    d = Guarded((3, 90, 256), torch.bfloat16)
-    api.dg_m_grouped_bf16_masked(ab, bb, d.t, torch.tensor([90, 0, 33], dtype=torch.int32, device="cuda"))
-    d.check("BF16 masked GEMM")
+    for bn in (128, 256):
+        _lib.check(_lib.load().dg_testing_bf16_bn(bn))
+        try:
+            d = Guarded((3, 90, 256), torch.bfloat16)
+            api.dg_m_grouped_bf16_masked(ab, bb, d.t, torch.tensor([90, 0, 33], dtype=torch.int32, device="cuda"))
+            d.check(f"BF16 masked GEMM, {bn}-column tiles")
+        finally:
+            _lib.check(_lib.load().dg_testing_bf16_bn(0))
     ac = wl.randn_bf16((M, 512), 17, 1.0, "cuda")
     bc = wl.randn_bf16((4, 256, 512), 18, 1.0, "cuda")
     d = Guarded((M, 256), torch.bfloat16)
