@@ -29,8 +29,8 @@ namespace {
 // items a pass covers (no division in the loop).  Three launch shapes share the item code:
 //   rows:    one CTA per chunk of rows_per_cta rows of one row group; it returns at once when
 //            the chunk lies past the group's count (groups on the grid's x axis: the chunks that
-//            hold rows are dispatched first).  Used without row counts, and for more groups than
-//            the walk below keeps in shared memory;
+//            hold rows are dispatched first).  Used without row counts, for more groups than
+//            the walk below keeps in shared memory, and for small masked inputs;
 //   masked:  a grid of resident CTAs walks one index space of the valid rows only (the rows under
 //            each group's count, numbered group after group): every CTA forms the prefix of the
 //            clamped counts, then casts an equal share of the valid (row, 128-block) items, mapping
@@ -46,6 +46,10 @@ constexpr int TOKEN_MIN_ITEMS_PER_CTA = 128;
 constexpr int TOKEN_CTAS_PER_SM = 4;  // resident 256-thread CTAs at the kernels' register counts
 constexpr int TOKEN_PER_WARP = 2 * TOKEN_ITEMS_PER_HW;
 constexpr int TOKEN_WALK_MAX_GROUPS = 1024; // groups whose prefix the masked walk keeps
+// Below this many (row, block) items of capacity the per-group grid is faster: the pages'
+// reproduction shape (8 x 32 rows, K = 256) casts in 2.4 us on 8 CTAs against 4.4 us on the walk's
+// 4 CTAs, several passes each; from the 8-expert decode case up the two are equal or the walk wins.
+constexpr int64_t TOKEN_WALK_MIN_ITEMS = 65536;
 
 __device__ __forceinline__ uint4 token_load(const uint16_t* x, int64_t ldx, bool live, int64_t m, int kb, int sub) {
     return live ? __ldg(reinterpret_cast<const uint4*>(x + m * ldx + static_cast<int64_t>(kb) * 128) + sub)
@@ -466,9 +470,12 @@ extern "C" int dg_quant_per_token_1x128(const void* x, int64_t M, int64_t K, int
     }
     const int64_t groups = row_counts != nullptr ? G : 1;
     const bool ue = sf_format == DG_SF_UE8M0;
-    if (row_counts != nullptr && G <= TOKEN_WALK_MAX_GROUPS && M < (1ll << 31) && M * (K / 128) < (1ll << 40)) {
+    const bool hooked = g_token_items.load(std::memory_order_relaxed) > 0;
+    if (row_counts != nullptr && G <= TOKEN_WALK_MAX_GROUPS && M < (1ll << 31) && M * (K / 128) < (1ll << 40) &&
+        (M * (K / 128) >= TOKEN_WALK_MIN_ITEMS || hooked)) {
         // the walk over valid rows: two CTAs per resident slot share the valid items equally (or,
-        // through the test hook, a grid of about that many items per CTA over the capacity)
+        // through the test hook, a grid of about that many items per CTA over the capacity; the
+        // hook also keeps small inputs on the walk, so that tests reach it at every size)
         int sms = 0;
         if (int rc = device_sm_count(&sms)) return rc;
         int64_t grid = std::min<int64_t>(2ll * TOKEN_CTAS_PER_SM * sms,
