@@ -68,6 +68,7 @@ TESTING_SIGNATURES = {
     "dg_testing_mgrouped_bn": (I32, [I32]),
     "dg_testing_token_items_per_cta": (I32, [I32]),
     "dg_testing_debug_out_rows": (I32, [I64]),
+    "dg_testing_debug_stop_producer": (I32, [I32]),
     "dg_testing_bf16_bn": (I32, [I32]),
 }
 

@@ -206,6 +206,11 @@ __global__ void __launch_bounds__(num_threads<EW>(), 1)
                 const TileInfo ti = decode_tile<L>(t, rt, R, a);
                 for (int kb = 0; kb < ti.kbt; ++kb) {
                     if (!mbar_wait_inl(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+#if DG_DEBUG
+                    // debug build, test hook: the producer stops as if stalled, so the MMA issuers'
+                    // bounded waits for this stage run out and the CTA takes its abort path
+                    if (blockIdx.x == 0 && a.dbg_stop_at > 0 && issued + 1 == a.dbg_stop_at) { ok = false; break; }
+#endif
                     uint8_t* sa = ring + stage * P::STAGE_BYTES;
                     uint8_t* sb = sa + P::A_BYTES;
                     mbar_arrive_expect_tx(&full[stage], P::STAGE_BYTES);
@@ -522,6 +527,8 @@ constexpr int DIRECT_MAX_KB = 32;
 std::atomic<int> g_force_store{0};
 // testing (debug build): the output rows the index checks let the stores reach; 0 = the layout's
 std::atomic<int64_t> g_debug_out_rows{0};
+// testing (debug build): CTA 0's producer stops before its n-th stage load; 0 = never
+std::atomic<int> g_debug_stop_at{0};
 
 int store_mode(int KB) {
     switch (g_force_store.load(std::memory_order_relaxed)) {
@@ -740,6 +747,7 @@ int m_grouped_masked(const uint8_t* a, const void* sfa, const uint8_t* b, const 
     GemmArgs args{};
 #if DG_DEBUG
     args.dbg_rows = g_debug_out_rows.load(std::memory_order_relaxed);
+    args.dbg_stop_at = g_debug_stop_at.load(std::memory_order_relaxed);
 #endif
     args.routing = counts;
     args.dense = dense ? 1 : 0;
@@ -806,6 +814,7 @@ int m_grouped_contiguous(const uint8_t* a, const void* sfa, const uint8_t* b, co
     GemmArgs args{};
 #if DG_DEBUG
     args.dbg_rows = g_debug_out_rows.load(std::memory_order_relaxed);
+    args.dbg_stop_at = g_debug_stop_at.load(std::memory_order_relaxed);
 #endif
     args.routing = routing;
     args.psum = psum ? 1 : 0;
@@ -912,6 +921,16 @@ extern "C" int dg_m_grouped_fp8_fp4_masked(const uint8_t* a, const uint8_t* sfa,
 extern "C" int dg_testing_debug_out_rows(int64_t rows) {
     DG_CHECK_ARG(rows >= 0, "rows must be >= 0");
     dg::g_debug_out_rows.store(rows, std::memory_order_relaxed);
+    return DG_OK;
+}
+
+// Debug build: the first CTA's TMA producer of the m-grouped FP8 promotion kernel stops before its
+// n-th stage load (0 restores normal operation), as a stalled producer would: the waits for that
+// stage run out after the wait limit, the kernel sets DG_STATUS_TIMEOUT, drains what it issued and
+// returns.  No effect on the release build.
+extern "C" int dg_testing_debug_stop_producer(int n) {
+    DG_CHECK_ARG(n >= 0, "n must be >= 0");
+    dg::g_debug_stop_at.store(n, std::memory_order_relaxed);
     return DG_OK;
 }
 

@@ -42,6 +42,7 @@ struct GemmArgs {
     const float* c;  // fp32 accumulator added to the result (fp32 output only), row stride ldd; may alias d
 #if DG_DEBUG
     int64_t dbg_rows;  // output rows the store checks allow if below the layout's (test hook); 0 = all
+    int dbg_stop_at;   // test hook: CTA 0's producer stops before its n-th stage load (0 = never)
 #endif
 };
 

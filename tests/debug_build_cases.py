@@ -5,8 +5,9 @@ binding loads libdg_debug.so) with the release build bit for bit.
     python tests/debug_build_cases.py OUT.npz
 
 Saved: every case's output bytes; "word", the debug word after the in-bounds cases (the debug
-build must raise no bit on them); and, for the planted case (the test hook narrows the output
-rows the store checks allow to the first group's), "planted_out" and "planted_word".
+build must raise no bit on them); for the planted case (the test hook narrows the output rows
+the store checks allow to the first group's), "planted_out" and "planted_word"; and for the
+injected producer stall, "stall_status" and the output of the clean call after it.
 """
 from __future__ import annotations
 
@@ -176,6 +177,28 @@ def main(path):
     finally:
         _lib.check(lib.dg_testing_debug_out_rows(0))
     out["planted_word"] = np.array([api.dg_debug_word(clear=True)], np.uint32)
+
+    # ---- injected stall (debug build): CTA 0's producer stops before its 5th stage load; with a
+    # 50 ms wait limit the call returns with DG_STATUS_TIMEOUT set, and the next call (hook off,
+    # default limit) is clean
+    G, cap, N, K = 4, 200, 512, 7168
+    a = wl.randn_bf16((G * cap, K), 21, 1.0, dev)
+    b = wl.randn_bf16((G, N, K), 22, 1.0, dev)
+    qa, sfa = tokens(a, DG_SF_FP32)
+    qb, sfb = blocks(b, DG_SF_FP32)
+    cnt = torch.tensor([200, 77, 0, 130], dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _lib.check(lib.dg_testing_wait_limit_ns(50_000_000))
+    _lib.check(lib.dg_testing_debug_stop_producer(5))
+    try:
+        d = sentinel((G, cap, N), torch.bfloat16)
+        api.dg_m_grouped_fp8_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, 0, DG_SF_FP32, status)
+        torch.cuda.synchronize()
+    finally:
+        _lib.check(lib.dg_testing_debug_stop_producer(0))
+        _lib.check(lib.dg_testing_wait_limit_ns(0))
+    out["stall_status"] = np.array([int(status.item())], np.int32)
+    keep("after_stall", masked(4, 200, 512, 7168, [200, 77, 0, 130], DG_SF_FP32, 21))
     out["debug_build"] = np.array([int(api.dg_debug_build())], np.int32)
     torch.cuda.synchronize()
     np.savez(path, **out)

@@ -1,7 +1,8 @@
 """The debug build (libdg_debug.so, -DDG_DEBUG=1): its index checks raise no bit on in-bounds
 calls of every kernel family and leave every result bit-identical to the release build; a
 planted narrowing of the output rows (a test hook, no out-of-bounds access) raises DG_DEBUG_OUT
-and skips exactly the stores past it."""
+and skips exactly the stores past it; an injected producer stall (a load that is never issued, so
+a bounded wait runs out) returns DG_STATUS_TIMEOUT and leaves the next call clean."""
 import os
 import subprocess
 import sys
@@ -9,7 +10,7 @@ import sys
 import numpy as np
 import pytest
 
-from moe_grouped_fp8_gb300 import DG_DEBUG_OUT, build
+from moe_grouped_fp8_gb300 import DG_DEBUG_OUT, DG_STATUS_TIMEOUT, build
 
 pytestmark = pytest.mark.gpu
 
@@ -63,3 +64,13 @@ def test_planted_row_limit_is_flagged_and_skipped(results):
     full = rel["masked_short.0"].reshape(G, cap, N * 2)
     assert np.array_equal(d[0], full[0])
     assert np.all(d[1:] == 0xFF)
+
+
+def test_injected_producer_stall_times_out_cleanly(results):
+    rel, dbg = results
+    # release: the hook has no effect
+    assert int(rel["stall_status"][0]) == 0
+    # debug: the stalled CTA's waits ran out; the call returned and the next one is bit-identical
+    assert int(dbg["stall_status"][0]) & DG_STATUS_TIMEOUT
+    assert np.array_equal(dbg["after_stall.0"], rel["masked_long.0"])
+    assert np.array_equal(rel["after_stall.0"], rel["masked_long.0"])
