@@ -177,3 +177,31 @@ def test_fp4_needs_n_multiple_of_256():
     with pytest.raises(DGError) as e:
         api.dg_m_grouped_fp8_fp4_contiguous(qa, sfa, qb, sfb, d, torch.zeros(128, dtype=torch.int32, device="cuda"))
     assert e.value.code == DG_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_fp4_decode_shape_full_size_whole_expert():
+    """The decode shape with FP4 weights (G=32, cap=4096, N=6144, K=7168, Poisson(192) counts,
+    UE8M0 scales on both operands): one full-size launch; every valid row x every output column of
+    the largest expert against the oracle's FP4 GEMM, and every padding row untouched."""
+    w = wl.masked_decode()
+    G, cap, N, K = w.G, w.cap, w.N, w.K
+    a, b = w.draw(device="cuda")
+    cnt = torch.tensor(w.counts, device="cuda")
+    qa, sfa = gpu_quant_tokens(a.view(G * cap, K), DG_SF_UE8M0, row_counts=cnt)
+    qb, sfb = gpu_quant_fp4(b)
+    d = sentinel_like((G, cap, N), torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dg_m_grouped_fp8_fp4_masked(qa.view(G, cap, K), sfa, qb, sfb, d, cnt, 192, status)
+    sync()
+    assert status.item() == 0
+    rows = torch.arange(cap, device="cuda")[None, :]
+    assert bool((d.view(torch.int16)[rows >= cnt[:, None]] == -1).all()), "padding rows written"
+    g = int(np.argmax(w.counts))
+    c = int(w.counts[g])
+    oqb, oue = oracle.quant_block_128x128_fp4(b[g:g + 1].cpu())
+    np.testing.assert_array_equal(qb[g].cpu().numpy(), oqb[0])
+    oqa, osfa, _ = oracle.quant_per_token_1x128(a[g, :c].cpu(), ue8m0=True)
+    ref = oracle.gemm_masked_fp4(oqa.reshape(1, c, K), osfa.reshape(1, c, K // 128), oqb, oracle.ue8m0_value(oue),
+                                 [c])
+    assert_close(to_f64(d[g, :c]), ref_out(ref[0], False), False, f"fp4 decode expert {g} whole")
